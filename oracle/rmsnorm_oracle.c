@@ -1,0 +1,105 @@
+/*
+ * rmsnorm_oracle.c -- plain, slow, fp64 CPU reference for the row-wise
+ * RMSNorm hot path (fused residual-add forward and the VJP).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file or the library built from it: only the test suite, the
+ * smoke check and the CPU-baseline leg of the benchmark use it.  It shares no
+ * code, header, table or helper with the CUDA library.
+ *
+ * Every function works on double-precision copies of the (already quantised)
+ * fp16/bf16 inputs, so the only rounding here is fp64 rounding.  Loops run in
+ * the plain order the definitions state: rows ascending, columns ascending.
+ * No blocking, fusion or reordering.
+ *
+ * Sources (web pages; the page title and section are named):
+ *  - "Fused residual-add RMSNorm and fused RoPE + KV-append decode kernels"
+ *    (lablup/mlxcel issue 905), Background, FusedAddRMSNorm bullet:
+ *    residual' = input + residual; out = rmsnorm(residual') * (weight_bias +
+ *    weight); weight_bias = 1 is the Gemma (1 + w) convention, 0 the usual one.
+ *    Same page, Background, last paragraph: the kernel has two outputs
+ *    (normed, new_residual).
+ *  - "RMSNormVJP backward writes a full {n_rows, D} gw_temp intermediate"
+ *    (ml-explore/mlx pull request 4293), POC section: the eager reference
+ *    rsqrt(mean(x^2, last axis) + eps) * x * w, and the gradients (gx, gw) of
+ *    sum(rms_norm(x, w, eps) * y) with respect to x and w.  "Proposed changes":
+ *    gw is the sum over rows of each row's contribution.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+
+/*
+ * Forward.  For every row i (h = x + residual, or h = x when residual is
+ * NULL):
+ *     ms  = (1/D) * sum_j h_j^2           -- the mean over the last axis
+ *     r   = 1 / sqrt(ms + eps)             -- eps inside the root
+ *     out_j = h_j * r * (weight_bias + w_j)
+ *     new_residual_j = h_j                 -- only when residual is given
+ * x, residual, out, new_residual: rows*D, row-major.  w: D.
+ */
+void rmsnorm_oracle_fwd(const double *x, const double *residual,
+                        const double *w, double eps, double weight_bias,
+                        double *out, double *new_residual,
+                        int64_t rows, int64_t D)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        const double *xi = x + i * D;
+        const double *ri = residual ? residual + i * D : NULL;
+
+        double sumsq = 0.0;
+        for (int64_t j = 0; j < D; ++j) {
+            double h = ri ? xi[j] + ri[j] : xi[j];
+            sumsq += h * h;
+        }
+        double ms = sumsq / (double)D;
+        double r = 1.0 / sqrt(ms + eps);
+
+        for (int64_t j = 0; j < D; ++j) {
+            double h = ri ? xi[j] + ri[j] : xi[j];
+            out[i * D + j] = h * r * (weight_bias + w[j]);
+            if (new_residual)
+                new_residual[i * D + j] = h;
+        }
+    }
+}
+
+/*
+ * VJP of L = sum_ij g_ij * out_ij with respect to the normalised input h
+ * (= x here; for the fused op pass new_residual) and to w.  With
+ * w'_j = weight_bias + w_j and r, ms as in the forward, per row:
+ *     dr/dh_k   = -(r^3 / D) * h_k
+ *     dot       = sum_j g_j * w'_j * h_j
+ *     gx_k      = r * g_k * w'_k - (r^3 / D) * h_k * dot
+ *     gw_k     += g_k * h_k * r            (summed over rows, ascending)
+ * gw is overwritten (not accumulated into).
+ */
+void rmsnorm_oracle_vjp(const double *x, const double *w, const double *g,
+                        double eps, double weight_bias, double *gx, double *gw,
+                        int64_t rows, int64_t D)
+{
+    for (int64_t j = 0; j < D; ++j)
+        gw[j] = 0.0;
+
+    for (int64_t i = 0; i < rows; ++i) {
+        const double *hi = x + i * D;
+        const double *gi = g + i * D;
+
+        double sumsq = 0.0;
+        for (int64_t j = 0; j < D; ++j)
+            sumsq += hi[j] * hi[j];
+        double ms = sumsq / (double)D;
+        double r = 1.0 / sqrt(ms + eps);
+
+        double dot = 0.0;
+        for (int64_t j = 0; j < D; ++j)
+            dot += gi[j] * (weight_bias + w[j]) * hi[j];
+
+        double r3_over_d = r * r * r / (double)D;
+        for (int64_t j = 0; j < D; ++j) {
+            gx[i * D + j] = r * gi[j] * (weight_bias + w[j])
+                            - r3_over_d * hi[j] * dot;
+            gw[j] += gi[j] * hi[j] * r;
+        }
+    }
+}

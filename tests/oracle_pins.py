@@ -1,0 +1,276 @@
+"""Pins for the fp64 oracle: checks against what the pages and the mathematics
+fix, independent of the oracle's own code.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError on
+a mismatch.  ``test_oracle_pins.py`` runs them on the real oracle;
+``test_oracle_mutants.py`` runs them on deliberately broken copies of the
+oracle source and requires every copy to fail at least one pin.
+
+What each pin rests on:
+  * worked examples -- hand-derived exact values (tests/golden), from the
+    definitions on "Fused residual-add RMSNorm and fused RoPE + KV-append
+    decode kernels" (Background) and "RMSNormVJP backward writes a full
+    {n_rows, D} gw_temp intermediate" (POC);
+  * closed forms -- constant rows, D = 1, weight_bias = 1 with w = 0 against a
+    library norm (numpy.linalg.norm), gw as a row sum written with einsum;
+  * invariants -- scale invariance at eps = 0, the sum_j h_j gx_j identity,
+    linearity in g, row-permutation equivariance, scaled weight;
+  * central finite differences of L = sum(g * out) through the forward only.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                      "worked_examples.json")
+
+
+def _close(a, b, rtol, atol=0.0, what=""):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    assert a.shape == b.shape, "%s: shape %s vs %s" % (what, a.shape, b.shape)
+    ok = np.abs(a - b) <= atol + rtol * np.abs(b)
+    assert ok.all(), "%s: max |diff| %.3e (rtol %.1e)" % (
+        what, float(np.max(np.abs(a - b))), rtol)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def pin_worked_examples(orc):
+    """Hand-derived exact values (tests/golden/worked_examples.json)."""
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        x = np.array(c["x"], np.float64)
+        res = None if c["residual"] is None else np.array(c["residual"], np.float64)
+        w = np.array(c["w"], np.float64)
+        out, new_res = orc.fwd(x, w, c["eps"], c["weight_bias"], res)
+        _close(out, c["out"], 1e-14, 1e-15, c["name"] + " out")
+        if res is not None:
+            _close(new_res, c["new_residual"], 0, 0, c["name"] + " new_residual")
+        h = x if res is None else x + res
+        gx, gw = orc.vjp(h, w, np.array(c["g"], np.float64), c["eps"], c["weight_bias"])
+        _close(gx, c["gx"], 1e-14, 1e-15, c["name"] + " gx")
+        _close(gw, c["gw"], 1e-14, 1e-15, c["name"] + " gw")
+
+
+def pin_constant_rows(orc):
+    """A row of equal values c with w = 1, weight_bias = 0 normalises to
+    c / sqrt(c^2 + eps): +-1 up to eps."""
+    D = 37
+    for c in (3.0, -0.5, 1e-3, 250.0):
+        for eps in (0.0, 1e-6, 1e-2):
+            x = np.full((2, D), c)
+            out, _ = orc.fwd(x, np.ones(D), eps, 0.0)
+            want = c / np.sqrt(c * c + orc.scalar(eps))
+            _close(out, np.full((2, D), want), 1e-14, 0, "constant row c=%g eps=%g" % (c, eps))
+
+
+def pin_d1(orc):
+    """D = 1: out = h / sqrt(h^2 + eps) * (weight_bias + w)."""
+    h = np.array([[-3.0], [0.25], [7.5]])
+    for wb, w in ((0.0, 2.0), (1.0, -0.5)):
+        out, _ = orc.fwd(h, np.array([w]), 0.5, wb)
+        want = h / np.sqrt(h * h + 0.5) * (wb + w)
+        _close(out, want, 1e-14, 0, "D=1")
+
+
+def pin_unit_weight_bias_plain_norm(orc):
+    """weight_bias = 1 with w = 0 is plain normalisation, written here with a
+    library norm: h / sqrt(||h||^2 / D + eps)."""
+    rng = _rng(11)
+    for R, D in ((3, 16), (5, 129), (1, 1000)):
+        h = rng.normal(size=(R, D)) * rng.uniform(0.1, 10, size=(R, 1))
+        eps = 1e-3
+        out, _ = orc.fwd(h, np.zeros(D), eps, 1.0)
+        nrm = np.linalg.norm(h, axis=1, keepdims=True)
+        want = h / np.sqrt(nrm ** 2 / D + orc.scalar(eps))
+        _close(out, want, 1e-12, 0, "wb=1,w=0 R=%d D=%d" % (R, D))
+
+
+def pin_residual_is_added(orc):
+    """The fused forward equals the plain forward of x + residual, and
+    new_residual is exactly x + residual."""
+    rng = _rng(12)
+    R, D = 4, 33
+    x = rng.normal(size=(R, D))
+    res = rng.normal(size=(R, D))
+    w = rng.normal(1.0, 0.1, size=D)
+    out_f, new_res = orc.fwd(x, w, 1e-5, 0.25, res)
+    out_p, none = orc.fwd(x + res, w, 1e-5, 0.25)
+    assert none is None
+    _close(new_res, x + res, 0, 0, "new_residual")
+    _close(out_f, out_p, 1e-14, 0, "fused vs plain on x + residual")
+    # weight_bias enters as an additive bias on w
+    out_b, _ = orc.fwd(x + res, w + 0.25, 1e-5, 0.0)
+    _close(out_f, out_b, 1e-13, 0, "weight_bias shifts w")
+
+
+def pin_scale_invariance(orc):
+    """With eps = 0: out(a*h) = sign(a) * out(h), so by the chain rule
+    gx(a*h) = gx(h) / |a| and gw(a*h) = sign(a) * gw(h)."""
+    rng = _rng(13)
+    R, D = 3, 20
+    h = rng.normal(size=(R, D))
+    w = rng.normal(1.0, 0.3, size=D)
+    g = rng.normal(size=(R, D))
+    out0, _ = orc.fwd(h, w, 0.0, 0.5)
+    gx0, gw0 = orc.vjp(h, w, g, 0.0, 0.5)
+    for a in (3.75, -0.25, 1e3):
+        out1, _ = orc.fwd(a * h, w, 0.0, 0.5)
+        gx1, gw1 = orc.vjp(a * h, w, g, 0.0, 0.5)
+        _close(out1, np.sign(a) * out0, 1e-13, 1e-15, "out scale a=%g" % a)
+        _close(gx1 * abs(a), gx0, 1e-12, 1e-14, "gx scale a=%g" % a)
+        _close(gw1, np.sign(a) * gw0, 1e-12, 1e-14, "gw scale a=%g" % a)
+
+
+def pin_gw_row_sum(orc):
+    """gw_j = sum_i g_ij * h_ij * r_i with r_i from a library norm."""
+    rng = _rng(14)
+    R, D = 7, 24
+    h = rng.normal(size=(R, D))
+    w = rng.normal(size=D)
+    g = rng.normal(size=(R, D))
+    eps = 1e-4
+    _, gw = orc.vjp(h, w, g, eps, 0.75)
+    r = 1.0 / np.sqrt(np.linalg.norm(h, axis=1) ** 2 / D + orc.scalar(eps))
+    want = np.einsum("ij,ij,i->j", g, h, r)
+    _close(gw, want, 1e-12, 1e-14, "gw row sum")
+
+
+def _loss(orc, x, w, g, eps, wb, res=None):
+    out, _ = orc.fwd(x, w, eps, wb, res)
+    return float(np.sum(g * out))
+
+
+def pin_finite_differences(orc):
+    """Central differences of L = sum(g * out) through the forward only match
+    gx (with respect to x, and to residual in the fused op) and gw."""
+    rng = _rng(15)
+    for (R, D, eps, wb, with_res) in ((1, 1, 1e-2, 0.0, False), (2, 5, 1e-5, 0.0, True),
+                                      (3, 9, 1e-3, 1.0, False), (3, 8, 0.0, 0.5, True)):
+        x = rng.normal(size=(R, D))
+        res = rng.normal(size=(R, D)) if with_res else None
+        w = rng.normal(0.5, 0.5, size=D)
+        g = rng.normal(size=(R, D))
+        h = x if res is None else x + res
+        gx, gw = orc.vjp(h, w, g, eps, wb)
+        fd_x = np.zeros_like(x)
+        fd_res = np.zeros_like(x)
+        for i in range(R):
+            for j in range(D):
+                d = 1e-5 * (1.0 + abs(x[i, j]))
+                xp = x.copy(); xp[i, j] += d
+                xm = x.copy(); xm[i, j] -= d
+                fd_x[i, j] = (_loss(orc, xp, w, g, eps, wb, res)
+                              - _loss(orc, xm, w, g, eps, wb, res)) / (2 * d)
+                if res is not None:
+                    d = 1e-5 * (1.0 + abs(res[i, j]))
+                    rp = res.copy(); rp[i, j] += d
+                    rm = res.copy(); rm[i, j] -= d
+                    fd_res[i, j] = (_loss(orc, x, w, g, eps, wb, rp)
+                                    - _loss(orc, x, w, g, eps, wb, rm)) / (2 * d)
+        fd_w = np.zeros(D)
+        for j in range(D):
+            d = 1e-5 * (1.0 + abs(w[j]))
+            wp = w.copy(); wp[j] += d
+            wm = w.copy(); wm[j] -= d
+            fd_w[j] = (_loss(orc, x, wp, g, eps, wb, res)
+                       - _loss(orc, x, wm, g, eps, wb, res)) / (2 * d)
+        scale = max(1.0, float(np.max(np.abs(gx))))
+        _close(gx, fd_x, 1e-6, 1e-6 * scale, "fd gx R=%d D=%d" % (R, D))
+        if res is not None:
+            _close(gx, fd_res, 1e-6, 1e-6 * scale, "fd g_residual R=%d D=%d" % (R, D))
+        _close(gw, fd_w, 1e-6, 1e-6 * max(1.0, float(np.max(np.abs(gw)))),
+               "fd gw R=%d D=%d" % (R, D))
+
+
+def pin_h_dot_gx_identity(orc):
+    """sum_j h_j gx_j = r * eps / (ms + eps) * dot for every row (zero when
+    eps = 0: the output does not change under h -> (1 + t) h)."""
+    rng = _rng(16)
+    R, D = 5, 31
+    h = rng.normal(size=(R, D))
+    w = rng.normal(1.0, 0.2, size=D)
+    g = rng.normal(size=(R, D))
+    wb = orc.scalar(0.2)
+    for eps in (0.0, 0.3):
+        e = orc.scalar(eps)
+        gx, _ = orc.vjp(h, w, g, eps, wb)
+        ms = np.mean(h * h, axis=1)
+        r = 1.0 / np.sqrt(ms + e)
+        dot = np.sum(g * (wb + w) * h, axis=1)
+        lhs = np.sum(h * gx, axis=1)
+        _close(lhs, r * e / (ms + e) * dot, 1e-11, 1e-13, "identity eps=%g" % eps)
+
+
+def pin_linearity_in_g(orc):
+    """(gx, gw) is linear in g."""
+    rng = _rng(17)
+    R, D = 4, 12
+    h = rng.normal(size=(R, D))
+    w = rng.normal(size=D)
+    g1 = rng.normal(size=(R, D))
+    g2 = rng.normal(size=(R, D))
+    a, b = 2.5, -0.75
+    gx1, gw1 = orc.vjp(h, w, g1, 1e-3, 0.1)
+    gx2, gw2 = orc.vjp(h, w, g2, 1e-3, 0.1)
+    gx3, gw3 = orc.vjp(h, w, a * g1 + b * g2, 1e-3, 0.1)
+    _close(gx3, a * gx1 + b * gx2, 1e-12, 1e-13, "gx linear")
+    _close(gw3, a * gw1 + b * gw2, 1e-12, 1e-13, "gw linear")
+
+
+def pin_row_permutation(orc):
+    """Permuting rows permutes out and gx and leaves gw unchanged."""
+    rng = _rng(18)
+    R, D = 6, 10
+    h = rng.normal(size=(R, D)) * rng.uniform(0.5, 3, size=(R, 1))
+    w = rng.normal(size=D)
+    g = rng.normal(size=(R, D))
+    p = rng.permutation(R)
+    out, _ = orc.fwd(h, w, 1e-4, 0.0)
+    outp, _ = orc.fwd(h[p], w, 1e-4, 0.0)
+    _close(outp, out[p], 0, 0, "out permuted")
+    gx, gw = orc.vjp(h, w, g, 1e-4, 0.0)
+    gxp, gwp = orc.vjp(h[p], w, g[p], 1e-4, 0.0)
+    _close(gxp, gx[p], 0, 0, "gx permuted")
+    _close(gwp, gw, 1e-13, 1e-15, "gw invariant")
+
+
+def pin_scaled_weight(orc):
+    """With weight_bias = 0, scaling w by a scales out and gx by a (the
+    scaled-weight check of the regression-guard list)."""
+    rng = _rng(19)
+    R, D = 3, 14
+    h = rng.normal(size=(R, D))
+    w = rng.normal(1.0, 0.1, size=D)
+    g = rng.normal(size=(R, D))
+    a = 1.7
+    out, _ = orc.fwd(h, w, 1e-5, 0.0)
+    outa, _ = orc.fwd(h, a * w, 1e-5, 0.0)
+    _close(outa, a * out, 1e-13, 1e-15, "out scaled weight")
+    gx, gw = orc.vjp(h, w, g, 1e-5, 0.0)
+    gxa, gwa = orc.vjp(h, a * w, g, 1e-5, 0.0)
+    _close(gxa, a * gx, 1e-12, 1e-14, "gx scaled weight")
+    _close(gwa, gw, 1e-13, 1e-15, "gw does not depend on w")
+
+
+ALL_PINS = [
+    pin_worked_examples,
+    pin_constant_rows,
+    pin_d1,
+    pin_unit_weight_bias_plain_norm,
+    pin_residual_is_added,
+    pin_scale_invariance,
+    pin_gw_row_sum,
+    pin_finite_differences,
+    pin_h_dot_gx_identity,
+    pin_linearity_in_g,
+    pin_row_permutation,
+    pin_scaled_weight,
+]
