@@ -1,0 +1,180 @@
+/*
+ * rmsnorm.h -- C ABI of librmsnorm_gb300.so: the row-wise RMSNorm hot path on
+ * one GB300 (sm_103a).  Plain pointers and sizes only; no C++ or framework
+ * types cross this boundary.
+ *
+ * Operations (sources are web pages, named by title and section):
+ *
+ *   rmsnorm_fwd -- fused residual-add RMSNorm forward, two outputs.
+ *     "Fused residual-add RMSNorm and fused RoPE + KV-append decode kernels",
+ *     Background, FusedAddRMSNorm bullet: h = x + residual, then
+ *     out = h * rsqrt(mean(h^2) + eps) * (weight_bias + w) in one pass, the fp32
+ *     sum kept once, a warp-then-block sum of squares; weight_bias = 1 gives the
+ *     Gemma (1 + w) convention.  Same page, Background, last paragraph: the
+ *     residual update is a second output (normed, new_residual).
+ *
+ *   rmsnorm_vjp -- RMSNorm VJP: gx and a gw reduced across rows on the GPU.
+ *     "RMSNormVJP backward writes a full {n_rows, D} gw_temp intermediate",
+ *     Proposed changes: gw must not go through a {n_rows, D} temporary that a
+ *     second kernel re-reduces; rows are combined inside the kernel.  POC: the
+ *     gradients of sum(rms_norm(x, w, eps) * y) with respect to x and w.
+ *
+ * Definitions, per row of D elements (h = x + residual, or x):
+ *     ms = (1/D) sum_j h_j^2,  r = 1 / sqrt(ms + eps),  w'_j = weight_bias + w_j
+ *     out_j = h_j * r * w'_j,   new_residual_j = h_j
+ *     dot = sum_j g_j * w'_j * h_j
+ *     gx_j = r * g_j * w'_j - (r^3 / D) * h_j * dot
+ *     gw_j = sum over rows of g_j * h_j * r
+ *
+ * Numerics: inputs and outputs are fp16 or bf16; all arithmetic is fp32; every
+ * fp16/bf16 output element is rounded once, to nearest-even, from fp32.  h is
+ * normalised unrounded (the fp32 sum), new_residual is its rounding.  gw is
+ * fp32 and bit-identical from run to run on the same device for the same
+ * (rows, D, dtype): its summation order is fixed and does not depend on timing.
+ *
+ * Layout and ownership: every tensor is a dense row-major device buffer owned
+ * by the caller: x, residual, out, new_residual, g, gx are [rows, D] of dtype;
+ * w is [D] of dtype; gw is [D] fp32.  Pointers must be device pointers of the
+ * current device (cudaGetDevice) and `stream` a cudaStream_t of that device
+ * (NULL = legacy default stream), passed as void*.  Any alignment is accepted;
+ * 16-byte aligned pointers with D * 2 a multiple of 16 take the fast kernels.
+ *
+ * Aliasing: an output may be the very same buffer as an input of the same
+ * shape (out == x, new_residual == residual, gx == g, ...): every element is
+ * read before the same thread writes it.  Any other overlap, and any overlap
+ * of two outputs, is rejected with RMSNORM_ERR_INVALID_ARG.
+ *
+ * Asynchrony and errors: calls enqueue work on `stream` and return without
+ * synchronising.  Every call returns an rmsnorm_status_t and never aborts.
+ * Host-side validation fails before anything is enqueued.  A CUDA error at
+ * launch gives RMSNORM_ERR_CUDA; rmsnorm_last_cuda_error() then returns the
+ * cudaError_t of the calling thread's last failure.  A kernel whose bounded
+ * wait for its own asynchronous copies runs out (about a second) stops, leaves
+ * its outputs undefined and sets RMSNORM_DEVSTATUS_WAIT_TIMEOUT in the
+ * library's device status word, read by rmsnorm_device_status().
+ */
+#ifndef RMSNORM_GB300_H
+#define RMSNORM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RMSNORM_F16 = 0,  /* IEEE binary16 */
+    RMSNORM_BF16 = 1  /* bfloat16 */
+} rmsnorm_dtype_t;
+
+typedef enum {
+    RMSNORM_OK = 0,
+    RMSNORM_ERR_INVALID_ARG = 1,  /* null pointer, D <= 0, rows < 0, bad dtype,
+                                     eps < 0 or not finite, weight_bias not
+                                     finite, residual/new_residual mismatch,
+                                     overlapping buffers, too small workspace */
+    RMSNORM_ERR_UNSUPPORTED = 2,  /* D > RMSNORM_MAX_D, or rows * D overflows */
+    RMSNORM_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+    RMSNORM_ERR_NO_MEMORY = 4,    /* scratch allocation failed */
+    RMSNORM_ERR_TIMEOUT = 5       /* a device-side bounded wait ran out */
+} rmsnorm_status_t;
+
+/* Largest supported row length. */
+#define RMSNORM_MAX_D ((int64_t)1 << 24)
+
+/* Bits of the device status word. */
+#define RMSNORM_DEVSTATUS_WAIT_TIMEOUT 1u
+
+/*
+ * Fused residual-add RMSNorm forward.
+ *   x            [rows, D] dtype, input.
+ *   residual     [rows, D] dtype, or NULL for plain RMSNorm (h = x).
+ *   w            [D] dtype, weight.
+ *   eps          >= 0, added to the mean square inside the root.
+ *   weight_bias  scalar added to every w_j in fp32 (0: standard, 1: Gemma).
+ *   out          [rows, D] dtype, normalised output.
+ *   new_residual [rows, D] dtype, receives round(x + residual); must be NULL
+ *                exactly when residual is NULL.
+ * rows == 0 is a no-op returning RMSNORM_OK.
+ */
+int rmsnorm_fwd(const void *x, const void *residual, const void *w, float eps,
+                float weight_bias, void *out, void *new_residual, int64_t rows,
+                int64_t D, int dtype, void *stream);
+
+/*
+ * RMSNorm VJP.
+ *   x   [rows, D] dtype, the tensor that was normalised (for the fused
+ *       forward pass its new_residual; the gradient with respect to both x and
+ *       residual of the fused op is then gx plus whatever gradient reaches
+ *       new_residual, which the caller adds).
+ *   w   [D] dtype;  g [rows, D] dtype, the incoming gradient of out.
+ *   gx  [rows, D] dtype, gradient with respect to x.
+ *   gw  [D] fp32, gradient with respect to w, summed over rows; overwritten
+ *       (rows == 0 writes zeros).
+ * The per-CTA gw partials ([P, D] fp32 with P about the SM count) live in
+ * scratch that this call takes and returns stream-ordered on `stream` from a
+ * memory pool the library keeps per device (cudaMallocFromPoolAsync /
+ * cudaFreeAsync; the pool holds on to freed memory for the next call);
+ * allocation failure returns RMSNORM_ERR_NO_MEMORY.  No [rows, D] temporary
+ * is ever allocated.
+ */
+int rmsnorm_vjp(const void *x, const void *w, const void *g, float eps,
+                float weight_bias, void *gx, float *gw, int64_t rows, int64_t D,
+                int dtype, void *stream);
+
+/*
+ * Bytes of scratch rmsnorm_vjp_ws needs for this problem on the current
+ * device (0 when rows == 0).  Returns 0 for invalid arguments as well.
+ */
+size_t rmsnorm_vjp_workspace_size(int64_t rows, int64_t D, int dtype);
+
+/*
+ * rmsnorm_vjp with caller-owned scratch: `workspace` is a device buffer of at
+ * least rmsnorm_vjp_workspace_size(rows, D, dtype) bytes, 256-byte aligned.
+ * Its contents on entry do not matter; it must not be used by other work while
+ * this call runs on `stream`.
+ */
+int rmsnorm_vjp_ws(const void *x, const void *w, const void *g, float eps,
+                   float weight_bias, void *gx, float *gw, int64_t rows,
+                   int64_t D, int dtype, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *rmsnorm_status_string(int status);
+
+/* cudaError_t of the calling thread's last RMSNORM_ERR_CUDA (0 if none). */
+int rmsnorm_last_cuda_error(void);
+
+/*
+ * Reads the device status word of the current device into *bits (a mask of
+ * RMSNORM_DEVSTATUS_* flags set by kernels since the last clear) and clears it
+ * when `clear` is non-zero.  Synchronises the device: diagnostics only.
+ * Returns RMSNORM_ERR_TIMEOUT when the timeout bit is set.
+ */
+int rmsnorm_device_status(unsigned int *bits, int clear);
+
+/*
+ * Test hook for the timeout path.  Until reset with (-1, 0), the staged
+ * kernels launched by the calling process skip the asynchronous copy of the
+ * tile with index `drop_tile` (so its wait can never finish) and give every
+ * wait `budget_cycles` SM clock cycles instead of the default.  The kernel then
+ * reports RMSNORM_DEVSTATUS_WAIT_TIMEOUT, drains its other copies and exits;
+ * no fault, trap or hang.  budget_cycles <= 0 restores the default budget.
+ */
+int rmsnorm_debug_inject(int64_t drop_tile, int64_t budget_cycles);
+
+/*
+ * Describes the kernel plan rmsnorm_fwd (op = 0) or rmsnorm_vjp (op = 1)
+ * would use for this problem and pointer alignment on the current device, as a
+ * static string such as "staged:cfg8:nt512:g512:v2:s6:tr1:grid152:smem..."; for
+ * tests and benchmarks.
+ */
+const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype,
+                                      int has_residual, int aligned);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_GB300_H */

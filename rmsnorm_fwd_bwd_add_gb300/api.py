@@ -1,0 +1,177 @@
+"""Python front end of the C ABI: same names, argument marshalling only.
+
+Every function checks dtype, device, contiguity and shape, then passes raw
+pointers and the current CUDA stream to librmsnorm_gb300.so.  All arithmetic
+runs in the library's CUDA kernels; nothing here computes.
+
+Tensors: x, residual, g are [..., D] fp16 or bf16 CUDA tensors, contiguous;
+w is [D] of the same dtype; gw is [D] fp32.  Leading dimensions are flattened
+into rows.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from . import _native
+
+_DTYPES = {torch.float16: 0, torch.bfloat16: 1}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError("unsupported dtype %s (fp16 or bf16)" % t.dtype) from None
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else (t.data_ptr() or None)
+
+
+def _check_like(name: str, t: torch.Tensor, ref: torch.Tensor) -> None:
+    if t.dtype != ref.dtype or t.device != ref.device:
+        raise ValueError("%s must be %s on %s" % (name, ref.dtype, ref.device))
+    if t.shape != ref.shape:
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(ref.shape), tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _rows_d(x: torch.Tensor) -> Tuple[int, int]:
+    if x.dim() < 1:
+        raise ValueError("x must have at least one dimension")
+    if not x.is_cuda:
+        raise ValueError("tensors must be CUDA tensors (there is no CPU path)")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    D = x.shape[-1]
+    return (x.numel() // D if D else 0), D
+
+
+def _stream(device: torch.device, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def _check_w(w: torch.Tensor, x: torch.Tensor, D: int) -> None:
+    if w.dtype != x.dtype or w.device != x.device or w.shape != (D,) or not w.is_contiguous():
+        raise ValueError("w must be a contiguous [%d] %s tensor on %s" % (D, x.dtype, x.device))
+
+
+def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, weight_bias: float = 0.0,
+                residual: Optional[torch.Tensor] = None, *, out: Optional[torch.Tensor] = None,
+                new_residual: Optional[torch.Tensor] = None, stream=None):
+    """Fused residual-add RMSNorm forward.  Returns (out, new_residual);
+    new_residual is None when residual is None.  Pass out=x or
+    new_residual=residual to update in place."""
+    rows, D = _rows_d(x)
+    code = _dtype_code(x)
+    _check_w(w, x, D)
+    if residual is not None:
+        _check_like("residual", residual, x)
+    if out is None:
+        out = torch.empty_like(x)
+    _check_like("out", out, x)
+    if residual is not None:
+        if new_residual is None:
+            new_residual = torch.empty_like(x)
+        _check_like("new_residual", new_residual, x)
+    elif new_residual is not None:
+        raise ValueError("new_residual given without residual")
+    with torch.cuda.device(x.device):
+        st = _native.lib().rmsnorm_fwd(_ptr(x), _ptr(residual), _ptr(w), eps, weight_bias,
+                                       _ptr(out), _ptr(new_residual), rows, D, code,
+                                       _stream(x.device, stream))
+    _native.check("rmsnorm_fwd", st)
+    return out, new_residual
+
+
+def _vjp_outputs(x, g, gx, gw, D):
+    _check_like("g", g, x)
+    if gx is None:
+        gx = torch.empty_like(x)
+    _check_like("gx", gx, x)
+    if gw is None:
+        gw = torch.empty(D, dtype=torch.float32, device=x.device)
+    if (gw.dtype != torch.float32 or gw.shape != (D,) or gw.device != x.device
+            or not gw.is_contiguous()):
+        raise ValueError("gw must be a contiguous [%d] float32 tensor on %s" % (D, x.device))
+    return gx, gw
+
+
+def rmsnorm_vjp(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float,
+                weight_bias: float = 0.0, *, gx: Optional[torch.Tensor] = None,
+                gw: Optional[torch.Tensor] = None, stream=None):
+    """RMSNorm VJP.  Returns (gx, gw) with gw fp32, reduced across rows on the
+    GPU.  The library takes its gw scratch from its own stream-ordered pool."""
+    rows, D = _rows_d(x)
+    code = _dtype_code(x)
+    _check_w(w, x, D)
+    gx, gw = _vjp_outputs(x, g, gx, gw, D)
+    with torch.cuda.device(x.device):
+        st = _native.lib().rmsnorm_vjp(_ptr(x), _ptr(w), _ptr(g), eps, weight_bias, _ptr(gx),
+                                       _ptr(gw), rows, D, code, _stream(x.device, stream))
+    _native.check("rmsnorm_vjp", st)
+    return gx, gw
+
+
+def rmsnorm_vjp_workspace_size(rows: int, D: int, dtype: torch.dtype) -> int:
+    """Bytes of scratch rmsnorm_vjp_ws needs on the current device."""
+    return int(_native.lib().rmsnorm_vjp_workspace_size(rows, D, _DTYPES[dtype]))
+
+
+def rmsnorm_vjp_ws(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float,
+                   weight_bias: float = 0.0, *, workspace: Optional[torch.Tensor] = None,
+                   gx: Optional[torch.Tensor] = None, gw: Optional[torch.Tensor] = None,
+                   stream=None):
+    """rmsnorm_vjp with caller-owned scratch (a uint8 CUDA tensor of at least
+    rmsnorm_vjp_workspace_size bytes; allocated here through torch when not
+    given)."""
+    rows, D = _rows_d(x)
+    code = _dtype_code(x)
+    _check_w(w, x, D)
+    gx, gw = _vjp_outputs(x, g, gx, gw, D)
+    with torch.cuda.device(x.device):
+        if workspace is None:
+            nbytes = rmsnorm_vjp_workspace_size(rows, D, x.dtype)
+            workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=x.device)
+        if workspace.device != x.device or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on %s" % x.device)
+        nbytes = workspace.numel() * workspace.element_size()
+        st = _native.lib().rmsnorm_vjp_ws(_ptr(x), _ptr(w), _ptr(g), eps, weight_bias,
+                                          _ptr(gx), _ptr(gw), rows, D, code, _ptr(workspace),
+                                          nbytes, _stream(x.device, stream))
+    _native.check("rmsnorm_vjp_ws", st)
+    return gx, gw
+
+
+def rmsnorm_device_status(clear: bool = True) -> int:
+    """Device status bits of the current device (synchronises)."""
+    bits = ctypes.c_uint(0)
+    st = _native.lib().rmsnorm_device_status(ctypes.byref(bits), 1 if clear else 0)
+    if st not in (0, 5):
+        _native.check("rmsnorm_device_status", st)
+    return int(bits.value)
+
+
+def rmsnorm_debug_inject(drop_tile: int = -1, budget_cycles: int = 0) -> None:
+    """Test hook: drop one staged tile's copy and shorten the wait budget
+    ((-1, 0) restores normal operation)."""
+    _native.check("rmsnorm_debug_inject",
+                  _native.lib().rmsnorm_debug_inject(drop_tile, budget_cycles))
+
+
+def rmsnorm_describe_dispatch(op: str, rows: int, D: int, dtype: torch.dtype,
+                              has_residual: bool = False, aligned: bool = True) -> str:
+    """The kernel plan the library would choose ('fwd' or 'vjp')."""
+    s = _native.lib().rmsnorm_describe_dispatch(1 if op == "vjp" else 0, rows, D, _DTYPES[dtype],
+                                                1 if has_residual else 0, 1 if aligned else 0)
+    return s.decode()
+
+
+def rmsnorm_status_string(status: int) -> str:
+    return _native.lib().rmsnorm_status_string(status).decode()

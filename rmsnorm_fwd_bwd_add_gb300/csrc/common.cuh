@@ -1,0 +1,164 @@
+// common.cuh -- device helpers shared by the RMSNorm kernels (sm_103a).
+//
+// 16-byte vectors of eight fp16/bf16 values, fp32 conversion with
+// round-to-nearest-even, warp sums in a fixed order, and inline-PTX wrappers
+// for mbarriers and the 1-D TMA bulk copy (cp.async.bulk) that stages rows
+// into shared memory.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+namespace rmsn {
+
+// Kernel modes.
+enum : int { MODE_FWD_RES = 0, MODE_FWD_NORES = 1, MODE_VJP = 2 };
+
+// Bits of the device status word (must match RMSNORM_DEVSTATUS_* in rmsnorm.h).
+constexpr unsigned int DEVSTATUS_WAIT_TIMEOUT = 1u;
+
+// Default budget of one bounded wait, in SM clock cycles (about a second at
+// the GB300's ~2 GHz SM clock).
+constexpr long long DEFAULT_WAIT_BUDGET = 2000000000LL;
+
+// ---------------------------------------------------------------------------
+// fp16 / bf16 <-> fp32.  Eight 16-bit values travel as one uint4.
+// ---------------------------------------------------------------------------
+template <typename T> struct Cvt;
+
+template <> struct Cvt<__half> {
+    static __device__ __forceinline__ float2 unpack2(uint32_t u) {
+        __half2 h;
+        memcpy(&h, &u, 4);
+        return __half22float2(h);
+    }
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);  // each rounded to nearest even
+        uint32_t u;
+        memcpy(&u, &h, 4);
+        return u;
+    }
+    static __device__ __forceinline__ float load1(const __half *p) { return __half2float(*p); }
+    static __device__ __forceinline__ void store1(__half *p, float v) { *p = __float2half_rn(v); }
+};
+
+template <> struct Cvt<__nv_bfloat16> {
+    static __device__ __forceinline__ float2 unpack2(uint32_t u) {
+        __nv_bfloat162 h;
+        memcpy(&h, &u, 4);
+        return __bfloat1622float2(h);
+    }
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // each rounded to nearest even
+        uint32_t u;
+        memcpy(&u, &h, 4);
+        return u;
+    }
+    static __device__ __forceinline__ float load1(const __nv_bfloat16 *p) {
+        return __bfloat162float(*p);
+    }
+    static __device__ __forceinline__ void store1(__nv_bfloat16 *p, float v) {
+        *p = __float2bfloat16_rn(v);
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4 &v, float f[8]) {
+    float2 a = Cvt<T>::unpack2(v.x), b = Cvt<T>::unpack2(v.y);
+    float2 c = Cvt<T>::unpack2(v.z), d = Cvt<T>::unpack2(v.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack8(const float f[8]) {
+    uint4 v;
+    v.x = Cvt<T>::pack2(f[0], f[1]);
+    v.y = Cvt<T>::pack2(f[2], f[3]);
+    v.z = Cvt<T>::pack2(f[4], f[5]);
+    v.w = Cvt<T>::pack2(f[6], f[7]);
+    return v;
+}
+
+// Streaming 16-byte global load (evict-first: every byte is read once) and a
+// plain 16-byte store.
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_global(uint4 *p, const uint4 &v) { *p = v; }
+
+// ---------------------------------------------------------------------------
+// Sums in a fixed order.  The xor butterfly leaves the same bits in every
+// lane (each step adds the same two operands in both lanes of a pair).
+// ---------------------------------------------------------------------------
+template <int WIDTH>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int off = WIDTH / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + 1-D TMA bulk copy (inline PTX).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the phase of `bar` with the given parity to complete; gives up
+// after `budget` SM clock cycles and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long budget) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > budget) return false;
+    }
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned), completing `bytes` transactions on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+}  // namespace rmsn

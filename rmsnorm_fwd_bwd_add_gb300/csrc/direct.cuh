@@ -1,0 +1,155 @@
+// direct.cuh -- RMSNorm kernels that load rows straight into registers, one
+// CTA per row (grid-stride over rows).
+//
+// Used for decode-sized problems (a few rows, where a staging ring has
+// nothing to overlap and latency is all that matters: every thread issues its
+// 16-byte loads at once) and for aligned rows too long for the shared-memory
+// ring.  Each thread owns V vectors of 8 elements of the row (fixed across
+// rows); the sum of squares is a warp shuffle tree plus the warp totals added
+// in warp order through shared memory.  The VJP keeps its gw contributions in
+// registers and writes one partial row per CTA.
+//
+// Sources: "Fused residual-add RMSNorm and fused RoPE + KV-append decode
+// kernels", Background (FusedAddRMSNorm; the decode loop runs it once per
+// token); "RMSNormVJP backward writes a full {n_rows, D} gw_temp
+// intermediate", Proposed changes (gw reduced inside the kernel).
+#pragma once
+
+#include "common.cuh"
+#include "plan.h"
+
+namespace rmsn {
+
+template <typename T, int MODE, int NT, int V>
+__global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
+    constexpr int NWARPS = NT / 32;
+    constexpr int NTENS = (MODE == MODE_FWD_NORES) ? 1 : 2;
+    constexpr bool VJP = (MODE == MODE_VJP);
+    __shared__ float red[2][NWARPS][2];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int D = a.D;
+    const int NV = D >> 3;
+    const float eps = a.eps;
+    const float wb = a.weight_bias;
+    const float Df = (float)D;
+    const uint4 *in0 = static_cast<const uint4 *>(a.in0);
+    const uint4 *in1 = static_cast<const uint4 *>(a.in1);
+    const uint4 *wg = static_cast<const uint4 *>(a.w);
+    uint4 *out0 = static_cast<uint4 *>(a.out0);
+    uint4 *out1 = static_cast<uint4 *>(a.out1);
+
+    float acc[VJP ? V : 1][8];
+#pragma unroll
+    for (int j = 0; j < (VJP ? V : 1); ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+
+    int it = 0;
+    for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, ++it) {
+        const size_t base = (size_t)row * NV;
+        uint4 v0[V], v1[V];
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int vi = tid + j * NT;
+            if (vi < NV) {
+                v0[j] = ld_stream(in0 + base + vi);
+                if constexpr (NTENS == 2) v1[j] = ld_stream(in1 + base + vi);
+            }
+        }
+        float sa = 0.f, sb = 0.f;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int vi = tid + j * NT;
+            if (vi < NV) {
+                float f0[8];
+                unpack8<T>(v0[j], f0);
+                if constexpr (MODE == MODE_FWD_RES) {
+                    float f1[8];
+                    unpack8<T>(v1[j], f1);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float h = f0[e] + f1[e];
+                        sa += h * h;
+                    }
+                } else if constexpr (MODE == MODE_FWD_NORES) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) sa += f0[e] * f0[e];
+                } else {
+                    float f1[8], wf[8];
+                    unpack8<T>(v1[j], f1);
+                    unpack8<T>(__ldg(wg + vi), wf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        sa += f0[e] * f0[e];
+                        sb += (f1[e] * (wb + wf[e])) * f0[e];
+                    }
+                }
+            }
+        }
+        sa = group_sum<32>(sa);
+        if constexpr (VJP) sb = group_sum<32>(sb);
+        if (lane == 0) {
+            red[it & 1][warp][0] = sa;
+            red[it & 1][warp][1] = sb;
+        }
+        __syncthreads();
+        float ss = 0.f, dot = 0.f;
+#pragma unroll
+        for (int w = 0; w < NWARPS; ++w) {
+            ss += red[it & 1][w][0];
+            if constexpr (VJP) dot += red[it & 1][w][1];
+        }
+        const float r = rsqrtf(ss / Df + eps);
+        const float c = (r * r) * (dot / Df);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int vi = tid + j * NT;
+            if (vi < NV) {
+                float f0[8], wf[8], o[8];
+                unpack8<T>(v0[j], f0);
+                unpack8<T>(__ldg(wg + vi), wf);
+                if constexpr (MODE == MODE_FWD_RES) {
+                    float f1[8];
+                    unpack8<T>(v1[j], f1);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        f0[e] = f0[e] + f1[e];
+                        o[e] = (f0[e] * r) * (wb + wf[e]);
+                    }
+                    st_global(out1 + base + vi, pack8<T>(f0));
+                } else if constexpr (MODE == MODE_FWD_NORES) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = (f0[e] * r) * (wb + wf[e]);
+                } else {
+                    float f1[8];
+                    unpack8<T>(v1[j], f1);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float gwp = f1[e] * (wb + wf[e]);
+                        o[e] = r * (gwp - f0[e] * c);
+                        acc[j][e] += (f1[e] * f0[e]) * r;
+                    }
+                }
+                st_global(out0 + base + vi, pack8<T>(o));
+            }
+        }
+    }
+
+    if constexpr (VJP) {
+        float *prow = a.partials + (size_t)blockIdx.x * D;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int vi = tid + j * NT;
+            if (vi < NV) {
+                float4 *dst = reinterpret_cast<float4 *>(prow + (size_t)vi * 8);
+                dst[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+                dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+            }
+        }
+    }
+}
+
+}  // namespace rmsn

@@ -1,0 +1,81 @@
+// direct_generic.cu -- launchers for the direct and generic tiers, the gw
+// stage-2 reduction, and the dtype switch of the staged tier.
+#include "direct.cuh"
+#include "generic.cuh"
+
+namespace rmsn {
+
+cudaError_t launch_staged_f16(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
+cudaError_t launch_staged_bf16(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
+
+cudaError_t launch_staged(int dtype, int mode, const Plan &p, const KernelArgs &a,
+                          cudaStream_t s) {
+    return dtype == 0 ? launch_staged_f16(mode, p, a, s) : launch_staged_bf16(mode, p, a, s);
+}
+
+namespace {
+
+template <typename T, int MODE, int NT, int V>
+cudaError_t direct_one(const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    direct_kernel<T, MODE, NT, V><<<p.grid, NT, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int MODE>
+cudaError_t direct_mode(const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    static_assert(N_DIRECT_CFG == 6, "keep this switch in step with DIRECT_CFGS");
+    switch (p.cfg) {
+        case 0: return direct_one<T, MODE, 128, 1>(p, a, s);
+        case 1: return direct_one<T, MODE, 256, 1>(p, a, s);
+        case 2: return direct_one<T, MODE, 512, 1>(p, a, s);
+        case 3: return direct_one<T, MODE, 1024, 1>(p, a, s);
+        case 4: return direct_one<T, MODE, 1024, 2>(p, a, s);
+        case 5:
+            // Four vectors of x and g per thread plus gw accumulators do not
+            // fit 1024 threads' registers; the VJP never plans this config.
+            if constexpr (MODE == MODE_VJP) return cudaErrorInvalidValue;
+            else return direct_one<T, MODE, 1024, 4>(p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t direct_t(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    switch (mode) {
+        case MODE_FWD_RES: return direct_mode<T, MODE_FWD_RES>(p, a, s);
+        case MODE_FWD_NORES: return direct_mode<T, MODE_FWD_NORES>(p, a, s);
+        case MODE_VJP: return direct_mode<T, MODE_VJP>(p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t generic_t(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    switch (mode) {
+        case MODE_FWD_RES: generic_kernel<T, MODE_FWD_RES><<<p.grid, GENERIC_NT, 0, s>>>(a); break;
+        case MODE_FWD_NORES: generic_kernel<T, MODE_FWD_NORES><<<p.grid, GENERIC_NT, 0, s>>>(a); break;
+        case MODE_VJP: generic_kernel<T, MODE_VJP><<<p.grid, GENERIC_NT, 0, s>>>(a); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_direct(int dtype, int mode, const Plan &p, const KernelArgs &a,
+                          cudaStream_t s) {
+    return dtype == 0 ? direct_t<__half>(mode, p, a, s) : direct_t<__nv_bfloat16>(mode, p, a, s);
+}
+
+cudaError_t launch_generic(int dtype, int mode, const Plan &p, const KernelArgs &a,
+                           cudaStream_t s) {
+    return dtype == 0 ? generic_t<__half>(mode, p, a, s) : generic_t<__nv_bfloat16>(mode, p, a, s);
+}
+
+cudaError_t launch_gw_reduce(const float *partials, float *gw, int P, int D, cudaStream_t s) {
+    const unsigned int blocks = (unsigned int)((D + 31) / 32);
+    gw_reduce_kernel<<<blocks, 256, 0, s>>>(partials, gw, P, D);
+    return cudaGetLastError();
+}
+
+}  // namespace rmsn

@@ -1,0 +1,121 @@
+// generic.cuh -- element-at-a-time RMSNorm kernels for any D and any
+// alignment (rows whose start is not 16-byte aligned, D not a multiple of 8,
+// or rows longer than the vectorised tiers take), and the gw stage-2 sum.
+//
+// One CTA per row, grid-stride; pass 1 forms the sums, pass 2 re-reads the row
+// (from L1/L2) and writes the outputs.  The VJP accumulates each CTA's gw
+// contributions in that CTA's own row of the partials buffer; thread t owns
+// columns t, t + NT, ..., so no two threads ever touch the same partial and
+// the order is fixed.
+//
+// Sources: as for the vectorised tiers ("Fused residual-add RMSNorm and fused
+// RoPE + KV-append decode kernels", Background; "RMSNormVJP backward writes a
+// full {n_rows, D} gw_temp intermediate", Proposed changes).
+#pragma once
+
+#include "common.cuh"
+#include "plan.h"
+
+namespace rmsn {
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a) {
+    constexpr int NT = GENERIC_NT;
+    constexpr int NWARPS = NT / 32;
+    constexpr bool VJP = (MODE == MODE_VJP);
+    __shared__ float red[2][NWARPS][2];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int D = a.D;
+    const float eps = a.eps;
+    const float wb = a.weight_bias;
+    const float Df = (float)D;
+    const T *in0 = static_cast<const T *>(a.in0);
+    const T *in1 = static_cast<const T *>(a.in1);
+    const T *w = static_cast<const T *>(a.w);
+    T *out0 = static_cast<T *>(a.out0);
+    T *out1 = static_cast<T *>(a.out1);
+    float *prow = VJP ? a.partials + (size_t)blockIdx.x * D : nullptr;
+
+    if constexpr (VJP)
+        for (int c = tid; c < D; c += NT) prow[c] = 0.f;
+
+    int it = 0;
+    for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, ++it) {
+        const size_t base = (size_t)row * D;
+        float sa = 0.f, sb = 0.f;
+        for (int c = tid; c < D; c += NT) {
+            const float x = Cvt<T>::load1(in0 + base + c);
+            if constexpr (MODE == MODE_FWD_RES) {
+                const float h = x + Cvt<T>::load1(in1 + base + c);
+                sa += h * h;
+            } else if constexpr (MODE == MODE_FWD_NORES) {
+                sa += x * x;
+            } else {
+                const float g = Cvt<T>::load1(in1 + base + c);
+                sa += x * x;
+                sb += (g * (wb + Cvt<T>::load1(w + c))) * x;
+            }
+        }
+        sa = group_sum<32>(sa);
+        if constexpr (VJP) sb = group_sum<32>(sb);
+        if (lane == 0) {
+            red[it & 1][warp][0] = sa;
+            red[it & 1][warp][1] = sb;
+        }
+        __syncthreads();
+        float ss = 0.f, dot = 0.f;
+#pragma unroll
+        for (int k = 0; k < NWARPS; ++k) {
+            ss += red[it & 1][k][0];
+            if constexpr (VJP) dot += red[it & 1][k][1];
+        }
+        const float r = rsqrtf(ss / Df + eps);
+        const float cc = (r * r) * (dot / Df);
+        for (int c = tid; c < D; c += NT) {
+            const float x = Cvt<T>::load1(in0 + base + c);
+            const float wp = wb + Cvt<T>::load1(w + c);
+            if constexpr (MODE == MODE_FWD_RES) {
+                const float h = x + Cvt<T>::load1(in1 + base + c);
+                Cvt<T>::store1(out1 + base + c, h);
+                Cvt<T>::store1(out0 + base + c, (h * r) * wp);
+            } else if constexpr (MODE == MODE_FWD_NORES) {
+                Cvt<T>::store1(out0 + base + c, (x * r) * wp);
+            } else {
+                const float g = Cvt<T>::load1(in1 + base + c);
+                Cvt<T>::store1(out0 + base + c, r * (g * wp - x * cc));
+                prow[c] += (g * x) * r;
+            }
+        }
+    }
+}
+
+// Stage 2 of gw: gw[c] = sum over p of partials[p, c].  A CTA covers 32
+// columns; its 8 warps each add a contiguous eighth of the P partial rows in
+// ascending order, then warp 0 adds the eight results in warp order.  The
+// order depends only on (P, D), never on timing.
+__global__ void __launch_bounds__(256) gw_reduce_kernel(const float *__restrict__ partials,
+                                                        float *__restrict__ gw, int P, int D) {
+    __shared__ float part[8][33];
+    const int tx = threadIdx.x & 31;
+    const int ty = threadIdx.x >> 5;
+    const int64_t col = (int64_t)blockIdx.x * 32 + tx;
+    const int per = (P + 7) / 8;
+    const int p0 = ty * per;
+    const int p1 = min(P, p0 + per);
+    float s = 0.f;
+    if (col < D)
+        for (int p = p0; p < p1; ++p) s += partials[(size_t)p * D + col];
+    part[ty][tx] = s;
+    __syncthreads();
+    if (ty == 0 && col < D) {
+        float t = part[0][tx];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) t += part[k][tx];
+        gw[col] = t;
+    }
+}
+
+}  // namespace rmsn

@@ -1,0 +1,49 @@
+// launch_staged.cuh -- picks the staged_kernel instance for a plan.
+#pragma once
+
+#include "launch_util.h"
+#include "staged.cuh"
+
+namespace rmsn {
+
+template <typename T, int MODE, int NT, int G, int V>
+cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
+    // Up to 512 threads: registers capped so that two CTAs fit on one SM.
+    constexpr int MINB = NT <= 512 ? 2 : 1;
+    static std::atomic<uint64_t> smem_mask{0};
+    auto kern = staged_kernel<T, MODE, NT, G, V, MINB>;
+    cudaError_t e = allow_max_dynamic_smem((const void *)kern, smem_mask);
+    if (e != cudaSuccess) return e;
+    kern<<<p.grid, NT, p.smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int MODE>
+cudaError_t launch_staged_mode(const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    static_assert(N_STAGED_CFG == 10, "keep this switch in step with STAGED_CFGS");
+    switch (p.cfg) {
+        case 0: return launch_staged_one<T, MODE, 256, 8, 1>(p, a, s);
+        case 1: return launch_staged_one<T, MODE, 256, 16, 1>(p, a, s);
+        case 2: return launch_staged_one<T, MODE, 256, 32, 1>(p, a, s);
+        case 3: return launch_staged_one<T, MODE, 256, 32, 2>(p, a, s);
+        case 4: return launch_staged_one<T, MODE, 256, 32, 3>(p, a, s);
+        case 5: return launch_staged_one<T, MODE, 256, 32, 4>(p, a, s);
+        case 6: return launch_staged_one<T, MODE, 128, 128, 2>(p, a, s);
+        case 7: return launch_staged_one<T, MODE, 256, 256, 2>(p, a, s);
+        case 8: return launch_staged_one<T, MODE, 512, 512, 2>(p, a, s);
+        case 9: return launch_staged_one<T, MODE, 1024, 1024, 2>(p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t launch_staged_t(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    switch (mode) {
+        case MODE_FWD_RES: return launch_staged_mode<T, MODE_FWD_RES>(p, a, s);
+        case MODE_FWD_NORES: return launch_staged_mode<T, MODE_FWD_NORES>(p, a, s);
+        case MODE_VJP: return launch_staged_mode<T, MODE_VJP>(p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rmsn

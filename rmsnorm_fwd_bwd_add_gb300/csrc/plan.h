@@ -1,0 +1,81 @@
+// plan.h -- launch plans and kernel parameters shared by the host dispatcher
+// (api.cu) and the per-tier launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rmsn {
+
+enum Tier : int { TIER_STAGED = 0, TIER_DIRECT = 1, TIER_GENERIC = 2 };
+
+// Kernel arguments.  in0 = x; in1 = residual (forward) or g (VJP);
+// out0 = out (forward) or gx (VJP); out1 = new_residual (forward).
+struct KernelArgs {
+    const void *in0;
+    const void *in1;
+    const void *w;
+    void *out0;
+    void *out1;
+    float *partials;          // VJP: [grid, D] fp32 gw partials, one row per CTA
+    unsigned int *status;     // device status word
+    float eps;
+    float weight_bias;
+    int64_t rows;
+    int D;
+    // staged tier
+    int tile_rows;            // rows per tile (one bulk copy per tensor)
+    int stages;               // shared-memory ring depth
+    int64_t num_tiles;
+    uint32_t stage_bytes;     // bytes of one full tile of one tensor
+    long long wait_budget;    // SM cycles per bounded wait
+    int64_t drop_tile;        // test hook: tile whose copy is never issued (-1: none)
+};
+
+struct Plan {
+    int tier;
+    int cfg;           // index into the tier's configuration table
+    int nt;            // threads per CTA
+    int g;             // threads per row
+    int v;             // 16-byte vectors per thread per row
+    int stages;
+    int tile_rows;
+    int64_t num_tiles;
+    int grid;          // CTAs; for the VJP also the number of gw partial rows
+    size_t smem;       // dynamic shared memory bytes
+    uint32_t stage_bytes;
+};
+
+// Configuration tables (index = Plan::cfg).
+struct StagedCfg { int nt, g, v, max_nv; };
+struct DirectCfg { int nt, v, max_nv; };
+
+constexpr int N_STAGED_CFG = 10;
+constexpr StagedCfg STAGED_CFGS[N_STAGED_CFG] = {
+    // sub-warp / warp per row (shuffle-only reductions), 256 threads
+    {256, 8, 1, 8}, {256, 16, 1, 16}, {256, 32, 1, 32},
+    {256, 32, 2, 64}, {256, 32, 3, 96}, {256, 32, 4, 128},
+    // CTA per row
+    {128, 128, 2, 256}, {256, 256, 2, 512}, {512, 512, 2, 1024}, {1024, 1024, 2, 2048},
+};
+
+constexpr int N_DIRECT_CFG = 6;
+constexpr DirectCfg DIRECT_CFGS[N_DIRECT_CFG] = {
+    {128, 1, 128}, {256, 1, 256}, {512, 1, 512}, {1024, 1, 1024}, {1024, 2, 2048}, {1024, 4, 4096},
+};
+
+constexpr int GENERIC_NT = 256;
+constexpr int STAGED_HEADER_BYTES = 640;  // 16 mbarriers (128 B) + reduction scratch (512 B)
+constexpr int MAX_STAGES = 8;
+
+// Launchers (one translation unit per tier / dtype).  dtype: 0 fp16, 1 bf16.
+cudaError_t launch_staged(int dtype, int mode, const Plan &plan, const KernelArgs &a,
+                          cudaStream_t stream);
+cudaError_t launch_direct(int dtype, int mode, const Plan &plan, const KernelArgs &a,
+                          cudaStream_t stream);
+cudaError_t launch_generic(int dtype, int mode, const Plan &plan, const KernelArgs &a,
+                           cudaStream_t stream);
+cudaError_t launch_gw_reduce(const float *partials, float *gw, int P, int D, cudaStream_t stream);
+
+}  // namespace rmsn
