@@ -1,0 +1,521 @@
+#!/usr/bin/env python
+"""Benchmark of the RMSNorm hot path on GB300: achieved HBM GB/s (and the
+fraction of the measured HBM copy bandwidth) of the fused add-RMSNorm forward
+and the RMSNorm VJP.
+
+One step = the prefill workload, bf16, rows 16384:
+    fwd(D=4096, with residual); fwd(D=8192, with residual);
+    vjp(D=4096, x = new_residual); vjp(D=8192, x = new_residual)
+(each VJP is its main kernel plus the gw stage-2 kernel).  The order puts at
+least one other launch of >= 400 MB between a tensor's write and its re-read,
+and every operand (134 or 268 MB) is larger than the 129 MB L2, so each step
+streams from HBM.  Algorithmic bytes: forward 4*R*D*2 + D*2, VJP
+3*R*D*2 + D*2 + 4*D (the gw partials are scratch and not counted).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  N > 1 runs N independent replicas of the step
+(torchrun, one process per GPU): the path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+import torch.distributed as dist
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s and % of GB300 peak for add-RMSNorm fwd and RMSNorm VJP"
+UNIT = "GB/s"
+ROWS = 16384
+DS = (4096, 8192)
+ITEM = 2  # bf16
+FALLBACK_HBM_GBS = 6800.0
+
+
+def fwd_bytes(rows, D, residual=True, s=ITEM):
+    return (4 if residual else 2) * rows * D * s + D * s
+
+
+def vjp_bytes(rows, D, s=ITEM):
+    return 3 * rows * D * s + D * s + 4 * D
+
+
+STEP_BYTES = sum(fwd_bytes(ROWS, D) + vjp_bytes(ROWS, D) for D in DS)
+OPS = [("fwd_d%d" % D, D) for D in DS] + [("vjp_d%d" % D, D) for D in DS]
+OP_BYTES = {"fwd_d%d" % D: fwd_bytes(ROWS, D) for D in DS}
+OP_BYTES.update({"vjp_d%d" % D: vjp_bytes(ROWS, D) for D in DS})
+KERNELS_PER_STEP = 6  # two forward kernels, two VJP main kernels, two gw reductions
+
+CONFIG = {
+    "workload": "prefill fused add-RMSNorm fwd (with residual) + RMSNorm VJP on new_residual, "
+                "rows 16384, D 4096 and 8192, bf16, eps 1e-6, weight_bias 0",
+    "rows": ROWS,
+    "D": list(DS),
+    "l2": "inputs larger than L2: every operand is 134-268 MB vs 129 MB L2; no operand is "
+          "re-read from L2 between steps",
+    "parallelism": "replicas",
+}
+
+
+# ---------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier():
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(value: float, device) -> float:
+    """Largest value over all ranks (the value itself without a process group)."""
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.bus = None
+        try:
+            props = torch.cuda.get_device_properties(device_index)
+            self.bus = "%08X:%02X:%02X" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        except Exception:
+            self.bus = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + CLOCK_FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [f.strip() for f in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [(t, f) for (t, f) in self.samples if len(f) >= 9]
+        buses = {f[0] for _, f in rows}
+        if len(buses) > 1 and self.bus:
+            rows = [(t, f) for (t, f) in rows if f[0].upper().startswith(self.bus.upper())] or rows
+        window = [f for (t, f) in rows if t0 - 0.1 <= t <= t1 + 0.1]
+        use = window or [f for _, f in rows]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(f[1]) for f in use if num(f[1]) is not None]
+        mx = [num(f[2]) for f in use if num(f[2]) is not None]
+        reasons = set()
+        for f in use:
+            for name, flag in zip(REASON_NAMES, f[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(use),
+                "in_timed_window": bool(window)}
+
+
+# ---------------------------------------------------------------------------
+# the measured path
+# ---------------------------------------------------------------------------
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    pkg = os.path.join(ROOT, "rmsnorm_fwd_bwd_add_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(pkg, "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(op):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("csrc_sha") != source_hash():
+        return None
+    return rec.get("bytes_per_launch", {}).get(op)
+
+
+def host_inputs():
+    from rmsnorm_fwd_bwd_add_gb300 import workloads as W
+    cases = {D: W.config4(D, ROWS) for D in DS}
+    return cases
+
+
+class Step:
+    """Device buffers for one step and the calls that make it."""
+
+    def __init__(self, cases, device):
+        import rmsnorm_fwd_bwd_add_gb300 as rn
+        self.rn = rn
+        self.dev = device
+        self.t = {}
+        for D, c in cases.items():
+            self.t[D] = dict(
+                x=c.x.to(device), res=c.residual.to(device), w=c.w.to(device), g=c.g.to(device),
+                out=torch.empty_like(c.x, device=device), nr=torch.empty_like(c.x, device=device),
+                gx=torch.empty_like(c.x, device=device),
+                gw=torch.empty(D, dtype=torch.float32, device=device))
+        self.eps = {D: c.eps for D, c in cases.items()}
+
+    def op(self, name, D):
+        t = self.t[D]
+        if name.startswith("fwd"):
+            self.rn.rmsnorm_fwd(t["x"], t["w"], self.eps[D], 0.0, t["res"], out=t["out"],
+                                new_residual=t["nr"])
+        else:
+            self.rn.rmsnorm_vjp(t["nr"], t["w"], t["g"], self.eps[D], 0.0, gx=t["gx"], gw=t["gw"])
+
+    def run(self):
+        for name, D in OPS:
+            self.op(name, D)
+
+
+def time_device(step: Step, steps: int, warmup: int, sampler: ClockSampler):
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.run()
+    torch.cuda.synchronize()
+    ev = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(steps)] for name, _ in OPS}
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for k in range(steps):
+        for name, D in OPS:
+            a, b = ev[name][k]
+            a.record(stream)
+            step.op(name, D)
+            b.record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    total_ms = start.elapsed_time(end)
+    per_op_us = {name: 1e3 * statistics.mean(a.elapsed_time(b) for a, b in ev[name])
+                 for name, _ in OPS}
+    return total_ms, per_op_us, sampler.summary(t0, t1)
+
+
+def time_e2e(cases, device, steps: int, warmup: int):
+    """Same step through the public API with pinned host buffers: every step
+    copies its inputs host->device, runs, and copies its results back."""
+    import rmsnorm_fwd_bwd_add_gb300 as rn
+    host = {}
+    dev = {}
+    h2d = d2h = 0
+    for D, c in cases.items():
+        host[D] = dict(x=c.x.pin_memory(), res=c.residual.pin_memory(), g=c.g.pin_memory(),
+                       w=c.w.pin_memory(),
+                       out=torch.empty_like(c.x).pin_memory(), nr=torch.empty_like(c.x).pin_memory(),
+                       gx=torch.empty_like(c.x).pin_memory(),
+                       gw=torch.empty(D, dtype=torch.float32).pin_memory())
+        dev[D] = {k: torch.empty_like(v, device=device) for k, v in host[D].items()}
+        h2d += sum(host[D][k].numel() * host[D][k].element_size() for k in ("x", "res", "g", "w"))
+        d2h += sum(host[D][k].numel() * host[D][k].element_size() for k in ("out", "nr", "gx", "gw"))
+
+    def one():
+        for D in DS:
+            for k in ("x", "res", "g", "w"):
+                dev[D][k].copy_(host[D][k], non_blocking=True)
+        for D in DS:
+            d = dev[D]
+            rn.rmsnorm_fwd(d["x"], d["w"], cases[D].eps, 0.0, d["res"], out=d["out"],
+                           new_residual=d["nr"])
+        for D in DS:
+            d = dev[D]
+            rn.rmsnorm_vjp(d["nr"], d["w"], d["g"], cases[D].eps, 0.0, gx=d["gx"], gw=d["gw"])
+        for D in DS:
+            for k in ("out", "nr", "gx", "gw"):
+                host[D][k].copy_(dev[D][k], non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), device)
+    return ms / steps, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (reported baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(cases, rows):
+    """float64 copies of the first `rows` rows of each D of the workload."""
+    import numpy as np
+    out = {}
+    for D, c in cases.items():
+        def f(t):
+            return np.ascontiguousarray(t[:rows].to(torch.float64).numpy())
+        out[D] = dict(x=f(c.x), res=f(c.residual), g=f(c.g),
+                      w=c.w.to(torch.float64).numpy(), eps=c.eps)
+    return out
+
+
+def oracle_pass(sample):
+    """One forward (with residual) + VJP on new_residual per D; returns the
+    algorithmic bytes it stands for."""
+    import oracle
+    nbytes = 0
+    for D, s in sample.items():
+        _, h = oracle.fwd(s["x"], s["w"], s["eps"], 0.0, s["res"])
+        oracle.vjp(h, s["w"], s["g"], s["eps"], 0.0)
+        rows = s["x"].shape[0]
+        nbytes += fwd_bytes(rows, D) + vjp_bytes(rows, D)
+    return nbytes
+
+
+def cpu_baseline(cases, min_seconds=10.0, max_seconds=30.0, rows=256):
+    import oracle
+    oracle.build()
+    sample = oracle_sample(cases, rows)
+    oracle_pass(sample)  # load and warm
+    t0 = time.perf_counter()
+    nbytes = 0
+    passes = 0
+    while True:
+        nbytes += oracle_pass(sample)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or el >= max_seconds:
+            break
+    return {"value": nbytes / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "first %d rows of each D (4096, 8192) of the prefill workload: fp64 C "
+                      "oracle forward with residual + VJP, %d passes in %.1f s, one thread"
+                      % (rows, passes, el)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    cases = host_inputs()
+    # size each step's sample so the whole run takes about a minute
+    cal = oracle_sample(cases, 32)
+    t0 = time.perf_counter()
+    cal_bytes = oracle_pass(cal)
+    rate = cal_bytes / max(time.perf_counter() - t0, 1e-6)
+    per_row = sum(fwd_bytes(1, D) + vjp_bytes(1, D) for D in DS)
+    rows = int(60.0 * rate / max(1, args.steps + args.warmup) / per_row)
+    rows = max(4, min(512, rows))
+    sample = oracle_sample(cases, rows)
+    for _ in range(args.warmup):
+        oracle_pass(sample)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += oracle_pass(sample)
+    el = time.perf_counter() - t0
+    value = nbytes / el / 1e9
+    desc = ("first %d rows of each D (4096, 8192) of the prefill workload per step: fp64 C oracle "
+            "forward with residual + VJP, one thread" % rows)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": CONFIG,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_single_op(args):
+    """One op on a case of the prefill recipe (for ncu captures of one kernel)."""
+    from rmsnorm_fwd_bwd_add_gb300 import build, workloads as W
+    import rmsnorm_fwd_bwd_add_gb300 as rn
+    build.build()
+    dev = torch.device("cuda", 0)
+    c = W.config4(args.D, args.rows)
+    x, res, w, g = (t.to(dev) for t in (c.x, c.residual, c.w, c.g))
+    out, nr, gx = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
+    gw = torch.empty(args.D, dtype=torch.float32, device=dev)
+
+    def once():
+        if args.op == "fwd":
+            rn.rmsnorm_fwd(x, w, c.eps, 0.0, res, out=out, new_residual=nr)
+        else:
+            rn.rmsnorm_vjp(x, w, g, c.eps, 0.0, gx=gx, gw=gw)
+    for _ in range(args.warmup):
+        once()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.reps):
+        once()
+    b.record()
+    torch.cuda.synchronize()
+    us = 1e3 * a.elapsed_time(b) / args.reps
+    nbytes = fwd_bytes(args.rows, args.D) if args.op == "fwd" else vjp_bytes(args.rows, args.D)
+    plan = rn.rmsnorm_describe_dispatch(args.op, args.rows, args.D, torch.bfloat16, True)
+    print("op=%s rows=%d D=%d plan=%s us=%.2f GB/s=%.1f" % (args.op, args.rows, args.D, plan, us,
+                                                          nbytes / us / 1e3), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=("fwd", "vjp"),
+                    help="profiling mode: run one op of the prefill recipe at --rows x --D "
+                         "(--reps launches after --warmup) and print its mean time; no JSON line")
+    ap.add_argument("--rows", type=int, default=8192)
+    ap.add_argument("--D", type=int, default=8192)
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.op is None:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.op is not None:
+        return run_single_op(args)
+
+    from rmsnorm_fwd_bwd_add_gb300 import build
+    rank, world, local = dist_setup(args.gpus)
+    if rank == 0:
+        build.build()
+    barrier()
+    if world > 1:
+        build.build()  # no-op once rank 0 has built it
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    cases = host_inputs()
+    step = Step(cases, device)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    total_ms, per_op_us, clocks = time_device(step, args.steps, args.warmup, sampler)
+    sampler.stop()
+    total_ms = max_over_ranks(total_ms, device)
+    ms_per_step = total_ms / args.steps
+    value = world * STEP_BYTES * args.steps / (total_ms * 1e-3) / 1e9
+
+    peak, peak_src = measured_peak()
+    ops = {}
+    for name, _ in OPS:
+        gbs = OP_BYTES[name] / (per_op_us[name] * 1e-6) / 1e9
+        ops[name] = {"us": round(per_op_us[name], 2), "gbs": round(gbs, 1),
+                     "frac": round(gbs / peak, 4), "bytes": OP_BYTES[name]}
+    dom = max(per_op_us, key=per_op_us.get)
+    roofline = {"bound": "hbm", "achieved": ops[dom]["gbs"], "peak": peak, "unit": UNIT,
+                "frac": ops[dom]["gbs"] / peak, "traffic": recorded_traffic(dom),
+                "kernel": dom, "peak_source": peak_src,
+                "note": "achieved = algorithmic bytes per launch / mean CUDA-event duration"}
+
+    e2e = None
+    if not args.no_e2e:
+        del step
+        torch.cuda.empty_cache()
+        e2e_steps = max(3, min(args.steps, 30))
+        ms_e2e, h2d, d2h = time_e2e(cases, device, e2e_steps, 3)
+        e2e = {"value": world * STEP_BYTES / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cases)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic", "config": CONFIG,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": KERNELS_PER_STEP * args.steps, "clocks": clocks, "ops": ops}
+        print(json.dumps(line), flush=True)
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -52,6 +52,45 @@ def assert_close(name: str, got: torch.Tensor, want: np.ndarray, dtype=None) -> 
         "%s: normwise error %.3e, worst row %.3e > tol %.1e" % (name, e_all, e_row, tol))
 
 
+U32 = 2.0 ** -24
+# Half the spacing of the smallest subnormals: the absolute rounding error of
+# an output that underflows.
+HALF_SUBNORMAL = {torch.float16: 2.0 ** -25, torch.bfloat16: 2.0 ** -134}
+
+
+def gx_term_magnitude(x, w, g, eps, wb):
+    """|r g w'| + |(r^3/D) h dot| elementwise: the size of the two terms whose
+    difference is gx.  Their cancellation sets how many fp32 digits any
+    evaluation of gx can keep (at D = 1 the terms agree to about
+    log10(h^2/eps) digits)."""
+    e = oracle.Oracle.scalar(eps)
+    b = oracle.Oracle.scalar(wb)
+    h = f64(x)
+    u = f64(g) * (b + f64(w))[None, :]
+    D = h.shape[1]
+    r = 1.0 / np.sqrt(np.mean(h * h, axis=1) + e)
+    dot = np.sum(u * h, axis=1)
+    return np.abs(r[:, None] * u) + np.abs((r ** 3 / D * dot)[:, None] * h)
+
+
+def assert_close_conditioned(name, got, want, terms, k=16.0):
+    """Normwise check with the stated dtype tolerance plus the error that fp32
+    cancellation of size `terms` and output underflow can cause: per row,
+    ||err|| <= tol ||want|| + k u32 ||terms|| + sqrt(D) * half-subnormal.
+    For the workload configurations the extra terms are far below tol."""
+    tol = TOL[got.dtype]
+    g = f64(got).reshape(-1, want.shape[-1])
+    want = want.reshape(-1, want.shape[-1])
+    terms = terms.reshape(-1, want.shape[-1])
+    assert np.all(np.isfinite(g)), "%s: non-finite values in the GPU result" % name
+    err = np.linalg.norm(g - want, axis=1)
+    allow = (tol * np.linalg.norm(want, axis=1) + k * U32 * np.linalg.norm(terms, axis=1)
+             + np.sqrt(want.shape[1]) * HALF_SUBNORMAL[got.dtype])
+    bad = np.nonzero(err > allow)[0]
+    assert bad.size == 0, "%s: row %d error %.3e > allowed %.3e" % (
+        name, bad[0], err[bad[0]], allow[bad[0]])
+
+
 def oracle_fwd(case, residual=True):
     res = case.residual if residual else None
     return oracle.fwd(f64(case.x), f64(case.w), case.eps, case.weight_bias,

@@ -1,0 +1,62 @@
+"""bench.py's multi-rank host logic on CPU: two gloo ranks agree on the
+slowest rank's time, and the reference arm runs on rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    local_ms = 10.0 + 5.0 * rank
+    got = bench.max_over_ranks(local_ms, "cpu")
+    bench.barrier()
+    q.put((rank, got))
+    dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 15.0, 1: 15.0}
+
+
+def test_single_process_max_is_identity():
+    import bench
+    assert bench.max_over_ranks(3.5, "cpu") == 3.5
+
+
+def test_reference_arm_skips_non_zero_ranks(monkeypatch, capsys):
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    assert bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_step_bytes():
+    import bench
+    # forward 4*R*D*2 + D*2 and VJP 3*R*D*2 + D*2 + 4*D at R = 16384
+    assert bench.fwd_bytes(16384, 4096) == 536879104
+    assert bench.vjp_bytes(16384, 4096) == 402677760
+    assert bench.fwd_bytes(16384, 8192) == 1073758208
+    assert bench.vjp_bytes(16384, 8192) == 805355520
+    assert bench.STEP_BYTES == 536879104 + 402677760 + 1073758208 + 805355520

@@ -8,7 +8,8 @@ import torch
 
 import rmsnorm_fwd_bwd_add_gb300 as rn
 from rmsnorm_fwd_bwd_add_gb300 import workloads as W
-from parity import assert_close, f64, oracle_fwd, oracle_vjp
+from parity import (assert_close, assert_close_conditioned, f64, gx_term_magnitude, oracle_fwd,
+                    oracle_vjp)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -47,10 +48,17 @@ def check_fwd(case, residual=True):
     return out, nr, want_h
 
 
-def check_vjp(case, x_cpu):
+def check_vjp(case, x_cpu, conditioned=False):
+    """conditioned=False: the stated tolerances as they are (the workload
+    configurations).  conditioned=True (edge shapes, e.g. D = 1): gx also gets
+    the error that fp32 cancellation between its two terms allows."""
     gx, gw = rn.rmsnorm_vjp(_dev(x_cpu), _dev(case.w), _dev(case.g), case.eps, case.weight_bias)
     want_gx, want_gw = oracle_vjp(x_cpu, case)
-    assert_close(case.name + " gx", gx, want_gx)
+    if conditioned:
+        terms = gx_term_magnitude(x_cpu, case.w, case.g, case.eps, case.weight_bias)
+        assert_close_conditioned(case.name + " gx", gx, want_gx, terms)
+    else:
+        assert_close(case.name + " gx", gx, want_gx)
     assert_close(case.name + " gw", gw, want_gw, torch.float32)
     return gx, gw
 
@@ -130,7 +138,7 @@ def test_edge_shapes(rows, D, dtype):
     case = W.random_case(rows, D, dtype, seed=rows * 7919 + D, weight_bias=0.5, eps=1e-5)
     _, _, want_h = check_fwd(case, residual=True)
     check_fwd(case, residual=False)
-    check_vjp(case, rounded_h(want_h, dtype))
+    check_vjp(case, rounded_h(want_h, dtype), conditioned=True)
 
 
 def test_empty_rows():
@@ -274,10 +282,19 @@ def test_errors_are_statuses():
     with pytest.raises(rn.RmsnormError) as e:
         rn.rmsnorm_fwd(xv, w, 1e-6, out=ov)
     assert e.value.status == 1
-    # workspace too small
+    # workspace too small (this shape needs one [D] fp32 partial row per CTA)
+    xl = torch.randn(4096, 1024, device=DEV).to(torch.bfloat16)
+    wl = torch.ones(1024, dtype=torch.bfloat16, device=DEV)
+    assert rn.rmsnorm_vjp_workspace_size(4096, 1024, torch.bfloat16) > 256
     with pytest.raises(rn.RmsnormError) as e:
-        rn.rmsnorm_vjp_ws(x, w, x, 1e-6, workspace=torch.empty(256, dtype=torch.uint8, device=DEV))
+        rn.rmsnorm_vjp_ws(xl, wl, xl, 1e-6, workspace=torch.empty(256, dtype=torch.uint8, device=DEV))
     assert e.value.status == 1
+    # null workspace through the C ABI
+    st = rn._native.lib().rmsnorm_vjp_ws(xl.data_ptr(), wl.data_ptr(), xl.data_ptr(), 1e-6, 0.0,
+                                         torch.empty_like(xl).data_ptr(),
+                                         torch.empty(1024, device=DEV).data_ptr(), 4096, 1024, 1,
+                                         None, 1 << 30, None)
+    assert st == 1
 
 
 def test_wait_timeout_is_reported_and_context_survives():
