@@ -70,20 +70,41 @@ int current_device(DevInfo *out) {
         e = cudaGetSymbolAddress(&p, g_devstatus);
         if (e != cudaSuccess) return cuda_fail(e);
         d.status = static_cast<unsigned int *>(p);
+        d.ready = true;
+    }
+    *out = d;
+    return RMSNORM_OK;
+}
+
+// The memory pool rmsnorm_vjp takes its gw scratch from, created on the
+// first rmsnorm_vjp call on the current device (no other entry point needs
+// one).
+int scratch_pool(cudaMemPool_t *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= MAX_DEVICES) return RMSNORM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.pool) {
         cudaMemPoolProps props{};
         props.allocType = cudaMemAllocationTypePinned;
         props.location.type = cudaMemLocationTypeDevice;
         props.location.id = dev;
-        e = cudaMemPoolCreate(&d.pool, &props);
+        cudaMemPool_t pool = nullptr;
+        e = cudaMemPoolCreate(&pool, &props);
         if (e != cudaSuccess) return cuda_fail(e);
         // Keep freed scratch in the pool: the next call reuses it without
         // going back to the driver.
         uint64_t keep = UINT64_MAX;
-        e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-        if (e != cudaSuccess) return cuda_fail(e);
-        d.ready = true;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return cuda_fail(e);
+        }
+        d.pool = pool;
     }
-    *out = d;
+    *out = d.pool;
     return RMSNORM_OK;
 }
 
@@ -369,8 +390,11 @@ int rmsnorm_vjp(const void *x, const void *w, const void *g, float eps, float we
         cudaError_t e = cudaMemsetAsync(gw, 0, (size_t)D * sizeof(float), s);
         return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e);
     }
+    cudaMemPool_t pool = nullptr;
+    st = scratch_pool(&pool);
+    if (st != RMSNORM_OK) return st;
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, partials_bytes(p, D), dev.pool, s);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, partials_bytes(p, D), pool, s);
     if (e == cudaErrorMemoryAllocation) {
         (void)cudaGetLastError();
         return RMSNORM_ERR_NO_MEMORY;
