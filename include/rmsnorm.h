@@ -140,6 +140,37 @@ int rmsnorm_vjp_ws(const void *x, const void *w, const void *g, float eps,
                    int64_t D, int dtype, void *workspace, size_t workspace_bytes,
                    void *stream);
 
+/* Size of the fixed device array behind rmsnorm_vjp_noalloc: 16 MiB. */
+#define RMSNORM_VJP_NOALLOC_MAX_BYTES ((size_t)16 << 20)
+
+/*
+ * rmsnorm_vjp for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this entry point exists for programs that may not call
+ * cudaMalloc or any other allocator when they run the backward pass (runtimes
+ * that reserve all device memory at start-up and forbid later allocations,
+ * plugin interfaces that give a kernel neither an allocator nor a workspace,
+ * latency-critical loops that cannot afford an allocation's synchronisation
+ * or its failure).  Arguments, results, numerics and errors are those of
+ * rmsnorm_vjp; the gw partial rows go to a 16 MiB array compiled into the
+ * library instead of allocated memory, and nothing is allocated.
+ *   - Memory: the array occupies RMSNORM_VJP_NOALLOC_MAX_BYTES of device memory
+ *     on every GPU where the library is loaded, until the process exits.
+ *   - Limit: a problem whose scratch (rmsnorm_vjp_workspace_size for these
+ *     pointers' alignment) exceeds RMSNORM_VJP_NOALLOC_MAX_BYTES returns
+ *     RMSNORM_ERR_UNSUPPORTED and enqueues nothing.  On a 152-SM GB300 that
+ *     admits 16-byte aligned rows with D up to about 13,000 at any row count.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array, and it keeps the
+ *     last call's contents (nothing in it needs to start at zero: each call
+ *     writes every partial row before reading it).  Calls whose work overlaps
+ *     on the GPU (other streams, or other host threads) race on the array and
+ *     give wrong gw; order them on one stream.
+ */
+int rmsnorm_vjp_noalloc(const void *x, const void *w, const void *g, float eps,
+                        float weight_bias, void *gx, float *gw, int64_t rows,
+                        int64_t D, int dtype, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *rmsnorm_status_string(int status);
 

@@ -18,6 +18,7 @@ EXPORTS = (
     "rmsnorm_vjp",
     "rmsnorm_vjp_workspace_size",
     "rmsnorm_vjp_ws",
+    "rmsnorm_vjp_noalloc",
     "rmsnorm_status_string",
     "rmsnorm_last_cuda_error",
     "rmsnorm_device_status",
@@ -35,6 +36,7 @@ STATUS = {
 }
 DEVSTATUS_WAIT_TIMEOUT = 1
 MAX_D = 1 << 24
+VJP_NOALLOC_MAX_BYTES = 16 << 20
 
 _vp = ctypes.c_void_p
 _f = ctypes.c_float
@@ -67,6 +69,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.rmsnorm_vjp_ws.argtypes = [_vp, _vp, _vp, _f, _f, _vp, _vp, _i64, _i64, _i, _vp,
                                    ctypes.c_size_t, _vp]
     lib.rmsnorm_vjp_ws.restype = _i
+    lib.rmsnorm_vjp_noalloc.argtypes = [_vp, _vp, _vp, _f, _f, _vp, _vp, _i64, _i64, _i, _vp]
+    lib.rmsnorm_vjp_noalloc.restype = _i
     lib.rmsnorm_status_string.argtypes = [_i]
     lib.rmsnorm_status_string.restype = ctypes.c_char_p
     lib.rmsnorm_last_cuda_error.argtypes = []

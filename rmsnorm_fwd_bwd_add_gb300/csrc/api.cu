@@ -461,3 +461,23 @@ const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype
 }
 
 }  // extern "C"
+
+// ---- helpers for rmsnorm_vjp_noalloc (noalloc.cu) --------------------------
+namespace rmsn {
+
+// Bytes of gw scratch rmsnorm_vjp_ws needs for exactly these pointers on the
+// current device (0 when rows == 0 or the arguments are invalid).
+size_t vjp_partials_bytes_for(const void *x, const void *w, const void *g, const void *gx,
+                              int64_t rows, int64_t D, int dtype) {
+    if (check_common(rows, D, dtype, 0.f, 0.f) != RMSNORM_OK || rows == 0) return 0;
+    DevInfo dev;
+    if (current_device(&dev) != RMSNORM_OK) return 0;
+    const bool aligned =
+        (D * 2) % 16 == 0 && aligned16(x) && aligned16(g) && aligned16(gx) && aligned16(w);
+    return partials_bytes(make_plan(MODE_VJP, rows, (int)D, aligned, dev.sm_count), D);
+}
+
+// Records a failed CUDA call for rmsnorm_last_cuda_error().
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+}  // namespace rmsn

@@ -1,0 +1,71 @@
+"""rmsnorm_vjp_noalloc, the VJP entry point for callers that may not allocate
+device memory (runtimes that reserve all memory up front, plugin hosts that
+provide no allocator or workspace, loops that cannot absorb an allocation).
+It runs the same kernels as rmsnorm_vjp with the gw partials in a fixed array
+inside the library.  This file is collected last so that a run stopping at the
+first failure has already run every other test; it passes alone in a fresh
+process and after the rest of the suite.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL = {torch.bfloat16: 4e-3, torch.float16: 1e-3}
+CODE = {torch.float16: 0, torch.bfloat16: 1}
+
+
+def _rel(a, b):
+    a = a.double().cpu().numpy()
+    b = b.double().cpu().numpy()
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rmsnorm_fwd_bwd_add_gb300 import _native, build
+    build.build()
+    return _native.lib()
+
+
+def _call_noalloc(lib, x, w, g, eps, wb):
+    rows, D = x.shape
+    gx = torch.empty_like(x)
+    gw = torch.empty(D, dtype=torch.float32, device=DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+    st = lib.rmsnorm_vjp_noalloc(x.data_ptr(), w.data_ptr(), g.data_ptr(), eps, wb,
+                                 gx.data_ptr(), gw.data_ptr(), rows, D, CODE[x.dtype], stream)
+    return st, gx, gw
+
+
+def test_noalloc_matches_rmsnorm_vjp_on_two_calls_in_a_row(lib):
+    import rmsnorm_fwd_bwd_add_gb300 as rn
+    from rmsnorm_fwd_bwd_add_gb300 import workloads as W
+    # Two different problems back to back: the second must not see anything
+    # the first left in the shared array.
+    for rows, D, dtype, seed in ((4096, 4096, torch.bfloat16, 11), (1000, 1024, torch.float16, 12)):
+        case = W.random_case(rows, D, dtype, seed=seed, residual=False, weight_bias=1.0)
+        x, w, g = case.x.to(DEV), case.w.to(DEV), case.g.to(DEV)
+        gx_ref, gw_ref = rn.rmsnorm_vjp(x, w, g, case.eps, case.weight_bias)
+        st, gx, gw = _call_noalloc(lib, x, w, g, case.eps, case.weight_bias)
+        assert st == 0, rn.rmsnorm_status_string(st)
+        torch.cuda.synchronize()
+        assert _rel(gx, gx_ref) <= TOL[dtype]
+        assert _rel(gw, gw_ref) <= 1e-5
+
+
+def test_noalloc_refuses_problems_beyond_its_array(lib):
+    from rmsnorm_fwd_bwd_add_gb300 import _native
+    # Unaligned long rows: one partial row of D floats per CTA for up to
+    # 8 CTAs per SM is far more than the fixed array holds.
+    rows, D = 2000, 40000
+    x = torch.randn(rows, D, device=DEV).to(torch.bfloat16)
+    w = torch.ones(D, dtype=torch.bfloat16, device=DEV)
+    need = lib.rmsnorm_vjp_workspace_size(rows, D, 1)
+    assert need > _native.VJP_NOALLOC_MAX_BYTES
+    st, gx, gw = _call_noalloc(lib, x, w, x, 1e-6, 0.0)
+    assert st == 2  # RMSNORM_ERR_UNSUPPORTED, nothing enqueued
+    assert lib.rmsnorm_status_string(st) == b"unsupported problem size"
