@@ -21,7 +21,6 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import glob
 import json
 import os
 import statistics
@@ -181,27 +180,46 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_hash():
+# Files that define the staged kernels and their launch plans: a change to any
+# of them invalidates recorded DRAM traffic.
+STAGED_SOURCES = ("api.cu", "common.cuh", "plan.h", "launch_staged.cuh", "staged.cuh",
+                  "staged_bf16.cu", "staged_f16.cu")
+
+
+def source_hash(files=STAGED_SOURCES):
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "rmsnorm_fwd_bwd_add_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(pkg, "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+    for name in files:
+        with open(os.path.join(pkg, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_prefill_r16384_bf16.md")
+
+
 def recorded_traffic(op):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; otherwise None."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes (read + write) per launch of `op`'s main kernel from the
+    committed ncu summary, if it was taken on the current staged-kernel
+    sources; otherwise None.  The summary's lines `staged sources: <hash>` and
+    `<op>: <bytes>` are read."""
     try:
-        with open(path) as f:
-            rec = json.load(f)
-    except Exception:
+        with open(TRAFFIC_FILE) as f:
+            text = f.read()
+    except OSError:
         return None
-    if rec.get("csrc_sha") != source_hash():
+    rec = {}
+    for line in text.splitlines():
+        line = line.strip().strip("`")
+        if ":" in line:
+            k, v = line.split(":", 1)
+            rec[k.strip()] = v.strip()
+    if rec.get("staged sources") != source_hash():
         return None
-    return rec.get("bytes_per_launch", {}).get(op)
+    try:
+        return int(rec[op])
+    except (KeyError, ValueError):
+        return None
 
 
 def host_inputs():

@@ -83,6 +83,32 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
     return v;
 }
 
+// Eight 16-bit values <-> four float2 (the operand shape of the packed fp32x2
+// arithmetic below).
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4 &v, float2 f[4]) {
+    f[0] = Cvt<T>::unpack2(v.x);
+    f[1] = Cvt<T>::unpack2(v.y);
+    f[2] = Cvt<T>::unpack2(v.z);
+    f[3] = Cvt<T>::unpack2(v.w);
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack8(const float2 f[4]) {
+    uint4 v;
+    v.x = Cvt<T>::pack2(f[0].x, f[0].y);
+    v.y = Cvt<T>::pack2(f[1].x, f[1].y);
+    v.z = Cvt<T>::pack2(f[2].x, f[2].y);
+    v.w = Cvt<T>::pack2(f[3].x, f[3].y);
+    return v;
+}
+
+// Packed fp32x2 arithmetic (one instruction for two lanes of work on sm_100+),
+// each result rounded to nearest even exactly as the scalar operation would be.
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
 // Streaming 16-byte global load (evict-first: every byte is read once) and a
 // plain 16-byte store.
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
@@ -142,6 +168,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if (mbar_try_wait(bar, parity)) return true;
         if (clock64() - t0 > budget) return false;
     }
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel on the stream finishes;
+// it must wait here before touching anything that kernel wrote (a no-op when
+// launched normally).  The previous kernel signals early with
+// griddep_launch_dependents(); the wait still covers all of its writes.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {

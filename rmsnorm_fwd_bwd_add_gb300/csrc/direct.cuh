@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
     }
 
     if constexpr (VJP) {
+        griddep_launch_dependents();  // the gw reduction may start launching
         float *prow = a.partials + (size_t)blockIdx.x * D;
 #pragma unroll
         for (int j = 0; j < V; ++j) {

@@ -73,9 +73,17 @@ cudaError_t launch_generic(int dtype, int mode, const Plan &p, const KernelArgs 
 }
 
 cudaError_t launch_gw_reduce(const float *partials, float *gw, int P, int D, cudaStream_t s) {
-    const unsigned int blocks = (unsigned int)((D + 31) / 32);
-    gw_reduce_kernel<<<blocks, 256, 0, s>>>(partials, gw, P, D);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned int)((D + 31) / 32));
+    cfg.blockDim = dim3(32 * GWR_CHUNKS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gw_reduce_kernel, partials, gw, P, D);
 }
 
 }  // namespace rmsn

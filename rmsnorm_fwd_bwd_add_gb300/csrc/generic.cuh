@@ -93,27 +93,43 @@ __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a)
 }
 
 // Stage 2 of gw: gw[c] = sum over p of partials[p, c].  A CTA covers 32
-// columns; its 8 warps each add a contiguous eighth of the P partial rows in
-// ascending order, then warp 0 adds the eight results in warp order.  The
-// order depends only on (P, D), never on timing.
-__global__ void __launch_bounds__(256) gw_reduce_kernel(const float *__restrict__ partials,
-                                                        float *__restrict__ gw, int P, int D) {
-    __shared__ float part[8][33];
+// columns with GWR_CHUNKS warps; warp k adds the k-th contiguous chunk of the
+// P partial rows in ascending order, then warp 0 adds the chunk sums in warp
+// order.  The order depends only on (P, D), never on timing.  Each thread
+// issues up to GWR_BATCH loads before its first add, so a chunk costs one
+// L2 round trip.  Launched as a programmatic dependent of the VJP kernel that
+// wrote the partials.
+constexpr int GWR_CHUNKS = 32;
+constexpr int GWR_BATCH = 16;
+
+__global__ void __launch_bounds__(32 * GWR_CHUNKS) gw_reduce_kernel(
+    const float *__restrict__ partials, float *__restrict__ gw, int P, int D) {
+    __shared__ float part[GWR_CHUNKS][33];
+    griddep_wait();
     const int tx = threadIdx.x & 31;
     const int ty = threadIdx.x >> 5;
     const int64_t col = (int64_t)blockIdx.x * 32 + tx;
-    const int per = (P + 7) / 8;
+    const int per = (P + GWR_CHUNKS - 1) / GWR_CHUNKS;
     const int p0 = ty * per;
     const int p1 = min(P, p0 + per);
     float s = 0.f;
-    if (col < D)
-        for (int p = p0; p < p1; ++p) s += partials[(size_t)p * D + col];
+    if (col < D) {
+        for (int b = p0; b < p1; b += GWR_BATCH) {
+            float v[GWR_BATCH];
+#pragma unroll
+            for (int i = 0; i < GWR_BATCH; ++i)
+                v[i] = b + i < p1 ? partials[(size_t)(b + i) * D + col] : 0.f;
+#pragma unroll
+            for (int i = 0; i < GWR_BATCH; ++i)
+                if (b + i < p1) s += v[i];
+        }
+    }
     part[ty][tx] = s;
     __syncthreads();
     if (ty == 0 && col < D) {
         float t = part[0][tx];
 #pragma unroll
-        for (int k = 1; k < 8; ++k) t += part[k][tx];
+        for (int k = 1; k < GWR_CHUNKS; ++k) t += part[k][tx];
         gw[col] = t;
     }
 }

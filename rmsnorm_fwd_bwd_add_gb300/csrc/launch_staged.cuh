@@ -8,8 +8,7 @@ namespace rmsn {
 
 template <typename T, int MODE, int NT, int G, int V>
 cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
-    // Up to 512 threads: registers capped so that two CTAs fit on one SM.
-    constexpr int MINB = NT <= 512 ? 2 : 1;
+    constexpr int MINB = staged_ctas_per_sm(MODE, NT, G, V);
     static std::atomic<uint64_t> smem_mask{0};
     auto kern = staged_kernel<T, MODE, NT, G, V, MINB>;
     cudaError_t e = allow_max_dynamic_smem((const void *)kern, smem_mask);
@@ -20,7 +19,7 @@ cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t s
 
 template <typename T, int MODE>
 cudaError_t launch_staged_mode(const Plan &p, const KernelArgs &a, cudaStream_t s) {
-    static_assert(N_STAGED_CFG == 10, "keep this switch in step with STAGED_CFGS");
+    static_assert(N_STAGED_CFG == 11, "keep this switch in step with STAGED_CFGS");
     switch (p.cfg) {
         case 0: return launch_staged_one<T, MODE, 256, 8, 1>(p, a, s);
         case 1: return launch_staged_one<T, MODE, 256, 16, 1>(p, a, s);
@@ -32,6 +31,9 @@ cudaError_t launch_staged_mode(const Plan &p, const KernelArgs &a, cudaStream_t 
         case 7: return launch_staged_one<T, MODE, 256, 256, 2>(p, a, s);
         case 8: return launch_staged_one<T, MODE, 512, 512, 2>(p, a, s);
         case 9: return launch_staged_one<T, MODE, 1024, 1024, 2>(p, a, s);
+        case 10:
+            if constexpr (MODE == MODE_VJP) return cudaErrorInvalidValue;
+            else return launch_staged_one<T, MODE, 256, 256, 4>(p, a, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -51,19 +51,31 @@ struct Plan {
 struct StagedCfg { int nt, g, v, max_nv; };
 struct DirectCfg { int nt, v, max_nv; };
 
-constexpr int N_STAGED_CFG = 10;
+constexpr int N_STAGED_CFG = 11;
 constexpr StagedCfg STAGED_CFGS[N_STAGED_CFG] = {
     // sub-warp / warp per row (shuffle-only reductions), 256 threads
     {256, 8, 1, 8}, {256, 16, 1, 16}, {256, 32, 1, 32},
     {256, 32, 2, 64}, {256, 32, 3, 96}, {256, 32, 4, 128},
     // CTA per row
     {128, 128, 2, 256}, {256, 256, 2, 512}, {512, 512, 2, 1024}, {1024, 1024, 2, 2048},
+    // CTA per row, four vectors per thread: two 256-thread CTAs per SM for
+    // rows of up to 8192 (forward only: the VJP would need too many registers)
+    {256, 256, 4, 1024},
 };
+constexpr int STAGED_CFG_WIDE = 10;
 
 constexpr int N_DIRECT_CFG = 6;
 constexpr DirectCfg DIRECT_CFGS[N_DIRECT_CFG] = {
     {128, 1, 128}, {256, 1, 256}, {512, 1, 512}, {1024, 1, 1024}, {1024, 2, 2048}, {1024, 4, 4096},
 };
+
+// CTAs of a staged configuration that share one SM.  Up to 256 threads two
+// CTAs fit (each capped at 128 registers per thread); a small-D VJP with three
+// or four vectors per lane needs the whole register file, and so does every
+// larger CTA.  The plan and the kernels' __launch_bounds__ both use this.
+constexpr int staged_ctas_per_sm(int mode, int nt, int g, int v) {
+    return (nt <= 256 && !(mode == 2 && v >= 3)) ? 2 : 1;
+}
 
 constexpr int GENERIC_NT = 256;
 constexpr int STAGED_HEADER_BYTES = 640;  // 16 mbarriers (128 B) + reduction scratch (512 B)

@@ -5,20 +5,24 @@
 // one tile of one tensor is ONE bulk copy.  CTA b owns tiles b, b + grid,
 // b + 2*grid, ... (a static assignment, so the VJP's gw partials are summed in
 // the same order on every run).  Thread 0 keeps `stages` tiles in flight;
-// every thread waits on the tile's mbarrier, reads its vectors from shared
-// memory, and writes its outputs straight to global memory.
+// every thread waits on the tile's mbarrier, converts its vectors of the row
+// from shared memory into fp32 registers once, and writes its outputs straight
+// to global memory.
 //
 // Two shapes of work inside a tile:
 //   * G == NT ("CTA per row", D > 1024): one row per tile; each thread owns
 //     V vectors of 8 elements; sum of squares = warp shuffle tree, then the
-//     warp totals in shared memory added in warp order (the warp-then-block
-//     reduction of the fused-norm design), one CTA barrier per row.
+//     warp totals (read one per lane from shared memory) summed by a second
+//     shuffle tree: the warp-then-block reduction of the fused-norm design,
+//     one CTA barrier per row.  A stage is handed back to the producer one row
+//     later, at the next barrier, when every thread is done with it.
 //   * G <= 32 ("sub-warp / warp per row", D <= 1024): NT/G rows at a time,
 //     each reduced by a G-lane shuffle tree only; no shared-memory reduction,
 //     so no multi-warp band exists to get wrong.
-// The weight vectors a thread multiplies by are the same for every row it
-// touches (fixed column ownership), so w is read once per CTA and, in the VJP,
-// the gw contribution of every row stays in the owning thread's registers.
+// A thread multiplies by the same weight columns in every row it touches
+// (fixed column ownership): w' = weight_bias + w is converted to fp32 once per
+// CTA, and the VJP's gw contributions stay in the owning thread's registers.
+// Per-element arithmetic is packed fp32x2.
 //
 // Sources: "Fused residual-add RMSNorm and fused RoPE + KV-append decode
 // kernels", Background (FusedAddRMSNorm: one pass, fp32 sum kept once,
@@ -40,11 +44,11 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     constexpr int NTENS = (MODE == MODE_FWD_NORES) ? 1 : 2;
     constexpr bool VJP = (MODE == MODE_VJP);
     static_assert(G <= 32 || G == NT, "a row belongs to at most one warp, or to the whole CTA");
-    static_assert(NWARPS <= 32, "reduction scratch holds 32 warps");
+    static_assert(NWARPS <= 32, "one warp total per lane");
 
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [MAX_STAGES]
-    float *red = reinterpret_cast<float *>(smem + 128);   // [2][NWARPS][2]
+    float2 *red = reinterpret_cast<float2 *>(smem + 128);  // [2][NWARPS]
     unsigned char *ring = smem + STAGED_HEADER_BYTES;
 
     const int tid = threadIdx.x;
@@ -61,7 +65,6 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     const int64_t grid = gridDim.x;
     const int64_t nk = (a.num_tiles - (int64_t)blockIdx.x + grid - 1) / grid;  // >= 1
     const float eps = a.eps;
-    const float wb = a.weight_bias;
     const float Df = (float)D;  // exact: D <= 2^24
 
     const T *in0 = static_cast<const T *>(a.in0);
@@ -69,25 +72,28 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     uint4 *out0 = static_cast<uint4 *>(a.out0);
     uint4 *out1 = static_cast<uint4 *>(a.out1);
 
-    auto stage_ptr = [&](int64_t k, int tensor) -> unsigned char * {
-        return ring + ((size_t)(k % S) * NTENS + tensor) * SB;
+    auto stage_ptr = [&](int s, int tensor) -> unsigned char * {
+        return ring + ((size_t)s * NTENS + tensor) * SB;
     };
 
-    // ---- producer state (thread 0 only) ----
-    int64_t issued = 0;
+    // ---- producer (thread 0 only) ----
+    int64_t issued = 0;  // tiles of this CTA issued so far
+    int issue_stage = 0;
     const uint64_t policy = l2_evict_first_policy();
-    auto issue = [&](int64_t k) {
-        const int64_t t = (int64_t)blockIdx.x + k * grid;
+    auto issue_next = [&]() {
+        const int64_t t = (int64_t)blockIdx.x + issued * grid;
         if (t != a.drop_tile) {
             const int64_t row0 = t * TR;
             const int64_t nr = min((int64_t)TR, rows - row0);
             const uint32_t bytes = (uint32_t)(nr * D * (int64_t)sizeof(T));
-            uint64_t *bar = &full[k % S];
+            uint64_t *bar = &full[issue_stage];
             mbar_arrive_expect_tx(bar, bytes * NTENS);
-            bulk_g2s(stage_ptr(k, 0), in0 + row0 * D, bytes, bar, policy);
-            if constexpr (NTENS == 2) bulk_g2s(stage_ptr(k, 1), in1 + row0 * D, bytes, bar, policy);
+            bulk_g2s(stage_ptr(issue_stage, 0), in0 + row0 * D, bytes, bar, policy);
+            if constexpr (NTENS == 2)
+                bulk_g2s(stage_ptr(issue_stage, 1), in1 + row0 * D, bytes, bar, policy);
         }
-        issued = k + 1;
+        ++issued;
+        issue_stage = issue_stage + 1 == S ? 0 : issue_stage + 1;
     };
     // Timeout exit: flag it, then wait (bounded) for this CTA's copies that
     // may still be landing in shared memory before the CTA retires.
@@ -108,154 +114,148 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     __syncthreads();
     if (tid == 0) {
         const int64_t n0 = min((int64_t)S, nk);
-        for (int64_t k = 0; k < n0; ++k) issue(k);
+        while (issued < n0) issue_next();
     }
 
-    // Weight vectors owned by this thread, packed (converted at use).
-    uint4 wv[V];
+    // w' = weight_bias + w for the columns this thread owns, in fp32.
+    float2 wp[V][4];
+    {
+        const float2 wb2 = make_float2(a.weight_bias, a.weight_bias);
 #pragma unroll
-    for (int j = 0; j < V; ++j) {
-        const int vi = gl + j * G;
-        wv[j] = vi < NV ? reinterpret_cast<const uint4 *>(a.w)[vi] : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < V; ++j) {
+            const int vi = gl + j * G;
+            const uint4 wv = vi < NV ? reinterpret_cast<const uint4 *>(a.w)[vi] : make_uint4(0, 0, 0, 0);
+            float2 wf[4];
+            unpack8<T>(wv, wf);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) wp[j][q] = f2add(wb2, wf[q]);
+        }
     }
-    float acc[VJP ? V : 1][8];
+    float2 acc[VJP ? V : 1][4];
 #pragma unroll
     for (int j = 0; j < (VJP ? V : 1); ++j)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+        for (int q = 0; q < 4; ++q) acc[j][q] = make_float2(0.f, 0.f);
 
-    // Phase 1: this thread's share of sum(h^2) and, for the VJP, of
-    // dot = sum(g * w' * x).
-    auto partial_sums = [&](const uint4 *r0, const uint4 *r1, float &sa, float &sb) {
-        sa = 0.f;
-        sb = 0.f;
+    // One row: load this thread's vectors from the stage into fp32 (h = x +
+    // residual, or x; the VJP also g), and its partial sum(h^2) and, for the
+    // VJP, partial dot = sum(g * w' * x).
+    auto load_row = [&](const uint4 *r0, const uint4 *r1, float2 (&xa)[V][4],
+                        float2 (&xb)[V][4], float &sa, float &sb) {
+        float2 s2 = make_float2(0.f, 0.f), d2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = gl + j * G;
             if (vi < NV) {
-                float f0[8];
-                unpack8<T>(r0[vi], f0);
+                unpack8<T>(r0[vi], xa[j]);
+                if constexpr (NTENS == 2) unpack8<T>(r1[vi], xb[j]);
                 if constexpr (MODE == MODE_FWD_RES) {
-                    float f1[8];
-                    unpack8<T>(r1[vi], f1);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float h = f0[e] + f1[e];
-                        sa += h * h;
-                    }
-                } else if constexpr (MODE == MODE_FWD_NORES) {
+                    for (int q = 0; q < 4; ++q) xa[j][q] = f2add(xa[j][q], xb[j][q]);  // h
+                }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) sa += f0[e] * f0[e];
-                } else {
-                    float f1[8], wf[8];
-                    unpack8<T>(r1[vi], f1);
-                    unpack8<T>(wv[j], wf);
+                for (int q = 0; q < 4; ++q) s2 = f2fma(xa[j][q], xa[j][q], s2);
+                if constexpr (VJP) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        sa += f0[e] * f0[e];
-                        sb += (f1[e] * (wb + wf[e])) * f0[e];
-                    }
+                    for (int q = 0; q < 4; ++q) d2 = f2fma(f2mul(xb[j][q], wp[j][q]), xa[j][q], d2);
                 }
             }
         }
+        sa = s2.x + s2.y;
+        sb = d2.x + d2.y;
     };
 
-    // Phase 2: outputs of one row (re-reading the staged row).
-    auto row_outputs = [&](const uint4 *r0, const uint4 *r1, int64_t row, float r, float dot) {
+    // Outputs of one row from the registers load_row filled.
+    auto row_outputs = [&](const float2 (&xa)[V][4], const float2 (&xb)[V][4], int64_t row,
+                           float r, float dot) {
         const size_t base = (size_t)row * NV;
+        const float2 r2 = make_float2(r, r);
         const float c = (r * r) * (dot / Df);  // r^2 * dot / D
+        const float2 nc2 = make_float2(-c, -c);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = gl + j * G;
             if (vi < NV) {
-                float f0[8], wf[8], o[8];
-                unpack8<T>(r0[vi], f0);
-                unpack8<T>(wv[j], wf);
-                if constexpr (MODE == MODE_FWD_RES) {
-                    float f1[8];
-                    unpack8<T>(r1[vi], f1);
+                float2 o[4];
+                if constexpr (VJP) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        f0[e] = f0[e] + f1[e];  // h, unrounded
-                        o[e] = (f0[e] * r) * (wb + wf[e]);
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 u = f2mul(xb[j][q], wp[j][q]);           // g w'
+                        o[q] = f2mul(f2fma(xa[j][q], nc2, u), r2);             // r (g w' - x c)
+                        acc[j][q] = f2fma(xb[j][q], f2mul(xa[j][q], r2), acc[j][q]);  // g x r
                     }
-                    st_global(out1 + base + vi, pack8<T>(f0));
-                } else if constexpr (MODE == MODE_FWD_NORES) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] = (f0[e] * r) * (wb + wf[e]);
                 } else {
-                    float f1[8];
-                    unpack8<T>(r1[vi], f1);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float gwp = f1[e] * (wb + wf[e]);
-                        o[e] = r * (gwp - f0[e] * c);
-                        acc[j][e] += (f1[e] * f0[e]) * r;
-                    }
+                    for (int q = 0; q < 4; ++q) o[q] = f2mul(f2mul(xa[j][q], r2), wp[j][q]);
+                    if constexpr (MODE == MODE_FWD_RES) st_global(out1 + base + vi, pack8<T>(xa[j]));
                 }
                 st_global(out0 + base + vi, pack8<T>(o));
             }
         }
     };
 
+    int s = 0;        // stage of tile k
+    uint32_t ph = 0;  // parity of that stage's phase
     if constexpr (CTA_ROW) {
         for (int64_t k = 0; k < nk; ++k) {
             const int64_t row = (int64_t)blockIdx.x + k * grid;  // tile_rows == 1
-            const bool ok = mbar_wait_bounded(&full[k % S], (uint32_t)((k / S) & 1), a.wait_budget);
-            const uint4 *r0 = reinterpret_cast<const uint4 *>(stage_ptr(k, 0));
-            const uint4 *r1 = reinterpret_cast<const uint4 *>(stage_ptr(k, NTENS - 1));
+            const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_budget);
+            float2 xa[V][4], xb[V][4];
             float sa, sb;
-            partial_sums(r0, r1, sa, sb);
+            load_row(reinterpret_cast<const uint4 *>(stage_ptr(s, 0)),
+                     reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS - 1)), xa, xb, sa, sb);
             sa = group_sum<32>(sa);
             if constexpr (VJP) sb = group_sum<32>(sb);
-            float *rb = red + (k & 1) * (NWARPS * 2);
-            if (lane == 0) {
-                rb[warp * 2] = sa;
-                rb[warp * 2 + 1] = sb;
-            }
-            // Everyone has finished row k-1 (so its stage is free) and has
+            float2 *rb = red + (k & 1) * NWARPS;
+            if (lane == 0) rb[warp] = make_float2(sa, sb);
+            // Everyone has finished row k-1 (its stage is free again) and has
             // published row k's warp totals.
             if (__syncthreads_or(!ok)) {
                 fail(k);
                 return;
             }
-            if (tid == 0 && k >= 1 && k - 1 + S < nk) issue(k - 1 + S);
-            float ss = 0.f, dot = 0.f;
-#pragma unroll
-            for (int w = 0; w < NWARPS; ++w) {
-                ss += rb[w * 2];
-                if constexpr (VJP) dot += rb[w * 2 + 1];
+            if (tid == 0 && k >= 1 && issued < nk) issue_next();
+            float2 tot = lane < NWARPS ? rb[lane] : make_float2(0.f, 0.f);
+            tot.x = group_sum<32>(tot.x);
+            if constexpr (VJP) tot.y = group_sum<32>(tot.y);
+            const float r = rsqrtf(tot.x / Df + eps);
+            row_outputs(xa, xb, row, r, tot.y);
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
             }
-            const float r = rsqrtf(ss / Df + eps);
-            row_outputs(r0, r1, row, r, dot);
         }
     } else {
         for (int64_t k = 0; k < nk; ++k) {
             const int64_t row0 = ((int64_t)blockIdx.x + k * grid) * TR;
             const int nr = (int)min((int64_t)TR, rows - row0);
-            const bool ok = mbar_wait_bounded(&full[k % S], (uint32_t)((k / S) & 1), a.wait_budget);
-            const uint4 *t0 = reinterpret_cast<const uint4 *>(stage_ptr(k, 0));
-            const uint4 *t1 = reinterpret_cast<const uint4 *>(stage_ptr(k, NTENS - 1));
+            const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_budget);
+            const uint4 *t0 = reinterpret_cast<const uint4 *>(stage_ptr(s, 0));
+            const uint4 *t1 = reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS - 1));
             for (int qb = 0; qb < TR; qb += NG) {  // same trip count in every lane
                 const int q = qb + gid;
                 const bool valid = q < nr;
-                const uint4 *r0 = t0 + (size_t)q * NV;
-                const uint4 *r1 = t1 + (size_t)q * NV;
+                float2 xa[V][4], xb[V][4];
                 float sa = 0.f, sb = 0.f;
-                if (valid) partial_sums(r0, r1, sa, sb);
+                if (valid) load_row(t0 + (size_t)q * NV, t1 + (size_t)q * NV, xa, xb, sa, sb);
                 sa = group_sum<G>(sa);
                 if constexpr (VJP) sb = group_sum<G>(sb);
-                if (valid && ok) row_outputs(r0, r1, row0 + q, rsqrtf(sa / Df + eps), sb);
+                if (valid && ok) row_outputs(xa, xb, row0 + q, rsqrtf(sa / Df + eps), sb);
             }
             if (__syncthreads_or(!ok)) {  // the whole tile is consumed
                 fail(k);
                 return;
             }
-            if (tid == 0 && k + S < nk) issue(k + S);
+            if (tid == 0 && issued < nk) issue_next();
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
     }
 
     if constexpr (VJP) {
+        griddep_launch_dependents();  // the gw reduction may start launching
         float *prow = a.partials + (size_t)blockIdx.x * D;
         if constexpr (CTA_ROW) {
             // Each column is owned by exactly one thread of the CTA.
@@ -264,8 +264,8 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
                 const int vi = gl + j * G;
                 if (vi < NV) {
                     float4 *dst = reinterpret_cast<float4 *>(prow + (size_t)vi * 8);
-                    dst[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
-                    dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+                    dst[0] = make_float4(acc[j][0].x, acc[j][0].y, acc[j][1].x, acc[j][1].y);
+                    dst[1] = make_float4(acc[j][2].x, acc[j][2].y, acc[j][3].x, acc[j][3].y);
                 }
             }
         } else {
@@ -278,15 +278,15 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
                 const int vi = gl + j * G;
                 if (vi < NV) {
                     float4 *dst = reinterpret_cast<float4 *>(buf + (size_t)gid * D + (size_t)vi * 8);
-                    dst[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
-                    dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+                    dst[0] = make_float4(acc[j][0].x, acc[j][0].y, acc[j][1].x, acc[j][1].y);
+                    dst[1] = make_float4(acc[j][2].x, acc[j][2].y, acc[j][3].x, acc[j][3].y);
                 }
             }
             __syncthreads();
             for (int col = tid; col < D; col += NT) {
-                float s = 0.f;
-                for (int gg = 0; gg < NG; ++gg) s += buf[(size_t)gg * D + col];
-                prow[col] = s;
+                float sum = 0.f;
+                for (int gg = 0; gg < NG; ++gg) sum += buf[(size_t)gg * D + col];
+                prow[col] = sum;
             }
         }
     }
