@@ -14,6 +14,8 @@
 
 #include <algorithm>
 #include <atomic>
+#include <chrono>
+#include <random>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -32,6 +34,7 @@ constexpr int MAX_DEVICES = 64;
 // Shared-memory budget of one CTA when two share an SM (228 KB per SM, 1 KB
 // reserved per CTA), and when one CTA has the SM to itself (227 KB opt-in).
 constexpr size_t SMEM_TWO_PER_SM = 110 * 1024;
+constexpr size_t SMEM_THREE_PER_SM = 72 * 1024;
 constexpr size_t SMEM_ONE_PER_SM = 225 * 1024;
 // Target bytes of one tensor's tile in the sub-warp/warp-per-row shape.
 constexpr size_t SMALL_TILE_BYTES = 16 * 1024;
@@ -57,6 +60,7 @@ std::mutex g_dev_mu;
 DevInfo g_dev[MAX_DEVICES];
 
 std::atomic<int64_t> g_drop_tile{-1};
+std::atomic<int> g_last_fused_error{0};  // last refused cooperative launch (diagnostics)
 std::atomic<long long> g_wait_budget{DEFAULT_WAIT_BUDGET};
 
 int cuda_fail(cudaError_t e) {
@@ -152,6 +156,7 @@ struct Tuning {
     int cfg = -1;    // staged configuration index
     int cps = 0;     // CTAs per SM (capped by what the registers allow)
     int stages = 0;  // maximum ring depth
+    int fuse = -1;   // 0: always sum gw with the separate kernel
 };
 
 Tuning parse_tuning() {
@@ -163,8 +168,9 @@ Tuning parse_tuning() {
     for (char *tok = std::strtok(buf, ","); tok; tok = std::strtok(nullptr, ",")) {
         int v = 0;
         if (std::sscanf(tok, "cfg=%d", &v) == 1 && v >= 0 && v < N_STAGED_CFG) t.cfg = v;
-        else if (std::sscanf(tok, "cps=%d", &v) == 1 && v >= 1 && v <= 2) t.cps = v;
+        else if (std::sscanf(tok, "cps=%d", &v) == 1 && v >= 1 && v <= 3) t.cps = v;
         else if (std::sscanf(tok, "stages=%d", &v) == 1 && v >= 2 && v <= MAX_STAGES) t.stages = v;
+        else if (std::sscanf(tok, "fuse=%d", &v) == 1 && (v == 0 || v == 1)) t.fuse = v;
     }
     return t;
 }
@@ -191,8 +197,8 @@ bool plan_staged(int mode, int64_t rows, int D, int sm_count, int ci, Plan *p) {
     const int ntens = mode == MODE_FWD_NORES ? 1 : 2;
     const size_t row_bytes = (size_t)D * 2;
     const int max_stages = tu.stages ? tu.stages : MAX_STAGES;
-    const int cps_max = staged_ctas_per_sm(mode, c.nt, c.g, c.v);
-    int cps = tu.cps ? std::min(tu.cps, cps_max) : cps_max;
+    const int cps_max = staged_max_ctas_per_sm(mode, c.nt, c.g, c.v);
+    int cps = tu.cps ? std::min(tu.cps, cps_max) : staged_ctas_per_sm(mode, c.nt, c.g, c.v);
     p->tier = TIER_STAGED;
     p->cfg = ci;
     p->nt = c.nt;
@@ -209,6 +215,7 @@ bool plan_staged(int mode, int64_t rows, int D, int sm_count, int ci, Plan *p) {
         p->tile_rows = (int)(ng * rpg);
         p->stage_bytes = (uint32_t)(p->tile_rows * row_bytes);
         const size_t per_stage = (size_t)ntens * p->stage_bytes;
+        cps = std::min(cps, 2);
         const size_t cap = cps == 2 ? SMEM_TWO_PER_SM : SMEM_ONE_PER_SM;
         p->stages = (int)std::min<size_t>(std::min<size_t>(max_stages, cap / per_stage),
                                           ring_stages(mode, per_stage, cps));
@@ -223,9 +230,14 @@ bool plan_staged(int mode, int64_t rows, int D, int sm_count, int ci, Plan *p) {
         p->tile_rows = 1;
         p->stage_bytes = (uint32_t)row_bytes;
         const size_t per_stage = (size_t)ntens * row_bytes;
+        const int64_t s3 = (int64_t)(SMEM_THREE_PER_SM / per_stage);
         const int64_t s2 = (int64_t)(SMEM_TWO_PER_SM / per_stage);
         const int64_t s1 = (int64_t)(SMEM_ONE_PER_SM / per_stage);
-        if (cps == 2 && s2 >= 3) {
+        if (cps == 3 && s3 >= 2) {
+            p->stages = (int)std::min<int64_t>(std::min<int64_t>(max_stages, s3),
+                                               ring_stages(mode, per_stage, 3));
+        } else if (cps >= 2 && s2 >= 3) {
+            cps = 2;
             p->stages = (int)std::min<int64_t>(std::min<int64_t>(max_stages, s2),
                                                ring_stages(mode, per_stage, 2));
         } else if (s1 >= 2) {
@@ -242,17 +254,32 @@ bool plan_staged(int mode, int64_t rows, int D, int sm_count, int ci, Plan *p) {
     return true;
 }
 
+Plan make_plan_(int mode, int64_t rows, int D, bool aligned, int sm_count);
+
 Plan make_plan(int mode, int64_t rows, int D, bool aligned, int sm_count) {
+    Plan p = make_plan_(mode, rows, D, aligned, sm_count);
+    if (tuning().fuse == 0) p.fuse_gw = 0;
+    if (tuning().fuse == 1 && mode == MODE_VJP && p.tier == TIER_STAGED) p.fuse_gw = 1;
+    return p;
+}
+
+Plan make_plan_(int mode, int64_t rows, int D, bool aligned, int sm_count) {
     Plan p{};
     const int nv = D / 8;
     if (aligned && rows > DECODE_ROWS) {
         const int forced = tuning().cfg;
         if (forced >= 0 && nv <= STAGED_CFGS[forced].max_nv &&
             !(mode == MODE_VJP && forced == STAGED_CFG_WIDE) &&
-            plan_staged(mode, rows, D, sm_count, forced, &p))
+            plan_staged(mode, rows, D, sm_count, forced, &p)) {
+            p.fuse_gw = mode == MODE_VJP && tuning().fuse == 1;
             return p;
+        }
         for (int ci = 0; ci < STAGED_CFG_WIDE; ++ci) {
             if (nv <= STAGED_CFGS[ci].max_nv) {
+                // The gw sum stays a separate, programmatically dependent
+                // kernel here: measured on GB300 (rows 16384, D 4096/8192) it
+                // costs less than folding it in, because a cooperative launch
+                // cannot overlap the previous kernel's tail.
                 if (plan_staged(mode, rows, D, sm_count, ci, &p)) return p;
                 break;
             }
@@ -272,6 +299,8 @@ Plan make_plan(int mode, int64_t rows, int D, bool aligned, int sm_count) {
                 p.num_tiles = rows;
                 const int64_t resident = std::max(1, 2048 / c.nt);
                 p.grid = (int)std::min<int64_t>(rows, (int64_t)sm_count * resident);
+                // decode: a handful of CTAs, one launch instead of two
+                p.fuse_gw = mode == MODE_VJP && rows <= DECODE_ROWS;
                 return p;
             }
         }
@@ -286,9 +315,27 @@ Plan make_plan(int mode, int64_t rows, int D, bool aligned, int sm_count) {
     return p;
 }
 
+size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// VJP scratch: the [grid, D] fp32 partial rows, then one 64-bit publication
+// flag per CTA (used when the gw sum is folded into the kernel).
 size_t partials_bytes(const Plan &p, int64_t D) {
-    const size_t b = (size_t)p.grid * (size_t)D * sizeof(float);
-    return (b + 255) & ~(size_t)255;
+    return align256((size_t)p.grid * (size_t)D * sizeof(float)) +
+           align256((size_t)p.grid * sizeof(unsigned long long));
+}
+
+// A value no earlier launch of this process used, and (seeded from the clock
+// and a random device) practically never one left in reused device memory by
+// another process.
+unsigned long long next_epoch() {
+    static const unsigned long long seed = [] {
+        std::random_device rd;
+        const unsigned long long t =
+            (unsigned long long)std::chrono::high_resolution_clock::now().time_since_epoch().count();
+        return ((unsigned long long)rd() << 32) ^ (unsigned long long)rd() ^ (t * 0x9E3779B97F4A7C15ull);
+    }();
+    static std::atomic<unsigned long long> counter{0};
+    return seed + 0x9E3779B97F4A7C15ull * (counter.fetch_add(1) + 1);
 }
 
 cudaError_t launch_plan(int dtype, int mode, const Plan &p, const KernelArgs &a, cudaStream_t s) {
@@ -354,10 +401,25 @@ int vjp_run(const void *x, const void *w, const void *g, float eps, float weight
     a.out0 = gx;
     a.out1 = nullptr;
     a.partials = partials;
+    a.gw = gw;
+    a.flags = reinterpret_cast<unsigned long long *>(
+        reinterpret_cast<char *>(partials) + align256((size_t)p.grid * (size_t)D * sizeof(float)));
+    a.epoch = next_epoch();
+    a.fuse_gw = p.fuse_gw;
     cudaError_t e = launch_plan(dtype, MODE_VJP, p, a, s);
+    if (e != cudaSuccess && a.fuse_gw) {
+        g_last_fused_error.store((int)e);
+        // The cooperative launch was refused (nothing was launched): sum the
+        // partials with the separate stage-2 kernel instead.
+        (void)cudaGetLastError();
+        a.fuse_gw = 0;
+        e = launch_plan(dtype, MODE_VJP, p, a, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
-    e = launch_gw_reduce(partials, gw, p.grid, (int)D, s);
-    if (e != cudaSuccess) return cuda_fail(e);
+    if (!a.fuse_gw) {
+        e = launch_gw_reduce(partials, gw, p.grid, (int)D, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
     return RMSNORM_OK;
 }
 
@@ -513,9 +575,9 @@ const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype
     if (current_device(&dev) != RMSNORM_OK) return "no-device";
     const int mode = op == 1 ? MODE_VJP : (has_residual ? MODE_FWD_RES : MODE_FWD_NORES);
     const Plan p = make_plan(mode, rows, (int)D, aligned && (D * 2) % 16 == 0, dev.sm_count);
-    std::snprintf(buf, sizeof(buf), "%s:cfg%d:nt%d:g%d:v%d:s%d:tr%d:grid%d:smem%zu",
+    std::snprintf(buf, sizeof(buf), "%s:cfg%d:nt%d:g%d:v%d:s%d:tr%d:grid%d:smem%zu%s",
                   tier_name(p.tier), p.cfg, p.nt, p.g, p.v, p.stages, p.tile_rows, p.grid,
-                  p.smem);
+                  p.smem, p.fuse_gw ? ":fused" : "");
     return buf;
 }
 

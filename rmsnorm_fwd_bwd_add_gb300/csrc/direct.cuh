@@ -16,6 +16,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "gw_fused.cuh"
 #include "plan.h"
 
 namespace rmsn {
@@ -47,6 +48,7 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
 
+    griddep_wait();  // programmatic dependent: no global access before this
     int it = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, ++it) {
         const size_t base = (size_t)row * NV;
@@ -138,8 +140,8 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
         }
     }
 
+    griddep_launch_dependents();
     if constexpr (VJP) {
-        griddep_launch_dependents();  // the gw reduction may start launching
         float *prow = a.partials + (size_t)blockIdx.x * D;
 #pragma unroll
         for (int j = 0; j < V; ++j) {
@@ -149,6 +151,10 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
                 dst[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
                 dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
             }
+        }
+        if (a.fuse_gw) {
+            __shared__ float fin[NWARPS * 33];
+            fused_gw_finish<NT>(a, fin);
         }
     }
 }

@@ -2,6 +2,7 @@
 // stage-2 reduction, and the dtype switch of the staged tier.
 #include "direct.cuh"
 #include "generic.cuh"
+#include "launch_util.h"
 
 namespace rmsn {
 
@@ -17,8 +18,8 @@ namespace {
 
 template <typename T, int MODE, int NT, int V>
 cudaError_t direct_one(const Plan &p, const KernelArgs &a, cudaStream_t s) {
-    direct_kernel<T, MODE, NT, V><<<p.grid, NT, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(direct_kernel<T, MODE, NT, V>, dim3(p.grid), dim3(NT), 0, s, a.fuse_gw != 0,
+                      a);
 }
 
 template <typename T, int MODE>
@@ -51,13 +52,15 @@ cudaError_t direct_t(int mode, const Plan &p, const KernelArgs &a, cudaStream_t 
 
 template <typename T>
 cudaError_t generic_t(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    const dim3 grid(p.grid), block(GENERIC_NT);
     switch (mode) {
-        case MODE_FWD_RES: generic_kernel<T, MODE_FWD_RES><<<p.grid, GENERIC_NT, 0, s>>>(a); break;
-        case MODE_FWD_NORES: generic_kernel<T, MODE_FWD_NORES><<<p.grid, GENERIC_NT, 0, s>>>(a); break;
-        case MODE_VJP: generic_kernel<T, MODE_VJP><<<p.grid, GENERIC_NT, 0, s>>>(a); break;
+        case MODE_FWD_RES:
+            return launch_pdl(generic_kernel<T, MODE_FWD_RES>, grid, block, 0, s, false, a);
+        case MODE_FWD_NORES:
+            return launch_pdl(generic_kernel<T, MODE_FWD_NORES>, grid, block, 0, s, false, a);
+        case MODE_VJP: return launch_pdl(generic_kernel<T, MODE_VJP>, grid, block, 0, s, false, a);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -73,17 +76,8 @@ cudaError_t launch_generic(int dtype, int mode, const Plan &p, const KernelArgs 
 }
 
 cudaError_t launch_gw_reduce(const float *partials, float *gw, int P, int D, cudaStream_t s) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned int)((D + 31) / 32));
-    cfg.blockDim = dim3(32 * GWR_CHUNKS);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gw_reduce_kernel, partials, gw, P, D);
+    return launch_pdl(gw_reduce_kernel, dim3((unsigned int)((D + 31) / 32)), dim3(32 * GWR_CHUNKS),
+                      0, s, false, partials, gw, P, D);
 }
 
 }  // namespace rmsn

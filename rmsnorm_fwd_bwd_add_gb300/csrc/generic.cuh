@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a)
     T *out1 = static_cast<T *>(a.out1);
     float *prow = VJP ? a.partials + (size_t)blockIdx.x * D : nullptr;
 
+    griddep_wait();  // programmatic dependent: no global access before this
     if constexpr (VJP)
         for (int c = tid; c < D; c += NT) prow[c] = 0.f;
 
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a)
             }
         }
     }
+    griddep_launch_dependents();
 }
 
 // Stage 2 of gw: gw[c] = sum over p of partials[p, c].  A CTA covers 32
@@ -106,6 +108,7 @@ __global__ void __launch_bounds__(32 * GWR_CHUNKS) gw_reduce_kernel(
     const float *__restrict__ partials, float *__restrict__ gw, int P, int D) {
     __shared__ float part[GWR_CHUNKS][33];
     griddep_wait();
+    griddep_launch_dependents();
     const int tx = threadIdx.x & 31;
     const int ty = threadIdx.x >> 5;
     const int64_t col = (int64_t)blockIdx.x * 32 + tx;

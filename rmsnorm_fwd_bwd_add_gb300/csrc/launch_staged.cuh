@@ -8,13 +8,12 @@ namespace rmsn {
 
 template <typename T, int MODE, int NT, int G, int V>
 cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
-    constexpr int MINB = staged_ctas_per_sm(MODE, NT, G, V);
+    constexpr int MINB = staged_max_ctas_per_sm(MODE, NT, G, V);
     static std::atomic<uint64_t> smem_mask{0};
     auto kern = staged_kernel<T, MODE, NT, G, V, MINB>;
     cudaError_t e = allow_max_dynamic_smem((const void *)kern, smem_mask);
     if (e != cudaSuccess) return e;
-    kern<<<p.grid, NT, p.smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(p.grid), dim3(NT), p.smem, stream, a.fuse_gw != 0, a);
 }
 
 template <typename T, int MODE>

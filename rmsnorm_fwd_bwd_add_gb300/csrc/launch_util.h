@@ -5,10 +5,12 @@
 
 #include <atomic>
 #include <cstdint>
+#include <utility>
 
 namespace rmsn {
 
-// Lets `func` use up to the device's opt-in maximum of dynamic shared memory.
+// Lets `func` use the device's opt-in maximum of shared memory per CTA, less
+// its own static shared memory, as dynamic shared memory.
 // Done once per kernel and device (one bit per device in `mask`).
 inline cudaError_t allow_max_dynamic_smem(const void *func, std::atomic<uint64_t> &mask) {
     int dev = 0;
@@ -19,10 +21,41 @@ inline cudaError_t allow_max_dynamic_smem(const void *func, std::atomic<uint64_t
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, func);  // the kernel's static shared memory counts too
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fa.sharedSizeBytes);
     if (e != cudaSuccess) return e;
     mask.fetch_or(bit, std::memory_order_acq_rel);
     return cudaSuccess;
+}
+
+// Launches `kern` with programmatic stream serialisation: it may begin while
+// the previous kernel on the stream finishes, and every kernel of this library
+// waits (griddepcontrol.wait) before its first global memory access.
+// With `cooperative`, the launch instead guarantees that all CTAs are
+// resident at once (or fails without launching), which the folded gw sum
+// needs; such a launch waits for the previous kernel in the usual way.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, bool cooperative, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (cooperative) {
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+    } else {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace rmsn

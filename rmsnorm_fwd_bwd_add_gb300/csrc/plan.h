@@ -31,6 +31,11 @@ struct KernelArgs {
     uint32_t stage_bytes;     // bytes of one full tile of one tensor
     long long wait_budget;    // SM cycles per bounded wait
     int64_t drop_tile;        // test hook: tile whose copy is never issued (-1: none)
+    // VJP with the gw sum folded in (cooperative launch, see gw_fused.cuh)
+    int fuse_gw;              // 1: the VJP kernel writes gw itself
+    float *gw;                // [D] fp32 output
+    unsigned long long *flags;  // [grid] publication flags
+    unsigned long long epoch;   // value unique to this launch
 };
 
 struct Plan {
@@ -45,6 +50,7 @@ struct Plan {
     int grid;          // CTAs; for the VJP also the number of gw partial rows
     size_t smem;       // dynamic shared memory bytes
     uint32_t stage_bytes;
+    int fuse_gw;       // VJP: fold the gw sum into the kernel (cooperative launch)
 };
 
 // Configuration tables (index = Plan::cfg).
@@ -69,12 +75,19 @@ constexpr DirectCfg DIRECT_CFGS[N_DIRECT_CFG] = {
     {128, 1, 128}, {256, 1, 256}, {512, 1, 512}, {1024, 1, 1024}, {1024, 2, 2048}, {1024, 4, 4096},
 };
 
-// CTAs of a staged configuration that share one SM.  Up to 256 threads two
-// CTAs fit (each capped at 128 registers per thread); a small-D VJP with three
-// or four vectors per lane needs the whole register file, and so does every
-// larger CTA.  The plan and the kernels' __launch_bounds__ both use this.
+// Most CTAs of a staged configuration that can share one SM, as the kernels'
+// __launch_bounds__ promise it (registers per thread capped to fit).  A
+// CTA-per-row forward of up to 256 threads and two vectors fits three times
+// (85 registers); other CTAs of up to 256 threads twice (128 registers),
+// except the small-D VJP with three or four vectors per lane, which needs the
+// whole register file like every larger CTA.
+constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
+    return (nt <= 256 && mode != 2 && g == nt && v <= 2) ? 3
+           : (nt <= 256 && !(mode == 2 && v >= 3)) ? 2 : 1;
+}
+// CTAs per SM the plan uses unless tuned otherwise.
 constexpr int staged_ctas_per_sm(int mode, int nt, int g, int v) {
-    return (nt <= 256 && !(mode == 2 && v >= 3)) ? 2 : 1;
+    return staged_max_ctas_per_sm(mode, nt, g, v) >= 2 ? 2 : 1;
 }
 
 constexpr int GENERIC_NT = 256;

@@ -32,6 +32,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "gw_fused.cuh"
 #include "plan.h"
 
 namespace rmsn {
@@ -112,6 +113,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
         fence_mbar_init();
     }
     __syncthreads();
+    // Launched as a programmatic dependent: nothing in global memory may be
+    // touched before the previous kernel on the stream has completed.
+    griddep_wait();
     if (tid == 0) {
         const int64_t n0 = min((int64_t)S, nk);
         while (issued < n0) issue_next();
@@ -254,8 +258,10 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
         }
     }
 
+    // The next kernel on the stream may start launching (it waits for this
+    // one to complete before touching memory).
+    griddep_launch_dependents();
     if constexpr (VJP) {
-        griddep_launch_dependents();  // the gw reduction may start launching
         float *prow = a.partials + (size_t)blockIdx.x * D;
         if constexpr (CTA_ROW) {
             // Each column is owned by exactly one thread of the CTA.
@@ -289,6 +295,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
                 prow[col] = sum;
             }
         }
+        if (a.fuse_gw) fused_gw_finish<NT>(a, reinterpret_cast<float *>(ring));
     }
 }
 
