@@ -300,47 +300,68 @@ def time_device(step: Step, steps: int, warmup: int, sampler: ClockSampler):
 
 
 def time_e2e(cases, device, steps: int, warmup: int):
-    """Same step through the public API with pinned host buffers: every step
-    copies its inputs host->device, runs, and copies its results back."""
+    """The step through the public Python API with pinned host buffers: every
+    step copies its inputs (x, residual, g, w of both D) host->device and its
+    results (out, new_residual, gx, gw) device->host.  Copies run on their own
+    streams with two device buffer sets, so step k's upload, step k-1's
+    compute and step k-2's download overlap, as a user streaming batches
+    would arrange it; the timed region ends when the last download is done."""
     import rmsnorm_fwd_bwd_add_gb300 as rn
+    ins = ("x", "res", "g", "w")
+    outs = ("out", "nr", "gx", "gw")
     host = {}
-    dev = {}
-    h2d = d2h = 0
     for D, c in cases.items():
         host[D] = dict(x=c.x.pin_memory(), res=c.residual.pin_memory(), g=c.g.pin_memory(),
                        w=c.w.pin_memory(),
                        out=torch.empty_like(c.x).pin_memory(), nr=torch.empty_like(c.x).pin_memory(),
                        gx=torch.empty_like(c.x).pin_memory(),
                        gw=torch.empty(D, dtype=torch.float32).pin_memory())
-        dev[D] = {k: torch.empty_like(v, device=device) for k, v in host[D].items()}
-        h2d += sum(host[D][k].numel() * host[D][k].element_size() for k in ("x", "res", "g", "w"))
-        d2h += sum(host[D][k].numel() * host[D][k].element_size() for k in ("out", "nr", "gx", "gw"))
+    sets = [{D: {k: torch.empty_like(v, device=device) for k, v in host[D].items()} for D in DS}
+            for _ in range(2)]
+    h2d = sum(host[D][k].numel() * host[D][k].element_size() for D in DS for k in ins)
+    d2h = sum(host[D][k].numel() * host[D][k].element_size() for D in DS for k in outs)
+    compute = torch.cuda.current_stream(device)
+    up = torch.cuda.Stream(device)
+    down = torch.cuda.Stream(device)
+    ev = [dict(inputs=torch.cuda.Event(), computed=torch.cuda.Event(), fetched=torch.cuda.Event())
+          for _ in range(2)]
 
-    def one():
+    def one(k):
+        s, e = sets[k % 2], ev[k % 2]
+        with torch.cuda.stream(up):
+            up.wait_event(e["computed"])  # step k-2 is done reading this set's inputs
+            for D in DS:
+                for name in ins:
+                    s[D][name].copy_(host[D][name], non_blocking=True)
+            e["inputs"].record(up)
+        compute.wait_event(e["inputs"])
+        compute.wait_event(e["fetched"])  # step k-2's results have left this set
         for D in DS:
-            for k in ("x", "res", "g", "w"):
-                dev[D][k].copy_(host[D][k], non_blocking=True)
-        for D in DS:
-            d = dev[D]
+            d = s[D]
             rn.rmsnorm_fwd(d["x"], d["w"], cases[D].eps, 0.0, d["res"], out=d["out"],
                            new_residual=d["nr"])
         for D in DS:
-            d = dev[D]
+            d = s[D]
             rn.rmsnorm_vjp(d["nr"], d["w"], d["g"], cases[D].eps, 0.0, gx=d["gx"], gw=d["gw"])
-        for D in DS:
-            for k in ("out", "nr", "gx", "gw"):
-                host[D][k].copy_(dev[D][k], non_blocking=True)
+        e["computed"].record(compute)
+        with torch.cuda.stream(down):
+            down.wait_event(e["computed"])
+            for D in DS:
+                for name in outs:
+                    host[D][name].copy_(s[D][name], non_blocking=True)
+            e["fetched"].record(down)
 
-    for _ in range(warmup):
-        one()
+    for k in range(warmup):
+        one(k)
     torch.cuda.synchronize()
     barrier()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        one()
-    b.record()
+    a.record(compute)
+    for k in range(steps):
+        one(warmup + k)
+    compute.wait_stream(down)
+    b.record(compute)
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b), device)
     return ms / steps, h2d, d2h
@@ -465,12 +486,88 @@ def run_single_op(args):
     return 0
 
 
+def run_all_configs(args):
+    """Every workload configuration, fwd and VJP: µs per call with L2 flushed
+    before each call (cold), back to back (warm: small problems then live in
+    L2), and replayed from a CUDA graph of back-to-back calls (launch cost
+    amortised); GB/s of algorithmic bytes.  Prints one table row per case."""
+    from rmsnorm_fwd_bwd_add_gb300 import build, workloads as W
+    import rmsnorm_fwd_bwd_add_gb300 as rn
+    build.build()
+    dev = torch.device("cuda", 0)
+    # Evicts L2 by reading 512 MB (a read leaves clean lines: the timed call does
+    # not pay for write-backs of the flush itself).
+    flush = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+    cases = [W.config1()]
+    cases += [W.config2(r, D, gm) for r in W.DECODE_ROWS for D in W.DECODE_D for gm in (False, True)]
+    cases += [W.config3()]
+    cases += [W.config4(D) for D in W.PREFILL_D]
+    cases += [W.config5(D, dt) for D in W.SWEEP_D for dt in (torch.float16, torch.bfloat16)]
+    print("%-22s %-4s %-62s %9s %9s %9s %9s" % ("case", "op", "plan", "cold_us", "warm_us",
+                                               "graph_us", "cold_GB/s"), flush=True)
+    for c in cases:
+        x, w = c.x.to(dev), c.w.to(dev)
+        res = c.residual.to(dev) if c.residual is not None else None
+        g = c.g.to(dev)
+        out, nr, gx = torch.empty_like(x), torch.empty_like(x) if res is not None else None, torch.empty_like(x)
+        gw = torch.empty(c.D, dtype=torch.float32, device=dev)
+        ws = torch.empty(max(256, rn.rmsnorm_vjp_workspace_size(c.rows, c.D, c.dtype)),
+                         dtype=torch.uint8, device=dev)
+        ops = [("fwd", lambda: rn.rmsnorm_fwd(x, w, c.eps, c.weight_bias, res, out=out, new_residual=nr),
+                fwd_bytes(c.rows, c.D, res is not None, 2))]
+        ops.append(("vjp", lambda: rn.rmsnorm_vjp_ws(x, w, g, c.eps, c.weight_bias, workspace=ws,
+                                                     gx=gx, gw=gw), vjp_bytes(c.rows, c.D, 2)))
+        for name, f, nbytes in ops:
+            for _ in range(5):
+                f()
+            torch.cuda.synchronize()
+            cold = []
+            for _ in range(20):
+                flush.sum()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                f()
+                b.record()
+                torch.cuda.synchronize()
+                cold.append(1e3 * a.elapsed_time(b))
+            n = 50
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(n):
+                f()
+            b.record()
+            torch.cuda.synchronize()
+            warm = 1e3 * a.elapsed_time(b) / n
+            s_ = torch.cuda.Stream()
+            s_.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s_):
+                f()
+            torch.cuda.current_stream().wait_stream(s_)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for _ in range(n):
+                    f()
+            graph.replay()
+            torch.cuda.synchronize()
+            a.record()
+            graph.replay()
+            b.record()
+            torch.cuda.synchronize()
+            graph_us = 1e3 * a.elapsed_time(b) / n
+            cold_us = statistics.median(cold)
+            plan = rn.rmsnorm_describe_dispatch(name, c.rows, c.D, c.dtype, res is not None)
+            print("%-22s %-4s %-62s %9.2f %9.2f %9.2f %9.1f" % (c.name, name, plan, cold_us, warm,
+                                                             graph_us, nbytes / cold_us / 1e3),
+                  flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------------------
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=1000)  # ~0.5 s of timed GPU work
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
@@ -481,6 +578,8 @@ def main(argv=None):
     ap.add_argument("--rows", type=int, default=8192)
     ap.add_argument("--D", type=int, default=8192)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--all-configs", action="store_true",
+                    help="table of µs/call and GB/s for every workload configuration; no JSON line")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.op is None:
         ap.error("--warmup must be at least 3")
@@ -488,6 +587,8 @@ def main(argv=None):
         return run_reference(args)
     if args.op is not None:
         return run_single_op(args)
+    if args.all_configs:
+        return run_all_configs(args)
 
     from rmsnorm_fwd_bwd_add_gb300 import build
     rank, world, local = dist_setup(args.gpus)
@@ -530,7 +631,10 @@ def main(argv=None):
         e2e_steps = max(3, min(args.steps, 30))
         ms_e2e, h2d, d2h = time_e2e(cases, device, e2e_steps, 3)
         e2e = {"value": world * STEP_BYTES / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "ms_per_step": ms_e2e,
+               "note": "public Python API, pinned host buffers; uploads, compute and "
+                       "downloads of consecutive steps overlap on three streams"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -51,10 +51,41 @@ def _rows_d(x: torch.Tensor) -> Tuple[int, int]:
     return (x.numel() // D if D else 0), D
 
 
+# The current stream's raw handle without building a Stream object (a private
+# torch entry point present in the supported versions; the public route is the
+# fallback).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(device: torch.device, stream) -> int:
-    if stream is None:
-        stream = torch.cuda.current_stream(device)
-    return stream.cuda_stream
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(device.index)
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+class _OnDevice:
+    """Makes `device` current for the C call (the library works on the current
+    device), switching only when it is not already."""
+
+    __slots__ = ("device", "prev")
+
+    def __init__(self, device: torch.device):
+        self.device = device
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.device.index:
+            self.prev = cur
+            torch.cuda.set_device(self.device)
+        return self
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+        return False
 
 
 def _check_w(w: torch.Tensor, x: torch.Tensor, D: int) -> None:
@@ -82,7 +113,7 @@ def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, weight_bias: float
         _check_like("new_residual", new_residual, x)
     elif new_residual is not None:
         raise ValueError("new_residual given without residual")
-    with torch.cuda.device(x.device):
+    with _OnDevice(x.device):
         st = _native.lib().rmsnorm_fwd(_ptr(x), _ptr(residual), _ptr(w), eps, weight_bias,
                                        _ptr(out), _ptr(new_residual), rows, D, code,
                                        _stream(x.device, stream))
@@ -112,7 +143,7 @@ def rmsnorm_vjp(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float,
     code = _dtype_code(x)
     _check_w(w, x, D)
     gx, gw = _vjp_outputs(x, g, gx, gw, D)
-    with torch.cuda.device(x.device):
+    with _OnDevice(x.device):
         st = _native.lib().rmsnorm_vjp(_ptr(x), _ptr(w), _ptr(g), eps, weight_bias, _ptr(gx),
                                        _ptr(gw), rows, D, code, _stream(x.device, stream))
     _native.check("rmsnorm_vjp", st)
@@ -135,7 +166,7 @@ def rmsnorm_vjp_ws(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float
     code = _dtype_code(x)
     _check_w(w, x, D)
     gx, gw = _vjp_outputs(x, g, gx, gw, D)
-    with torch.cuda.device(x.device):
+    with _OnDevice(x.device):
         if workspace is None:
             nbytes = rmsnorm_vjp_workspace_size(rows, D, x.dtype)
             workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=x.device)

@@ -14,8 +14,6 @@
 
 #include <algorithm>
 #include <atomic>
-#include <chrono>
-#include <random>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -60,7 +58,6 @@ std::mutex g_dev_mu;
 DevInfo g_dev[MAX_DEVICES];
 
 std::atomic<int64_t> g_drop_tile{-1};
-std::atomic<int> g_last_fused_error{0};  // last refused cooperative launch (diagnostics)
 std::atomic<long long> g_wait_budget{DEFAULT_WAIT_BUDGET};
 
 int cuda_fail(cudaError_t e) {
@@ -156,7 +153,6 @@ struct Tuning {
     int cfg = -1;    // staged configuration index
     int cps = 0;     // CTAs per SM (capped by what the registers allow)
     int stages = 0;  // maximum ring depth
-    int fuse = -1;   // 0: always sum gw with the separate kernel
 };
 
 Tuning parse_tuning() {
@@ -170,7 +166,6 @@ Tuning parse_tuning() {
         if (std::sscanf(tok, "cfg=%d", &v) == 1 && v >= 0 && v < N_STAGED_CFG) t.cfg = v;
         else if (std::sscanf(tok, "cps=%d", &v) == 1 && v >= 1 && v <= 3) t.cps = v;
         else if (std::sscanf(tok, "stages=%d", &v) == 1 && v >= 2 && v <= MAX_STAGES) t.stages = v;
-        else if (std::sscanf(tok, "fuse=%d", &v) == 1 && (v == 0 || v == 1)) t.fuse = v;
     }
     return t;
 }
@@ -254,32 +249,17 @@ bool plan_staged(int mode, int64_t rows, int D, int sm_count, int ci, Plan *p) {
     return true;
 }
 
-Plan make_plan_(int mode, int64_t rows, int D, bool aligned, int sm_count);
-
 Plan make_plan(int mode, int64_t rows, int D, bool aligned, int sm_count) {
-    Plan p = make_plan_(mode, rows, D, aligned, sm_count);
-    if (tuning().fuse == 0) p.fuse_gw = 0;
-    if (tuning().fuse == 1 && mode == MODE_VJP && p.tier == TIER_STAGED) p.fuse_gw = 1;
-    return p;
-}
-
-Plan make_plan_(int mode, int64_t rows, int D, bool aligned, int sm_count) {
     Plan p{};
     const int nv = D / 8;
     if (aligned && rows > DECODE_ROWS) {
         const int forced = tuning().cfg;
         if (forced >= 0 && nv <= STAGED_CFGS[forced].max_nv &&
             !(mode == MODE_VJP && forced == STAGED_CFG_WIDE) &&
-            plan_staged(mode, rows, D, sm_count, forced, &p)) {
-            p.fuse_gw = mode == MODE_VJP && tuning().fuse == 1;
+            plan_staged(mode, rows, D, sm_count, forced, &p))
             return p;
-        }
         for (int ci = 0; ci < STAGED_CFG_WIDE; ++ci) {
             if (nv <= STAGED_CFGS[ci].max_nv) {
-                // The gw sum stays a separate, programmatically dependent
-                // kernel here: measured on GB300 (rows 16384, D 4096/8192) it
-                // costs less than folding it in, because a cooperative launch
-                // cannot overlap the previous kernel's tail.
                 if (plan_staged(mode, rows, D, sm_count, ci, &p)) return p;
                 break;
             }
@@ -299,8 +279,6 @@ Plan make_plan_(int mode, int64_t rows, int D, bool aligned, int sm_count) {
                 p.num_tiles = rows;
                 const int64_t resident = std::max(1, 2048 / c.nt);
                 p.grid = (int)std::min<int64_t>(rows, (int64_t)sm_count * resident);
-                // decode: a handful of CTAs, one launch instead of two
-                p.fuse_gw = mode == MODE_VJP && rows <= DECODE_ROWS;
                 return p;
             }
         }
@@ -315,27 +293,9 @@ Plan make_plan_(int mode, int64_t rows, int D, bool aligned, int sm_count) {
     return p;
 }
 
-size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
-
-// VJP scratch: the [grid, D] fp32 partial rows, then one 64-bit publication
-// flag per CTA (used when the gw sum is folded into the kernel).
 size_t partials_bytes(const Plan &p, int64_t D) {
-    return align256((size_t)p.grid * (size_t)D * sizeof(float)) +
-           align256((size_t)p.grid * sizeof(unsigned long long));
-}
-
-// A value no earlier launch of this process used, and (seeded from the clock
-// and a random device) practically never one left in reused device memory by
-// another process.
-unsigned long long next_epoch() {
-    static const unsigned long long seed = [] {
-        std::random_device rd;
-        const unsigned long long t =
-            (unsigned long long)std::chrono::high_resolution_clock::now().time_since_epoch().count();
-        return ((unsigned long long)rd() << 32) ^ (unsigned long long)rd() ^ (t * 0x9E3779B97F4A7C15ull);
-    }();
-    static std::atomic<unsigned long long> counter{0};
-    return seed + 0x9E3779B97F4A7C15ull * (counter.fetch_add(1) + 1);
+    const size_t b = (size_t)p.grid * (size_t)D * sizeof(float);
+    return (b + 255) & ~(size_t)255;
 }
 
 cudaError_t launch_plan(int dtype, int mode, const Plan &p, const KernelArgs &a, cudaStream_t s) {
@@ -401,25 +361,10 @@ int vjp_run(const void *x, const void *w, const void *g, float eps, float weight
     a.out0 = gx;
     a.out1 = nullptr;
     a.partials = partials;
-    a.gw = gw;
-    a.flags = reinterpret_cast<unsigned long long *>(
-        reinterpret_cast<char *>(partials) + align256((size_t)p.grid * (size_t)D * sizeof(float)));
-    a.epoch = next_epoch();
-    a.fuse_gw = p.fuse_gw;
     cudaError_t e = launch_plan(dtype, MODE_VJP, p, a, s);
-    if (e != cudaSuccess && a.fuse_gw) {
-        g_last_fused_error.store((int)e);
-        // The cooperative launch was refused (nothing was launched): sum the
-        // partials with the separate stage-2 kernel instead.
-        (void)cudaGetLastError();
-        a.fuse_gw = 0;
-        e = launch_plan(dtype, MODE_VJP, p, a, s);
-    }
     if (e != cudaSuccess) return cuda_fail(e);
-    if (!a.fuse_gw) {
-        e = launch_gw_reduce(partials, gw, p.grid, (int)D, s);
-        if (e != cudaSuccess) return cuda_fail(e);
-    }
+    e = launch_gw_reduce(partials, gw, p.grid, (int)D, s);
+    if (e != cudaSuccess) return cuda_fail(e);
     return RMSNORM_OK;
 }
 
@@ -575,9 +520,9 @@ const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype
     if (current_device(&dev) != RMSNORM_OK) return "no-device";
     const int mode = op == 1 ? MODE_VJP : (has_residual ? MODE_FWD_RES : MODE_FWD_NORES);
     const Plan p = make_plan(mode, rows, (int)D, aligned && (D * 2) % 16 == 0, dev.sm_count);
-    std::snprintf(buf, sizeof(buf), "%s:cfg%d:nt%d:g%d:v%d:s%d:tr%d:grid%d:smem%zu%s",
+    std::snprintf(buf, sizeof(buf), "%s:cfg%d:nt%d:g%d:v%d:s%d:tr%d:grid%d:smem%zu",
                   tier_name(p.tier), p.cfg, p.nt, p.g, p.v, p.stages, p.tile_rows, p.grid,
-                  p.smem, p.fuse_gw ? ":fused" : "");
+                  p.smem);
     return buf;
 }
 

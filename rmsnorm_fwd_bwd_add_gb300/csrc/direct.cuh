@@ -16,7 +16,6 @@
 #pragma once
 
 #include "common.cuh"
-#include "gw_fused.cuh"
 #include "plan.h"
 
 namespace rmsn {
@@ -151,10 +150,6 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
                 dst[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
                 dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
             }
-        }
-        if (a.fuse_gw) {
-            __shared__ float fin[NWARPS * 33];
-            fused_gw_finish<NT>(a, fin);
         }
     }
 }

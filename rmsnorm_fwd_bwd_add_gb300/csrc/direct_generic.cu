@@ -18,8 +18,7 @@ namespace {
 
 template <typename T, int MODE, int NT, int V>
 cudaError_t direct_one(const Plan &p, const KernelArgs &a, cudaStream_t s) {
-    return launch_pdl(direct_kernel<T, MODE, NT, V>, dim3(p.grid), dim3(NT), 0, s, a.fuse_gw != 0,
-                      a);
+    return launch_pdl(direct_kernel<T, MODE, NT, V>, dim3(p.grid), dim3(NT), 0, s, a);
 }
 
 template <typename T, int MODE>
@@ -55,10 +54,10 @@ cudaError_t generic_t(int mode, const Plan &p, const KernelArgs &a, cudaStream_t
     const dim3 grid(p.grid), block(GENERIC_NT);
     switch (mode) {
         case MODE_FWD_RES:
-            return launch_pdl(generic_kernel<T, MODE_FWD_RES>, grid, block, 0, s, false, a);
+            return launch_pdl(generic_kernel<T, MODE_FWD_RES>, grid, block, 0, s, a);
         case MODE_FWD_NORES:
-            return launch_pdl(generic_kernel<T, MODE_FWD_NORES>, grid, block, 0, s, false, a);
-        case MODE_VJP: return launch_pdl(generic_kernel<T, MODE_VJP>, grid, block, 0, s, false, a);
+            return launch_pdl(generic_kernel<T, MODE_FWD_NORES>, grid, block, 0, s, a);
+        case MODE_VJP: return launch_pdl(generic_kernel<T, MODE_VJP>, grid, block, 0, s, a);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -77,7 +76,7 @@ cudaError_t launch_generic(int dtype, int mode, const Plan &p, const KernelArgs 
 
 cudaError_t launch_gw_reduce(const float *partials, float *gw, int P, int D, cudaStream_t s) {
     return launch_pdl(gw_reduce_kernel, dim3((unsigned int)((D + 31) / 32)), dim3(32 * GWR_CHUNKS),
-                      0, s, false, partials, gw, P, D);
+                      0, s, partials, gw, P, D);
 }
 
 }  // namespace rmsn

@@ -13,7 +13,7 @@ cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t s
     auto kern = staged_kernel<T, MODE, NT, G, V, MINB>;
     cudaError_t e = allow_max_dynamic_smem((const void *)kern, smem_mask);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(p.grid), dim3(NT), p.smem, stream, a.fuse_gw != 0, a);
+    return launch_pdl(kern, dim3(p.grid), dim3(NT), p.smem, stream, a);
 }
 
 template <typename T, int MODE>

@@ -34,25 +34,17 @@ inline cudaError_t allow_max_dynamic_smem(const void *func, std::atomic<uint64_t
 // Launches `kern` with programmatic stream serialisation: it may begin while
 // the previous kernel on the stream finishes, and every kernel of this library
 // waits (griddepcontrol.wait) before its first global memory access.
-// With `cooperative`, the launch instead guarantees that all CTAs are
-// resident at once (or fails without launching), which the folded gw sum
-// needs; such a launch waits for the previous kernel in the usual way.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t stream, bool cooperative, Args &&...args) {
+                       cudaStream_t stream, Args &&...args) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    if (cooperative) {
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-    } else {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-    }
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);

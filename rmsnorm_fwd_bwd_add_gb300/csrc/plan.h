@@ -31,11 +31,6 @@ struct KernelArgs {
     uint32_t stage_bytes;     // bytes of one full tile of one tensor
     long long wait_budget;    // SM cycles per bounded wait
     int64_t drop_tile;        // test hook: tile whose copy is never issued (-1: none)
-    // VJP with the gw sum folded in (cooperative launch, see gw_fused.cuh)
-    int fuse_gw;              // 1: the VJP kernel writes gw itself
-    float *gw;                // [D] fp32 output
-    unsigned long long *flags;  // [grid] publication flags
-    unsigned long long epoch;   // value unique to this launch
 };
 
 struct Plan {
@@ -50,7 +45,6 @@ struct Plan {
     int grid;          // CTAs; for the VJP also the number of gw partial rows
     size_t smem;       // dynamic shared memory bytes
     uint32_t stage_bytes;
-    int fuse_gw;       // VJP: fold the gw sum into the kernel (cooperative launch)
 };
 
 // Configuration tables (index = Plan::cfg).

@@ -32,7 +32,6 @@
 #pragma once
 
 #include "common.cuh"
-#include "gw_fused.cuh"
 #include "plan.h"
 
 namespace rmsn {
@@ -295,7 +294,6 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
                 prow[col] = sum;
             }
         }
-        if (a.fuse_gw) fused_gw_finish<NT>(a, reinterpret_cast<float *>(ring));
     }
 }
 
