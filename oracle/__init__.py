@@ -14,7 +14,8 @@ examples, invariants, central finite differences, mutation tests) by
 
 Sources (web pages, by title and section):
   * "Fused residual-add RMSNorm and fused RoPE + KV-append decode kernels",
-    Background (FusedAddRMSNorm bullet; two-output paragraph) -- the forward.
+    Background (FusedAddRMSNorm bullet; two-output paragraph) -- the forward,
+    and the two-output op whose full VJP fused_vjp computes.
   * "RMSNormVJP backward writes a full {n_rows, D} gw_temp intermediate",
     POC section (eager fp32 reference and the gradient check) -- the VJP.
 """
@@ -64,6 +65,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.rmsnorm_oracle_vjp.argtypes = [_dp, _dp, _dp, ctypes.c_double, ctypes.c_double,
                                        _dp, _dp, ctypes.c_int64, ctypes.c_int64]
     lib.rmsnorm_oracle_vjp.restype = None
+    lib.rmsnorm_oracle_fused_vjp.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_double, ctypes.c_double,
+                                             _dp, _dp, ctypes.c_int64, ctypes.c_int64]
+    lib.rmsnorm_oracle_fused_vjp.restype = None
     return lib
 
 
@@ -120,6 +124,23 @@ class Oracle:
         return gx, gw
 
 
+    def fused_vjp(self, h, w, g_out, eps, weight_bias=0.0, g_residual=None):
+        """VJP of the two-output fused op at h = x + residual: returns (g_h, gw),
+        g_h the gradient with respect to both x and residual."""
+        h = self._arr(h)
+        rows, D = h.shape
+        w = self._arr(w, (D,))
+        g_out = self._arr(g_out, (rows, D))
+        g_res = None if g_residual is None else self._arr(g_residual, (rows, D))
+        g_h = np.empty((rows, D), np.float64)
+        gw = np.empty((D,), np.float64)
+        self._lib.rmsnorm_oracle_fused_vjp(self._ptr(h), self._ptr(w), self._ptr(g_out),
+                                           self._ptr(g_res), self.scalar(eps),
+                                           self.scalar(weight_bias), self._ptr(g_h),
+                                           self._ptr(gw), rows, D)
+        return g_h, gw
+
+
 _ORACLE = None
 
 
@@ -137,3 +158,7 @@ def fwd(x, w, eps, weight_bias=0.0, residual=None):
 
 def vjp(x, w, g, eps, weight_bias=0.0):
     return load().vjp(x, w, g, eps, weight_bias)
+
+
+def fused_vjp(h, w, g_out, eps, weight_bias=0.0, g_residual=None):
+    return load().fused_vjp(h, w, g_out, eps, weight_bias, g_residual)

@@ -103,3 +103,24 @@ void rmsnorm_oracle_vjp(const double *x, const double *w, const double *g,
         }
     }
 }
+
+/*
+ * VJP of the two-output fused op (out, new_residual) = F(x, residual, w).
+ * With h = x + residual, out depending on h through the RMSNorm and
+ * new_residual = h, the loss L = sum(g_out * out) + sum(g_residual *
+ * new_residual) has
+ *     dL/dx = dL/dresidual = g_h = (VJP of out at h, g_out) + g_residual
+ *     dL/dw = gw of the plain VJP (new_residual does not depend on w).
+ * h is the tensor the forward normalised (its new_residual); g_residual may be
+ * NULL (no gradient reaches new_residual), which gives the plain VJP.
+ */
+void rmsnorm_oracle_fused_vjp(const double *h, const double *w, const double *g_out,
+                              const double *g_residual, double eps, double weight_bias,
+                              double *g_h, double *gw, int64_t rows, int64_t D)
+{
+    rmsnorm_oracle_vjp(h, w, g_out, eps, weight_bias, g_h, gw, rows, D);
+    if (g_residual) {
+        for (int64_t i = 0; i < rows * D; ++i)
+            g_h[i] = g_h[i] + g_residual[i];
+    }
+}

@@ -260,6 +260,57 @@ def pin_scaled_weight(orc):
     _close(gwa, gw, 1e-13, 1e-15, "gw does not depend on w")
 
 
+def _fused_loss(orc, x, res, w, g_out, g_res, eps, wb):
+    out, new_res = orc.fwd(x, w, eps, wb, res)
+    return float(np.sum(g_out * out) + np.sum(g_res * new_res))
+
+
+def pin_fused_vjp_finite_differences(orc):
+    """The two-output op's VJP: central differences of
+    L = sum(g_out * out) + sum(g_res * new_residual) with respect to x, to
+    residual and to w, through the forward only."""
+    rng = _rng(20)
+    for (R, D, eps, wb) in ((2, 6, 1e-4, 0.0), (3, 5, 1e-2, 1.0)):
+        x = rng.normal(size=(R, D))
+        res = rng.normal(size=(R, D))
+        w = rng.normal(0.5, 0.5, size=D)
+        g_out = rng.normal(size=(R, D))
+        g_res = rng.normal(size=(R, D))
+        g_h, gw = orc.fused_vjp(x + res, w, g_out, eps, wb, g_res)
+        fd_x = np.zeros_like(x)
+        fd_r = np.zeros_like(x)
+        for i in range(R):
+            for j in range(D):
+                for arr, fd in ((x, fd_x), (res, fd_r)):
+                    d = 1e-5 * (1.0 + abs(arr[i, j]))
+                    keep = arr[i, j]
+                    arr[i, j] = keep + d
+                    lp = _fused_loss(orc, x, res, w, g_out, g_res, eps, wb)
+                    arr[i, j] = keep - d
+                    lm = _fused_loss(orc, x, res, w, g_out, g_res, eps, wb)
+                    arr[i, j] = keep
+                    fd[i, j] = (lp - lm) / (2 * d)
+        fd_w = np.zeros(D)
+        for j in range(D):
+            d = 1e-5 * (1.0 + abs(w[j]))
+            wp = w.copy(); wp[j] += d
+            wm = w.copy(); wm[j] -= d
+            fd_w[j] = (_fused_loss(orc, x, res, wp, g_out, g_res, eps, wb)
+                       - _fused_loss(orc, x, res, wm, g_out, g_res, eps, wb)) / (2 * d)
+        scale = max(1.0, float(np.max(np.abs(g_h))))
+        _close(g_h, fd_x, 1e-6, 1e-6 * scale, "fused fd d/dx")
+        _close(g_h, fd_r, 1e-6, 1e-6 * scale, "fused fd d/dresidual")
+        _close(gw, fd_w, 1e-6, 1e-6 * max(1.0, float(np.max(np.abs(gw)))), "fused fd d/dw")
+    # without a residual gradient it is the plain VJP
+    h = rng.normal(size=(2, 7))
+    w = rng.normal(size=7)
+    g = rng.normal(size=(2, 7))
+    a = orc.fused_vjp(h, w, g, 1e-3, 0.5)
+    b = orc.vjp(h, w, g, 1e-3, 0.5)
+    _close(a[0], b[0], 0, 0, "fused without g_res")
+    _close(a[1], b[1], 0, 0, "fused gw without g_res")
+
+
 ALL_PINS = [
     pin_worked_examples,
     pin_constant_rows,
@@ -273,4 +324,5 @@ ALL_PINS = [
     pin_linearity_in_g,
     pin_row_permutation,
     pin_scaled_weight,
+    pin_fused_vjp_finite_differences,
 ]

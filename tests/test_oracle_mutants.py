@@ -42,6 +42,8 @@ MUTANTS = [
     ("vjp_gx_weight_bias_dropped", "gx[i * D + j] = r * gi[j] * (weight_bias + w[j])",
      "gx[i * D + j] = r * gi[j] * w[j]", 0),
     ("vjp_g_row0", "const double *gi = g + i * D;", "const double *gi = g;", 0),
+    ("fused_g_residual_dropped", "g_h[i] = g_h[i] + g_residual[i];", "g_h[i] = g_h[i];", 0),
+    ("fused_g_residual_sign", "g_h[i] = g_h[i] + g_residual[i];", "g_h[i] = g_h[i] - g_residual[i];", 0),
 ]
 
 
