@@ -51,6 +51,11 @@ def vjp_bytes(rows, D, s=ITEM):
     return 3 * rows * D * s + D * s + 4 * D
 
 
+def fused_vjp_bytes(rows, D, s=ITEM):
+    """The two-output op's VJP: h, g_out and g_residual read, g_h written."""
+    return 4 * rows * D * s + D * s + 4 * D
+
+
 STEP_BYTES = sum(fwd_bytes(ROWS, D) + vjp_bytes(ROWS, D) for D in DS)
 OPS = [("fwd_d%d" % D, D) for D in DS] + [("vjp_d%d" % D, D) for D in DS]
 OP_BYTES = {"fwd_d%d" % D: fwd_bytes(ROWS, D) for D in DS}
@@ -467,8 +472,10 @@ def run_single_op(args):
     def once():
         if args.op == "fwd":
             rn.rmsnorm_fwd(x, w, c.eps, 0.0, res, out=out, new_residual=nr)
-        else:
+        elif args.op == "vjp":
             rn.rmsnorm_vjp(x, w, g, c.eps, 0.0, gx=gx, gw=gw)
+        else:
+            rn.rmsnorm_fused_vjp(x, w, g, c.eps, 0.0, res, g_h=gx, gw=gw)
     for _ in range(args.warmup):
         once()
     torch.cuda.synchronize()
@@ -479,8 +486,9 @@ def run_single_op(args):
     b.record()
     torch.cuda.synchronize()
     us = 1e3 * a.elapsed_time(b) / args.reps
-    nbytes = fwd_bytes(args.rows, args.D) if args.op == "fwd" else vjp_bytes(args.rows, args.D)
-    plan = rn.rmsnorm_describe_dispatch(args.op, args.rows, args.D, torch.bfloat16, True)
+    nbytes = {"fwd": fwd_bytes, "vjp": vjp_bytes, "fvjp": fused_vjp_bytes}[args.op](args.rows, args.D)
+    plan = rn.rmsnorm_describe_dispatch("fwd" if args.op == "fwd" else "vjp", args.rows, args.D,
+                                        torch.bfloat16, args.op != "vjp")
     print("op=%s rows=%d D=%d plan=%s us=%.2f GB/s=%.1f" % (args.op, args.rows, args.D, plan, us,
                                                           nbytes / us / 1e3), flush=True)
     return 0
@@ -517,6 +525,11 @@ def run_all_configs(args):
                 fwd_bytes(c.rows, c.D, res is not None, 2))]
         ops.append(("vjp", lambda: rn.rmsnorm_vjp_ws(x, w, g, c.eps, c.weight_bias, workspace=ws,
                                                      gx=gx, gw=gw), vjp_bytes(c.rows, c.D, 2)))
+        if res is not None and c.config == 4:
+            # the two-output op's VJP, with the residual standing in for g_residual
+            ops.append(("fvjp", lambda: rn.rmsnorm_fused_vjp(x, w, g, c.eps, c.weight_bias, res,
+                                                             g_h=gx, gw=gw),
+                        fused_vjp_bytes(c.rows, c.D, 2)))
         for name, f, nbytes in ops:
             for _ in range(5):
                 f()
@@ -555,7 +568,8 @@ def run_all_configs(args):
             torch.cuda.synchronize()
             graph_us = 1e3 * a.elapsed_time(b) / n
             cold_us = statistics.median(cold)
-            plan = rn.rmsnorm_describe_dispatch(name, c.rows, c.D, c.dtype, res is not None)
+            plan = rn.rmsnorm_describe_dispatch("fwd" if name == "fwd" else "vjp", c.rows, c.D,
+                                                c.dtype, name != "vjp" and res is not None)
             print("%-22s %-4s %-62s %9.2f %9.2f %9.2f %9.1f" % (c.name, name, plan, cold_us, warm,
                                                              graph_us, nbytes / cold_us / 1e3),
                   flush=True)
@@ -572,7 +586,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=("fwd", "vjp"),
+    ap.add_argument("--op", choices=("fwd", "vjp", "fvjp"),
                     help="profiling mode: run one op of the prefill recipe at --rows x --D "
                          "(--reps launches after --warmup) and print its mean time; no JSON line")
     ap.add_argument("--rows", type=int, default=8192)

@@ -124,6 +124,25 @@ int rmsnorm_vjp(const void *x, const void *w, const void *g, float eps,
                 int dtype, void *stream);
 
 /*
+ * VJP of the two-output fused op (out, new_residual) = fused forward of
+ * (x, residual, w).  Source: "Fused residual-add RMSNorm and fused RoPE +
+ * KV-append decode kernels", Background: the residual update is a second
+ * output, so a gradient can reach it as well as out.
+ *   h           [rows, D] dtype, the new_residual the forward produced.
+ *   g_out       [rows, D] dtype, the gradient of out.
+ *   g_residual  [rows, D] dtype, the gradient of new_residual, or NULL (none).
+ *   g_h         [rows, D] dtype, receives VJP(h, g_out) + g_residual, rounded
+ *               once: the gradient with respect to x and to residual alike.
+ *   gw          [D] fp32, as for rmsnorm_vjp (new_residual does not depend on w).
+ * One pass over h, g_out and g_residual; scratch, errors and aliasing (g_h may
+ * be g_out or g_residual) as for rmsnorm_vjp.  With g_residual == NULL this is
+ * rmsnorm_vjp.
+ */
+int rmsnorm_fused_vjp(const void *h, const void *w, const void *g_out,
+                      const void *g_residual, float eps, float weight_bias, void *g_h,
+                      float *gw, int64_t rows, int64_t D, int dtype, void *stream);
+
+/*
  * Bytes of scratch rmsnorm_vjp_ws needs for this problem on the current
  * device (0 when rows == 0).  Returns 0 for invalid arguments as well.
  */
@@ -196,8 +215,9 @@ int rmsnorm_device_status(unsigned int *bits, int clear);
 int rmsnorm_debug_inject(int64_t drop_tile, int64_t budget_cycles);
 
 /*
- * Describes the kernel plan rmsnorm_fwd (op = 0) or rmsnorm_vjp (op = 1)
- * would use for this problem and pointer alignment on the current device, as a
+ * Describes the kernel plan rmsnorm_fwd (op = 0) or rmsnorm_vjp (op = 1;
+ * with has_residual, rmsnorm_fused_vjp with a g_residual) would use for this
+ * problem and pointer alignment on the current device, as a
  * static string such as "staged:cfg8:nt512:g512:v2:s6:tr1:grid152:smem..."; for
  * tests and benchmarks.
  */

@@ -7,6 +7,9 @@ include/rmsnorm.h (librmsnorm_gb300.so), with these thin Python bindings:
                   (out, new_residual), fp32 accumulation, weight_bias scalar.
   rmsnorm_vjp  -- RMSNorm VJP: gx and an fp32 gw reduced across rows inside
                   the kernels (deterministic, no [rows, D] temporary).
+  rmsnorm_fused_vjp -- VJP of the two-output fused op (adds the gradient that
+                  reaches new_residual in the same pass).
+  fused_add_rmsnorm, rms_norm -- torch.autograd wrappers.
 
 PyTorch supplies device memory and streams only.
 """
@@ -14,6 +17,7 @@ from .api import (  # noqa: F401
     rmsnorm_debug_inject,
     rmsnorm_describe_dispatch,
     rmsnorm_device_status,
+    rmsnorm_fused_vjp,
     rmsnorm_fwd,
     rmsnorm_status_string,
     rmsnorm_vjp,
@@ -21,10 +25,14 @@ from .api import (  # noqa: F401
     rmsnorm_vjp_ws,
 )
 from ._native import DEVSTATUS_WAIT_TIMEOUT, MAX_D, RmsnormError  # noqa: F401
+from .autograd import fused_add_rmsnorm, rms_norm  # noqa: F401
 
 __all__ = [
     "rmsnorm_fwd",
     "rmsnorm_vjp",
+    "rmsnorm_fused_vjp",
+    "fused_add_rmsnorm",
+    "rms_norm",
     "rmsnorm_vjp_ws",
     "rmsnorm_vjp_workspace_size",
     "rmsnorm_device_status",

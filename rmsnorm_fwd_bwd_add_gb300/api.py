@@ -150,6 +150,27 @@ def rmsnorm_vjp(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float,
     return gx, gw
 
 
+def rmsnorm_fused_vjp(h: torch.Tensor, w: torch.Tensor, g_out: torch.Tensor, eps: float,
+                      weight_bias: float = 0.0, g_residual: Optional[torch.Tensor] = None, *,
+                      g_h: Optional[torch.Tensor] = None, gw: Optional[torch.Tensor] = None,
+                      stream=None):
+    """VJP of the two-output fused op at h (its new_residual): returns
+    (g_h, gw), g_h = VJP(h, g_out) + g_residual the gradient with respect to
+    both x and residual."""
+    rows, D = _rows_d(h)
+    code = _dtype_code(h)
+    _check_w(w, h, D)
+    if g_residual is not None:
+        _check_like("g_residual", g_residual, h)
+    g_h, gw = _vjp_outputs(h, g_out, g_h, gw, D)
+    with _OnDevice(h.device):
+        st = _native.lib().rmsnorm_fused_vjp(_ptr(h), _ptr(w), _ptr(g_out), _ptr(g_residual), eps,
+                                             weight_bias, _ptr(g_h), _ptr(gw), rows, D, code,
+                                             _stream(h.device, stream))
+    _native.check("rmsnorm_fused_vjp", st)
+    return g_h, gw
+
+
 def rmsnorm_vjp_workspace_size(rows: int, D: int, dtype: torch.dtype) -> int:
     """Bytes of scratch rmsnorm_vjp_ws needs on the current device."""
     return int(_native.lib().rmsnorm_vjp_workspace_size(rows, D, _DTYPES[dtype]))

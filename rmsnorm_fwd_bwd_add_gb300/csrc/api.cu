@@ -180,7 +180,7 @@ const Tuning &tuning() {
 // (at least one).  An explicit RMSNORM_TUNE stages= wins.
 int ring_stages(int mode, size_t per_stage, int cps) {
     if (tuning().stages) return tuning().stages;
-    const size_t target = mode == MODE_VJP ? INFLIGHT_VJP : INFLIGHT_FWD;
+    const size_t target = is_vjp(mode) ? INFLIGHT_VJP : INFLIGHT_FWD;
     const size_t per_sm_stage = per_stage * (size_t)cps;
     const int ahead = (int)std::max<size_t>(1, (target + per_sm_stage / 2) / per_sm_stage);
     return std::min(MAX_STAGES, 1 + ahead);
@@ -189,7 +189,7 @@ int ring_stages(int mode, size_t per_stage, int cps) {
 bool plan_staged(int mode, int64_t rows, int D, int sm_count, int ci, Plan *p) {
     const StagedCfg &c = STAGED_CFGS[ci];
     const Tuning &tu = tuning();
-    const int ntens = mode == MODE_FWD_NORES ? 1 : 2;
+    const int ntens = input_tensors(mode);
     const size_t row_bytes = (size_t)D * 2;
     const int max_stages = tu.stages ? tu.stages : MAX_STAGES;
     const int cps_max = staged_max_ctas_per_sm(mode, c.nt, c.g, c.v);
@@ -216,7 +216,7 @@ bool plan_staged(int mode, int64_t rows, int D, int sm_count, int ci, Plan *p) {
                                           ring_stages(mode, per_stage, cps));
         if (p->stages < 2) return false;
         p->smem = STAGED_HEADER_BYTES + (size_t)p->stages * per_stage;
-        if (mode == MODE_VJP)  // the cross-group gw sum reuses the ring
+        if (is_vjp(mode))  // the cross-group gw sum reuses the ring
             p->smem = std::max(p->smem, (size_t)STAGED_HEADER_BYTES + (size_t)ng * D * 4);
     } else {
         // One row per tile, the whole CTA on it.  Two CTAs per SM when the
@@ -255,7 +255,7 @@ Plan make_plan(int mode, int64_t rows, int D, bool aligned, int sm_count) {
     if (aligned && rows > DECODE_ROWS) {
         const int forced = tuning().cfg;
         if (forced >= 0 && nv <= STAGED_CFGS[forced].max_nv &&
-            !(mode == MODE_VJP && forced == STAGED_CFG_WIDE) &&
+            !(is_vjp(mode) && forced == STAGED_CFG_WIDE) &&
             plan_staged(mode, rows, D, sm_count, forced, &p))
             return p;
         for (int ci = 0; ci < STAGED_CFG_WIDE; ++ci) {
@@ -268,7 +268,7 @@ Plan make_plan(int mode, int64_t rows, int D, bool aligned, int sm_count) {
     if (aligned) {
         for (int ci = 0; ci < N_DIRECT_CFG; ++ci) {
             const DirectCfg &c = DIRECT_CFGS[ci];
-            if (nv <= c.max_nv && !(mode == MODE_VJP && c.v > 2)) {
+            if (nv <= c.max_nv && !(is_vjp(mode) && c.v > 2)) {
                 p = Plan{};
                 p.tier = TIER_DIRECT;
                 p.cfg = ci;
@@ -324,10 +324,11 @@ KernelArgs base_args(const DevInfo &dev, const Plan &p, float eps, float wb, int
 }
 
 // Validation shared by the VJP entry points; *plan is filled on success when
-// rows > 0.
-int vjp_prepare(const void *x, const void *w, const void *g, float eps, float weight_bias,
-                void *gx, float *gw, int64_t rows, int64_t D, int dtype, DevInfo *dev,
-                Plan *plan) {
+// rows > 0.  g_res (the gradient reaching new_residual of the fused op) is
+// null for the plain VJP.
+int vjp_prepare(const void *x, const void *w, const void *g, const void *g_res, float eps,
+                float weight_bias, void *gx, float *gw, int64_t rows, int64_t D, int dtype,
+                DevInfo *dev, Plan *plan) {
     int st = check_common(rows, D, dtype, eps, weight_bias);
     if (st != RMSNORM_OK) return st;
     if (!w || !gw) return RMSNORM_ERR_INVALID_ARG;
@@ -336,36 +337,69 @@ int vjp_prepare(const void *x, const void *w, const void *g, float eps, float we
         if (!x || !g || !gx) return RMSNORM_ERR_INVALID_ARG;
         const size_t n = (size_t)rows * (size_t)D * 2;
         if (overlaps(gx, n, gw, ngw)) return RMSNORM_ERR_INVALID_ARG;
-        if (bad_alias(gx, n, x, n) || bad_alias(gx, n, g, n) || overlaps(gx, n, w, nw))
+        if (bad_alias(gx, n, x, n) || bad_alias(gx, n, g, n) || bad_alias(gx, n, g_res, n) ||
+            overlaps(gx, n, w, nw))
             return RMSNORM_ERR_INVALID_ARG;
-        if (overlaps(gw, ngw, x, n) || overlaps(gw, ngw, g, n)) return RMSNORM_ERR_INVALID_ARG;
+        if (overlaps(gw, ngw, x, n) || overlaps(gw, ngw, g, n) || overlaps(gw, ngw, g_res, n))
+            return RMSNORM_ERR_INVALID_ARG;
     }
     if (overlaps(gw, ngw, w, nw)) return RMSNORM_ERR_INVALID_ARG;
     st = current_device(dev);
     if (st != RMSNORM_OK) return st;
     if (rows > 0) {
         const bool aligned = (D * 2) % 16 == 0 && aligned16(x) && aligned16(g) && aligned16(gx) &&
-                             aligned16(w);
-        *plan = make_plan(MODE_VJP, rows, (int)D, aligned, dev->sm_count);
+                             aligned16(w) && (!g_res || aligned16(g_res));
+        *plan = make_plan(g_res ? MODE_VJP_ADD : MODE_VJP, rows, (int)D, aligned, dev->sm_count);
     }
     return RMSNORM_OK;
 }
 
-int vjp_run(const void *x, const void *w, const void *g, float eps, float weight_bias, void *gx,
-            float *gw, int64_t rows, int64_t D, int dtype, const DevInfo &dev, const Plan &p,
-            float *partials, cudaStream_t s) {
+int vjp_run(const void *x, const void *w, const void *g, const void *g_res, float eps,
+            float weight_bias, void *gx, float *gw, int64_t rows, int64_t D, int dtype,
+            const DevInfo &dev, const Plan &p, float *partials, cudaStream_t s) {
     KernelArgs a = base_args(dev, p, eps, weight_bias, rows, D);
     a.in0 = x;
     a.in1 = g;
+    a.in2 = g_res;
     a.w = w;
     a.out0 = gx;
     a.out1 = nullptr;
     a.partials = partials;
-    cudaError_t e = launch_plan(dtype, MODE_VJP, p, a, s);
+    cudaError_t e = launch_plan(dtype, g_res ? MODE_VJP_ADD : MODE_VJP, p, a, s);
     if (e != cudaSuccess) return cuda_fail(e);
     e = launch_gw_reduce(partials, gw, p.grid, (int)D, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return RMSNORM_OK;
+}
+
+// The VJP with scratch from the library's stream-ordered pool.
+int vjp_pooled(const void *x, const void *w, const void *g, const void *g_res, float eps,
+               float weight_bias, void *gx, float *gw, int64_t rows, int64_t D, int dtype,
+               void *stream) {
+    DevInfo dev;
+    Plan p{};
+    int st = vjp_prepare(x, w, g, g_res, eps, weight_bias, gx, gw, rows, D, dtype, &dev, &p);
+    if (st != RMSNORM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (rows == 0) {
+        cudaError_t e = cudaMemsetAsync(gw, 0, (size_t)D * sizeof(float), s);
+        return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e);
+    }
+    cudaMemPool_t pool = nullptr;
+    st = scratch_pool(&pool);
+    if (st != RMSNORM_OK) return st;
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, partials_bytes(p, D), pool, s);
+    if (e == cudaErrorMemoryAllocation) {
+        (void)cudaGetLastError();
+        return RMSNORM_ERR_NO_MEMORY;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = vjp_run(x, w, g, g_res, eps, weight_bias, gx, gw, rows, D, dtype, dev, p,
+                 static_cast<float *>(ws), s);
+    e = cudaFreeAsync(ws, s);
+    if (st == RMSNORM_OK && e != cudaSuccess) st = cuda_fail(e);
+    return st;
 }
 
 const char *tier_name(int t) {
@@ -426,7 +460,7 @@ int rmsnorm_vjp_ws(const void *x, const void *w, const void *g, float eps, float
                    size_t workspace_bytes, void *stream) {
     DevInfo dev;
     Plan p{};
-    int st = vjp_prepare(x, w, g, eps, weight_bias, gx, gw, rows, D, dtype, &dev, &p);
+    int st = vjp_prepare(x, w, g, nullptr, eps, weight_bias, gx, gw, rows, D, dtype, &dev, &p);
     if (st != RMSNORM_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (rows == 0) {
@@ -441,36 +475,19 @@ int rmsnorm_vjp_ws(const void *x, const void *w, const void *g, float eps, float
         overlaps(workspace, need, gx, n) || overlaps(workspace, need, w, (size_t)D * 2) ||
         overlaps(workspace, need, gw, (size_t)D * 4))
         return RMSNORM_ERR_INVALID_ARG;
-    return vjp_run(x, w, g, eps, weight_bias, gx, gw, rows, D, dtype, dev, p,
+    return vjp_run(x, w, g, nullptr, eps, weight_bias, gx, gw, rows, D, dtype, dev, p,
                    static_cast<float *>(workspace), s);
 }
 
 int rmsnorm_vjp(const void *x, const void *w, const void *g, float eps, float weight_bias,
                 void *gx, float *gw, int64_t rows, int64_t D, int dtype, void *stream) {
-    DevInfo dev;
-    Plan p{};
-    int st = vjp_prepare(x, w, g, eps, weight_bias, gx, gw, rows, D, dtype, &dev, &p);
-    if (st != RMSNORM_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (rows == 0) {
-        cudaError_t e = cudaMemsetAsync(gw, 0, (size_t)D * sizeof(float), s);
-        return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e);
-    }
-    cudaMemPool_t pool = nullptr;
-    st = scratch_pool(&pool);
-    if (st != RMSNORM_OK) return st;
-    void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, partials_bytes(p, D), pool, s);
-    if (e == cudaErrorMemoryAllocation) {
-        (void)cudaGetLastError();
-        return RMSNORM_ERR_NO_MEMORY;
-    }
-    if (e != cudaSuccess) return cuda_fail(e);
-    st = vjp_run(x, w, g, eps, weight_bias, gx, gw, rows, D, dtype, dev, p,
-                 static_cast<float *>(ws), s);
-    e = cudaFreeAsync(ws, s);
-    if (st == RMSNORM_OK && e != cudaSuccess) st = cuda_fail(e);
-    return st;
+    return vjp_pooled(x, w, g, nullptr, eps, weight_bias, gx, gw, rows, D, dtype, stream);
+}
+
+int rmsnorm_fused_vjp(const void *h, const void *w, const void *g_out, const void *g_residual,
+                      float eps, float weight_bias, void *g_h, float *gw, int64_t rows, int64_t D,
+                      int dtype, void *stream) {
+    return vjp_pooled(h, w, g_out, g_residual, eps, weight_bias, g_h, gw, rows, D, dtype, stream);
 }
 
 const char *rmsnorm_status_string(int status) {
@@ -518,7 +535,8 @@ const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype
         return "invalid";
     DevInfo dev;
     if (current_device(&dev) != RMSNORM_OK) return "no-device";
-    const int mode = op == 1 ? MODE_VJP : (has_residual ? MODE_FWD_RES : MODE_FWD_NORES);
+    const int mode = op == 1 ? (has_residual ? MODE_VJP_ADD : MODE_VJP)
+                             : (has_residual ? MODE_FWD_RES : MODE_FWD_NORES);
     const Plan p = make_plan(mode, rows, (int)D, aligned && (D * 2) % 16 == 0, dev.sm_count);
     std::snprintf(buf, sizeof(buf), "%s:cfg%d:nt%d:g%d:v%d:s%d:tr%d:grid%d:smem%zu",
                   tier_name(p.tier), p.cfg, p.nt, p.g, p.v, p.stages, p.tile_rows, p.grid,

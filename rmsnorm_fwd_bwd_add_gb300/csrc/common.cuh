@@ -14,8 +14,14 @@
 
 namespace rmsn {
 
-// Kernel modes.
-enum : int { MODE_FWD_RES = 0, MODE_FWD_NORES = 1, MODE_VJP = 2 };
+// Kernel modes.  MODE_VJP_ADD is the VJP of the two-output fused op: the
+// plain VJP plus the gradient that reaches new_residual (a third input).
+enum : int { MODE_FWD_RES = 0, MODE_FWD_NORES = 1, MODE_VJP = 2, MODE_VJP_ADD = 3 };
+
+__host__ __device__ constexpr bool is_vjp(int mode) { return mode == MODE_VJP || mode == MODE_VJP_ADD; }
+__host__ __device__ constexpr int input_tensors(int mode) {
+    return mode == MODE_FWD_NORES ? 1 : mode == MODE_VJP_ADD ? 3 : 2;
+}
 
 // Bits of the device status word (must match RMSNORM_DEVSTATUS_* in rmsnorm.h).
 constexpr unsigned int DEVSTATUS_WAIT_TIMEOUT = 1u;

@@ -23,8 +23,9 @@ namespace rmsn {
 template <typename T, int MODE, int NT, int V>
 __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
     constexpr int NWARPS = NT / 32;
-    constexpr int NTENS = (MODE == MODE_FWD_NORES) ? 1 : 2;
-    constexpr bool VJP = (MODE == MODE_VJP);
+    constexpr int NTENS = input_tensors(MODE);
+    constexpr bool VJP = is_vjp(MODE);
+    constexpr bool ADD = (MODE == MODE_VJP_ADD);
     __shared__ float red[2][NWARPS][2];
 
     const int tid = threadIdx.x;
@@ -37,6 +38,7 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
     const float Df = (float)D;
     const uint4 *in0 = static_cast<const uint4 *>(a.in0);
     const uint4 *in1 = static_cast<const uint4 *>(a.in1);
+    const uint4 *in2 = static_cast<const uint4 *>(a.in2);
     const uint4 *wg = static_cast<const uint4 *>(a.w);
     uint4 *out0 = static_cast<uint4 *>(a.out0);
     uint4 *out1 = static_cast<uint4 *>(a.out1);
@@ -51,13 +53,14 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
     int it = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, ++it) {
         const size_t base = (size_t)row * NV;
-        uint4 v0[V], v1[V];
+        uint4 v0[V], v1[V], v2[ADD ? V : 1];
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = tid + j * NT;
             if (vi < NV) {
                 v0[j] = ld_stream(in0 + base + vi);
-                if constexpr (NTENS == 2) v1[j] = ld_stream(in1 + base + vi);
+                if constexpr (NTENS >= 2) v1[j] = ld_stream(in1 + base + vi);
+                if constexpr (ADD) v2[j] = ld_stream(in2 + base + vi);
             }
         }
         float sa = 0.f, sb = 0.f;
@@ -132,6 +135,12 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
                         const float gwp = f1[e] * (wb + wf[e]);
                         o[e] = r * (gwp - f0[e] * c);
                         acc[j][e] += (f1[e] * f0[e]) * r;
+                    }
+                    if constexpr (ADD) {
+                        float f2[8];
+                        unpack8<T>(v2[j], f2);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = o[e] + f2[e];  // + g_new_residual
                     }
                 }
                 st_global(out0 + base + vi, pack8<T>(o));

@@ -33,7 +33,7 @@ cudaError_t direct_mode(const Plan &p, const KernelArgs &a, cudaStream_t s) {
         case 5:
             // Four vectors of x and g per thread plus gw accumulators do not
             // fit 1024 threads' registers; the VJP never plans this config.
-            if constexpr (MODE == MODE_VJP) return cudaErrorInvalidValue;
+            if constexpr (is_vjp(MODE)) return cudaErrorInvalidValue;
             else return direct_one<T, MODE, 1024, 4>(p, a, s);
         default: return cudaErrorInvalidValue;
     }
@@ -45,6 +45,7 @@ cudaError_t direct_t(int mode, const Plan &p, const KernelArgs &a, cudaStream_t 
         case MODE_FWD_RES: return direct_mode<T, MODE_FWD_RES>(p, a, s);
         case MODE_FWD_NORES: return direct_mode<T, MODE_FWD_NORES>(p, a, s);
         case MODE_VJP: return direct_mode<T, MODE_VJP>(p, a, s);
+        case MODE_VJP_ADD: return direct_mode<T, MODE_VJP_ADD>(p, a, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -58,6 +59,7 @@ cudaError_t generic_t(int mode, const Plan &p, const KernelArgs &a, cudaStream_t
         case MODE_FWD_NORES:
             return launch_pdl(generic_kernel<T, MODE_FWD_NORES>, grid, block, 0, s, a);
         case MODE_VJP: return launch_pdl(generic_kernel<T, MODE_VJP>, grid, block, 0, s, a);
+        case MODE_VJP_ADD: return launch_pdl(generic_kernel<T, MODE_VJP_ADD>, grid, block, 0, s, a);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -22,7 +22,8 @@ template <typename T, int MODE>
 __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a) {
     constexpr int NT = GENERIC_NT;
     constexpr int NWARPS = NT / 32;
-    constexpr bool VJP = (MODE == MODE_VJP);
+    constexpr bool VJP = is_vjp(MODE);
+    constexpr bool ADD = (MODE == MODE_VJP_ADD);
     __shared__ float red[2][NWARPS][2];
 
     const int tid = threadIdx.x;
@@ -34,6 +35,7 @@ __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a)
     const float Df = (float)D;
     const T *in0 = static_cast<const T *>(a.in0);
     const T *in1 = static_cast<const T *>(a.in1);
+    const T *in2 = static_cast<const T *>(a.in2);
     const T *w = static_cast<const T *>(a.w);
     T *out0 = static_cast<T *>(a.out0);
     T *out1 = static_cast<T *>(a.out1);
@@ -86,7 +88,9 @@ __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a)
                 Cvt<T>::store1(out0 + base + c, (x * r) * wp);
             } else {
                 const float g = Cvt<T>::load1(in1 + base + c);
-                Cvt<T>::store1(out0 + base + c, r * (g * wp - x * cc));
+                float o = r * (g * wp - x * cc);
+                if constexpr (ADD) o = o + Cvt<T>::load1(in2 + base + c);  // + g_new_residual
+                Cvt<T>::store1(out0 + base + c, o);
                 prow[c] += (g * x) * r;
             }
         }

@@ -31,7 +31,7 @@ cudaError_t launch_staged_mode(const Plan &p, const KernelArgs &a, cudaStream_t 
         case 8: return launch_staged_one<T, MODE, 512, 512, 2>(p, a, s);
         case 9: return launch_staged_one<T, MODE, 1024, 1024, 2>(p, a, s);
         case 10:
-            if constexpr (MODE == MODE_VJP) return cudaErrorInvalidValue;
+            if constexpr (is_vjp(MODE)) return cudaErrorInvalidValue;
             else return launch_staged_one<T, MODE, 256, 256, 4>(p, a, s);
         default: return cudaErrorInvalidValue;
     }
@@ -43,6 +43,7 @@ cudaError_t launch_staged_t(int mode, const Plan &p, const KernelArgs &a, cudaSt
         case MODE_FWD_RES: return launch_staged_mode<T, MODE_FWD_RES>(p, a, s);
         case MODE_FWD_NORES: return launch_staged_mode<T, MODE_FWD_NORES>(p, a, s);
         case MODE_VJP: return launch_staged_mode<T, MODE_VJP>(p, a, s);
+        case MODE_VJP_ADD: return launch_staged_mode<T, MODE_VJP_ADD>(p, a, s);
         default: return cudaErrorInvalidValue;
     }
 }

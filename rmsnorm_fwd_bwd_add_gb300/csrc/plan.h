@@ -11,10 +11,12 @@ namespace rmsn {
 enum Tier : int { TIER_STAGED = 0, TIER_DIRECT = 1, TIER_GENERIC = 2 };
 
 // Kernel arguments.  in0 = x; in1 = residual (forward) or g (VJP);
-// out0 = out (forward) or gx (VJP); out1 = new_residual (forward).
+// in2 = the gradient of new_residual (fused-op VJP); out0 = out (forward), gx
+// (VJP) or gx + in2 (fused-op VJP); out1 = new_residual (forward).
 struct KernelArgs {
     const void *in0;
     const void *in1;
+    const void *in2;
     const void *w;
     void *out0;
     void *out1;
@@ -76,8 +78,8 @@ constexpr DirectCfg DIRECT_CFGS[N_DIRECT_CFG] = {
 // except the small-D VJP with three or four vectors per lane, which needs the
 // whole register file like every larger CTA.
 constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
-    return (nt <= 256 && mode != 2 && g == nt && v <= 2) ? 3
-           : (nt <= 256 && !(mode == 2 && v >= 3)) ? 2 : 1;
+    return (nt <= 256 && mode < 2 && g == nt && v <= 2) ? 3
+           : (nt <= 256 && !(mode >= 2 && v >= 3)) ? 2 : 1;
 }
 // CTAs per SM the plan uses unless tuned otherwise.
 constexpr int staged_ctas_per_sm(int mode, int nt, int g, int v) {

@@ -41,8 +41,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     constexpr int NWARPS = NT / 32;
     constexpr int NG = NT / G;  // rows processed side by side
     constexpr bool CTA_ROW = (G == NT);
-    constexpr int NTENS = (MODE == MODE_FWD_NORES) ? 1 : 2;
-    constexpr bool VJP = (MODE == MODE_VJP);
+    constexpr int NTENS = input_tensors(MODE);
+    constexpr bool VJP = is_vjp(MODE);
+    constexpr bool ADD = (MODE == MODE_VJP_ADD);
     static_assert(G <= 32 || G == NT, "a row belongs to at most one warp, or to the whole CTA");
     static_assert(NWARPS <= 32, "one warp total per lane");
 
@@ -69,6 +70,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
 
     const T *in0 = static_cast<const T *>(a.in0);
     const T *in1 = static_cast<const T *>(a.in1);
+    const T *in2 = static_cast<const T *>(a.in2);
     uint4 *out0 = static_cast<uint4 *>(a.out0);
     uint4 *out1 = static_cast<uint4 *>(a.out1);
 
@@ -89,8 +91,10 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
             uint64_t *bar = &full[issue_stage];
             mbar_arrive_expect_tx(bar, bytes * NTENS);
             bulk_g2s(stage_ptr(issue_stage, 0), in0 + row0 * D, bytes, bar, policy);
-            if constexpr (NTENS == 2)
+            if constexpr (NTENS >= 2)
                 bulk_g2s(stage_ptr(issue_stage, 1), in1 + row0 * D, bytes, bar, policy);
+            if constexpr (NTENS == 3)
+                bulk_g2s(stage_ptr(issue_stage, 2), in2 + row0 * D, bytes, bar, policy);
         }
         ++issued;
         issue_stage = issue_stage + 1 == S ? 0 : issue_stage + 1;
@@ -151,7 +155,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
             const int vi = gl + j * G;
             if (vi < NV) {
                 unpack8<T>(r0[vi], xa[j]);
-                if constexpr (NTENS == 2) unpack8<T>(r1[vi], xb[j]);
+                if constexpr (NTENS >= 2) unpack8<T>(r1[vi], xb[j]);
                 if constexpr (MODE == MODE_FWD_RES) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) xa[j][q] = f2add(xa[j][q], xb[j][q]);  // h
@@ -168,11 +172,12 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
         sb = d2.x + d2.y;
     };
 
-    // Outputs of one row from the registers load_row filled.
-    auto row_outputs = [&](const float2 (&xa)[V][4], const float2 (&xb)[V][4], int64_t row,
-                           float r, float dot) {
+    // Outputs of one row from the registers load_row filled (the fused-op VJP
+    // also reads its row of the new_residual gradient, r2, from the stage).
+    auto row_outputs = [&](const float2 (&xa)[V][4], const float2 (&xb)[V][4], const uint4 *r2,
+                           int64_t row, float r, float dot) {
         const size_t base = (size_t)row * NV;
-        const float2 r2 = make_float2(r, r);
+        const float2 rr = make_float2(r, r);
         const float c = (r * r) * (dot / Df);  // r^2 * dot / D
         const float2 nc2 = make_float2(-c, -c);
 #pragma unroll
@@ -184,12 +189,18 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float2 u = f2mul(xb[j][q], wp[j][q]);           // g w'
-                        o[q] = f2mul(f2fma(xa[j][q], nc2, u), r2);             // r (g w' - x c)
-                        acc[j][q] = f2fma(xb[j][q], f2mul(xa[j][q], r2), acc[j][q]);  // g x r
+                        o[q] = f2mul(f2fma(xa[j][q], nc2, u), rr);             // r (g w' - x c)
+                        acc[j][q] = f2fma(xb[j][q], f2mul(xa[j][q], rr), acc[j][q]);  // g x r
+                    }
+                    if constexpr (ADD) {
+                        float2 gr[4];
+                        unpack8<T>(r2[vi], gr);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) o[q] = f2add(o[q], gr[q]);  // + g_new_residual
                     }
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) o[q] = f2mul(f2mul(xa[j][q], r2), wp[j][q]);
+                    for (int q = 0; q < 4; ++q) o[q] = f2mul(f2mul(xa[j][q], rr), wp[j][q]);
                     if constexpr (MODE == MODE_FWD_RES) st_global(out1 + base + vi, pack8<T>(xa[j]));
                 }
                 st_global(out0 + base + vi, pack8<T>(o));
@@ -206,7 +217,8 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
             float2 xa[V][4], xb[V][4];
             float sa, sb;
             load_row(reinterpret_cast<const uint4 *>(stage_ptr(s, 0)),
-                     reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS - 1)), xa, xb, sa, sb);
+                     reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS >= 2 ? 1 : 0)), xa, xb, sa,
+                     sb);
             sa = group_sum<32>(sa);
             if constexpr (VJP) sb = group_sum<32>(sb);
             float2 *rb = red + (k & 1) * NWARPS;
@@ -222,7 +234,8 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
             tot.x = group_sum<32>(tot.x);
             if constexpr (VJP) tot.y = group_sum<32>(tot.y);
             const float r = rsqrtf(tot.x / Df + eps);
-            row_outputs(xa, xb, row, r, tot.y);
+            row_outputs(xa, xb, reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS - 1)), row, r,
+                        tot.y);
             if (++s == S) {
                 s = 0;
                 ph ^= 1u;
@@ -234,7 +247,8 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
             const int nr = (int)min((int64_t)TR, rows - row0);
             const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_budget);
             const uint4 *t0 = reinterpret_cast<const uint4 *>(stage_ptr(s, 0));
-            const uint4 *t1 = reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS - 1));
+            const uint4 *t1 = reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS >= 2 ? 1 : 0));
+            const uint4 *t2 = reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS - 1));
             for (int qb = 0; qb < TR; qb += NG) {  // same trip count in every lane
                 const int q = qb + gid;
                 const bool valid = q < nr;
@@ -243,7 +257,8 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
                 if (valid) load_row(t0 + (size_t)q * NV, t1 + (size_t)q * NV, xa, xb, sa, sb);
                 sa = group_sum<G>(sa);
                 if constexpr (VJP) sb = group_sum<G>(sb);
-                if (valid && ok) row_outputs(xa, xb, row0 + q, rsqrtf(sa / Df + eps), sb);
+                if (valid && ok)
+                    row_outputs(xa, xb, t2 + (size_t)q * NV, row0 + q, rsqrtf(sa / Df + eps), sb);
             }
             if (__syncthreads_or(!ok)) {  // the whole tile is consumed
                 fail(k);
