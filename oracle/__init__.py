@@ -18,6 +18,8 @@ Sources (web pages, by title and section):
     and the two-output op whose full VJP fused_vjp computes.
   * "RMSNormVJP backward writes a full {n_rows, D} gw_temp intermediate",
     POC section (eager fp32 reference and the gradient check) -- the VJP.
+  * "Fused residual-add RMSNorm and fused RoPE + KV-append decode kernels",
+    Background, third bullet -- the gated activation silu(x[:d]) * x[d:2d].
 """
 from __future__ import annotations
 
@@ -68,6 +70,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.rmsnorm_oracle_fused_vjp.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_double, ctypes.c_double,
                                              _dp, _dp, ctypes.c_int64, ctypes.c_int64]
     lib.rmsnorm_oracle_fused_vjp.restype = None
+    lib.rmsnorm_oracle_gated_silu.argtypes = [_dp, _dp, ctypes.c_int64, ctypes.c_int64]
+    lib.rmsnorm_oracle_gated_silu.restype = None
     return lib
 
 
@@ -141,6 +145,18 @@ class Oracle:
         return g_h, gw
 
 
+    def gated_silu(self, x):
+        """x: (rows, 2d) -> silu(x[:, :d]) * x[:, d:], shape (rows, d)."""
+        x = self._arr(x)
+        rows, two_d = x.shape
+        if two_d % 2:
+            raise ValueError("x must have an even number of columns")
+        d = two_d // 2
+        out = np.empty((rows, d), np.float64)
+        self._lib.rmsnorm_oracle_gated_silu(self._ptr(x), self._ptr(out), rows, d)
+        return out
+
+
 _ORACLE = None
 
 
@@ -162,3 +178,7 @@ def vjp(x, w, g, eps, weight_bias=0.0):
 
 def fused_vjp(h, w, g_out, eps, weight_bias=0.0, g_residual=None):
     return load().fused_vjp(h, w, g_out, eps, weight_bias, g_residual)
+
+
+def gated_silu(x):
+    return load().gated_silu(x)

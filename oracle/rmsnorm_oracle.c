@@ -124,3 +124,22 @@ void rmsnorm_oracle_fused_vjp(const double *h, const double *w, const double *g_
             g_h[i] = g_h[i] + g_residual[i];
     }
 }
+
+/*
+ * Gated activation of the decode loop ("Fused residual-add RMSNorm and fused
+ * RoPE + KV-append decode kernels", Background, third bullet): for each row
+ * of x = [a | b] (2*d values, a = the first d, b = the last d),
+ *     out_j = silu(a_j) * b_j,   silu(a) = a * sigmoid(a) = a / (1 + exp(-a)).
+ * x: rows * 2d, out: rows * d, row-major.
+ */
+void rmsnorm_oracle_gated_silu(const double *x, double *out, int64_t rows, int64_t d)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        const double *a = x + i * 2 * d;
+        const double *b = a + d;
+        for (int64_t j = 0; j < d; ++j) {
+            double silu = a[j] / (1.0 + exp(-a[j]));
+            out[i * d + j] = silu * b[j];
+        }
+    }
+}

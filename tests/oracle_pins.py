@@ -311,6 +311,39 @@ def pin_fused_vjp_finite_differences(orc):
     _close(a[1], b[1], 0, 0, "fused gw without g_res")
 
 
+def pin_gated_silu(orc):
+    """Gated activation: silu(a) - silu(-a) = a (since sigmoid(a) +
+    sigmoid(-a) = 1); silu(0) = 0; out is linear in the second half;
+    sigmoid(ln k) = k / (k + 1) gives exact values at a = ln k (ln from the math
+    library); silu(a) -> a for large a and -> 0 for very negative a."""
+    import math
+    rng = _rng(21)
+    d = 9
+    a = rng.normal(size=d) * 3
+    b1 = np.ones(d)
+    x = np.stack([np.concatenate([a, b1]), np.concatenate([-a, b1])])
+    out = orc.gated_silu(x)
+    _close(out[0] - out[1], a, 1e-13, 1e-14, "silu(a) - silu(-a) = a")
+    b = rng.normal(size=d)
+    z = orc.gated_silu(np.concatenate([np.zeros(d), b])[None, :])
+    _close(z, np.zeros((1, d)), 0, 0, "silu(0) = 0")
+    o1 = orc.gated_silu(np.concatenate([a, b])[None, :])
+    o2 = orc.gated_silu(np.concatenate([a, 2.5 * b])[None, :])
+    _close(o2, 2.5 * o1, 1e-14, 1e-15, "linear in the gate's second half")
+    ks = np.array([1.0, 3.0, 7.0, 0.25, 1.0 / 3.0])
+    av = np.array([math.log(k) for k in ks])
+    bv = np.array([4.0, 4.0, 8.0, 5.0, 4.0])
+    want = av * ks / (ks + 1.0) * bv
+    got = orc.gated_silu(np.concatenate([av, bv])[None, :])
+    _close(got, want[None, :], 1e-14, 1e-15, "silu(ln k) = ln k * k / (k + 1)")
+    big = orc.gated_silu(np.array([[40.0, -40.0, 1.0, 1.0]]))
+    _close(big[0, 0], 40.0, 1e-15, 0, "silu(40) ~ 40")
+    assert abs(big[0, 1]) < 1e-15, "silu(-40) ~ 0"
+    # rows are independent and the halves are taken per row
+    xs = rng.normal(size=(3, 2 * d))
+    _close(orc.gated_silu(xs)[1], orc.gated_silu(xs[1:2])[0], 0, 0, "row 1 alone")
+
+
 ALL_PINS = [
     pin_worked_examples,
     pin_constant_rows,
@@ -325,4 +358,5 @@ ALL_PINS = [
     pin_row_permutation,
     pin_scaled_weight,
     pin_fused_vjp_finite_differences,
+    pin_gated_silu,
 ]

@@ -44,6 +44,11 @@ MUTANTS = [
     ("vjp_g_row0", "const double *gi = g + i * D;", "const double *gi = g;", 0),
     ("fused_g_residual_dropped", "g_h[i] = g_h[i] + g_residual[i];", "g_h[i] = g_h[i];", 0),
     ("fused_g_residual_sign", "g_h[i] = g_h[i] + g_residual[i];", "g_h[i] = g_h[i] - g_residual[i];", 0),
+    ("silu_exp_sign", "a[j] / (1.0 + exp(-a[j]))", "a[j] / (1.0 + exp(a[j]))", 0),
+    ("silu_halves_swapped", "out[i * d + j] = silu * b[j];", "out[i * d + j] = b[j] / (1.0 + exp(-b[j])) * a[j];", 0),
+    ("silu_no_gate", "out[i * d + j] = silu * b[j];", "out[i * d + j] = silu;", 0),
+    ("silu_row_stride", "const double *a = x + i * 2 * d;", "const double *a = x + i * d;", 0),
+    ("silu_second_half_offset", "const double *b = a + d;", "const double *b = a + d - 1;", 0),
 ]
 
 
