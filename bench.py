@@ -51,6 +51,11 @@ def vjp_bytes(rows, D, s=ITEM):
     return 3 * rows * D * s + D * s + 4 * D
 
 
+def gate_bytes(rows, d, s=ITEM):
+    """Gated activation: 2d values read, d written per row."""
+    return 3 * rows * d * s
+
+
 def fused_vjp_bytes(rows, D, s=ITEM):
     """The two-output op's VJP: h, g_out and g_residual read, g_h written."""
     return 4 * rows * D * s + D * s + 4 * D
@@ -227,10 +232,25 @@ def recorded_traffic(op):
         return None
 
 
-def host_inputs():
+def device_inputs(device):
+    """The workload drawn on the GPU (seeded CUDA generator, same
+    distributions as the tests' CPU draws): fast at any number of ranks."""
     from rmsnorm_fwd_bwd_add_gb300 import workloads as W
-    cases = {D: W.config4(D, ROWS) for D in DS}
-    return cases
+    return {D: W.config4_on_device(D, device, ROWS) for D in DS}
+
+
+def to_host(cases, rows=None):
+    """Host copies of the cases (all rows, or the first `rows`)."""
+    import copy
+    out = {}
+    for D, c in cases.items():
+        h = copy.copy(c)
+        sl = slice(None) if rows is None else slice(0, rows)
+        h.x, h.residual, h.g = (t[sl].cpu() for t in (c.x, c.residual, c.g))
+        h.w = c.w.cpu()
+        h.rows = h.x.shape[0]
+        out[D] = h
+    return out
 
 
 class Step:
@@ -243,7 +263,7 @@ class Step:
         self.t = {}
         for D, c in cases.items():
             self.t[D] = dict(
-                x=c.x.to(device), res=c.residual.to(device), w=c.w.to(device), g=c.g.to(device),
+                x=c.x, res=c.residual, w=c.w, g=c.g,
                 out=torch.empty_like(c.x, device=device), nr=torch.empty_like(c.x, device=device),
                 gx=torch.empty_like(c.x, device=device),
                 gw=torch.empty(D, dtype=torch.float32, device=device))
@@ -427,7 +447,8 @@ def run_reference(args):
         return 0
     import oracle
     oracle.build()
-    cases = host_inputs()
+    from rmsnorm_fwd_bwd_add_gb300 import workloads as W
+    cases = {D: W.config4(D, 512) for D in DS}  # rows of the same recipe; a sample is taken below
     # size each step's sample so the whole run takes about a minute
     cal = oracle_sample(cases, 32)
     t0 = time.perf_counter()
@@ -464,13 +485,19 @@ def run_single_op(args):
     import rmsnorm_fwd_bwd_add_gb300 as rn
     build.build()
     dev = torch.device("cuda", 0)
-    c = W.config4(args.D, args.rows)
-    x, res, w, g = (t.to(dev) for t in (c.x, c.residual, c.w, c.g))
+    c = W.config4_on_device(args.D, dev, args.rows)
+    x, res, w, g = c.x, c.residual, c.w, c.g
     out, nr, gx = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
     gw = torch.empty(args.D, dtype=torch.float32, device=dev)
 
+    if args.op == "gate":  # x = [a | b] of width 2D from the same draws
+        xg = torch.cat([x, res], dim=1)
+        og = torch.empty_like(x)
+
     def once():
-        if args.op == "fwd":
+        if args.op == "gate":
+            rn.rmsnorm_gated_silu(xg, out=og)
+        elif args.op == "fwd":
             rn.rmsnorm_fwd(x, w, c.eps, 0.0, res, out=out, new_residual=nr)
         elif args.op == "vjp":
             rn.rmsnorm_vjp(x, w, g, c.eps, 0.0, gx=gx, gw=gw)
@@ -486,9 +513,11 @@ def run_single_op(args):
     b.record()
     torch.cuda.synchronize()
     us = 1e3 * a.elapsed_time(b) / args.reps
-    nbytes = {"fwd": fwd_bytes, "vjp": vjp_bytes, "fvjp": fused_vjp_bytes}[args.op](args.rows, args.D)
-    plan = rn.rmsnorm_describe_dispatch("fwd" if args.op == "fwd" else "vjp", args.rows, args.D,
-                                        torch.bfloat16, args.op != "vjp")
+    nbytes = {"fwd": fwd_bytes, "vjp": vjp_bytes, "fvjp": fused_vjp_bytes,
+              "gate": gate_bytes}[args.op](args.rows, args.D)
+    plan = ("gate" if args.op == "gate" else
+            rn.rmsnorm_describe_dispatch("fwd" if args.op == "fwd" else "vjp", args.rows, args.D,
+                                         torch.bfloat16, args.op != "vjp"))
     print("op=%s rows=%d D=%d plan=%s us=%.2f GB/s=%.1f" % (args.op, args.rows, args.D, plan, us,
                                                           nbytes / us / 1e3), flush=True)
     return 0
@@ -586,7 +615,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=("fwd", "vjp", "fvjp"),
+    ap.add_argument("--op", choices=("fwd", "vjp", "fvjp", "gate"),
                     help="profiling mode: run one op of the prefill recipe at --rows x --D "
                          "(--reps launches after --warmup) and print its mean time; no JSON line")
     ap.add_argument("--rows", type=int, default=8192)
@@ -614,7 +643,9 @@ def main(argv=None):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
 
-    cases = host_inputs()
+    if world > 1:
+        torch.set_num_threads(max(1, (os.cpu_count() or 1) // world))
+    cases = device_inputs(device)
     step = Step(cases, device)
     sampler = ClockSampler(local)
     sampler.start()
@@ -641,9 +672,10 @@ def main(argv=None):
     e2e = None
     if not args.no_e2e:
         del step
+        host_cases = to_host(cases)
         torch.cuda.empty_cache()
         e2e_steps = max(3, min(args.steps, 30))
-        ms_e2e, h2d, d2h = time_e2e(cases, device, e2e_steps, 3)
+        ms_e2e, h2d, d2h = time_e2e(host_cases, device, e2e_steps, 3)
         e2e = {"value": world * STEP_BYTES / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "ms_per_step": ms_e2e,
@@ -652,7 +684,7 @@ def main(argv=None):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(cases)
+        cpu = cpu_baseline(to_host(cases, rows=256))
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,

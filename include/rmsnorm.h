@@ -159,6 +159,20 @@ int rmsnorm_vjp_ws(const void *x, const void *w, const void *g, float eps,
                    int64_t D, int dtype, void *workspace, size_t workspace_bytes,
                    void *stream);
 
+/*
+ * Gated activation of the decode loop.  Source: "Fused residual-add RMSNorm
+ * and fused RoPE + KV-append decode kernels", Background, third bullet (a
+ * fused silu(x[:d]) * x[d:2d] gate with 16-byte vectorised loads).
+ *   x    [rows, 2*d] dtype: each row is [a | b], a and b of d values.
+ *   out  [rows, d] dtype: out_j = silu(a_j) * b_j, silu(a) = a / (1 + e^-a),
+ *        computed in fp32 and rounded once.
+ * out must not overlap x.  d % 8 == 0 with 16-byte aligned pointers takes the
+ * vectorised kernel; other shapes and alignments are accepted.  rows == 0 is a
+ * no-op.  Errors as for rmsnorm_fwd.
+ */
+int rmsnorm_gated_silu(const void *x, void *out, int64_t rows, int64_t d, int dtype,
+                       void *stream);
+
 /* Size of the fixed device array behind rmsnorm_vjp_noalloc: 16 MiB. */
 #define RMSNORM_VJP_NOALLOC_MAX_BYTES ((size_t)16 << 20)
 

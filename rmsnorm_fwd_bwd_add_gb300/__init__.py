@@ -10,6 +10,7 @@ include/rmsnorm.h (librmsnorm_gb300.so), with these thin Python bindings:
   rmsnorm_fused_vjp -- VJP of the two-output fused op (adds the gradient that
                   reaches new_residual in the same pass).
   fused_add_rmsnorm, rms_norm -- torch.autograd wrappers.
+  rmsnorm_gated_silu -- the decode loop's gated activation silu(x[:d]) * x[d:].
 
 PyTorch supplies device memory and streams only.
 """
@@ -19,6 +20,7 @@ from .api import (  # noqa: F401
     rmsnorm_device_status,
     rmsnorm_fused_vjp,
     rmsnorm_fwd,
+    rmsnorm_gated_silu,
     rmsnorm_status_string,
     rmsnorm_vjp,
     rmsnorm_vjp_workspace_size,
@@ -31,6 +33,7 @@ __all__ = [
     "rmsnorm_fwd",
     "rmsnorm_vjp",
     "rmsnorm_fused_vjp",
+    "rmsnorm_gated_silu",
     "fused_add_rmsnorm",
     "rms_norm",
     "rmsnorm_vjp_ws",

@@ -17,6 +17,7 @@ EXPORTS = (
     "rmsnorm_fwd",
     "rmsnorm_vjp",
     "rmsnorm_fused_vjp",
+    "rmsnorm_gated_silu",
     "rmsnorm_vjp_workspace_size",
     "rmsnorm_vjp_ws",
     "rmsnorm_vjp_noalloc",
@@ -67,6 +68,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.rmsnorm_vjp.restype = _i
     lib.rmsnorm_fused_vjp.argtypes = [_vp, _vp, _vp, _vp, _f, _f, _vp, _vp, _i64, _i64, _i, _vp]
     lib.rmsnorm_fused_vjp.restype = _i
+    lib.rmsnorm_gated_silu.argtypes = [_vp, _vp, _i64, _i64, _i, _vp]
+    lib.rmsnorm_gated_silu.restype = _i
     lib.rmsnorm_vjp_workspace_size.argtypes = [_i64, _i64, _i]
     lib.rmsnorm_vjp_workspace_size.restype = ctypes.c_size_t
     lib.rmsnorm_vjp_ws.argtypes = [_vp, _vp, _vp, _f, _f, _vp, _vp, _i64, _i64, _i, _vp,

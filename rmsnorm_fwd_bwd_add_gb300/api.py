@@ -171,6 +171,27 @@ def rmsnorm_fused_vjp(h: torch.Tensor, w: torch.Tensor, g_out: torch.Tensor, eps
     return g_h, gw
 
 
+def rmsnorm_gated_silu(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, stream=None):
+    """silu(x[..., :d]) * x[..., d:] for x of last dimension 2d; returns the
+    [..., d] result."""
+    if x.shape[-1] % 2:
+        raise ValueError("the last dimension of x must be even (2d)")
+    rows, two_d = _rows_d(x)
+    d = two_d // 2
+    code = _dtype_code(x)
+    if out is None:
+        out = torch.empty(*x.shape[:-1], d, dtype=x.dtype, device=x.device)
+    if (out.dtype != x.dtype or out.device != x.device or out.shape != (*x.shape[:-1], d)
+            or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous %s tensor of shape %s" % (
+            x.dtype, tuple((*x.shape[:-1], d))))
+    with _OnDevice(x.device):
+        st = _native.lib().rmsnorm_gated_silu(_ptr(x), _ptr(out), rows, d, code,
+                                              _stream(x.device, stream))
+    _native.check("rmsnorm_gated_silu", st)
+    return out
+
+
 def rmsnorm_vjp_workspace_size(rows: int, D: int, dtype: torch.dtype) -> int:
     """Bytes of scratch rmsnorm_vjp_ws needs on the current device."""
     return int(_native.lib().rmsnorm_vjp_workspace_size(rows, D, _DTYPES[dtype]))

@@ -546,7 +546,7 @@ const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype
 
 }  // extern "C"
 
-// ---- helpers for rmsnorm_vjp_noalloc (noalloc.cu) --------------------------
+// ---- helpers for the entry points of noalloc.cu and gated.cu -----------------
 namespace rmsn {
 
 // Bytes of gw scratch rmsnorm_vjp_ws needs for exactly these pointers on the
@@ -563,5 +563,13 @@ size_t vjp_partials_bytes_for(const void *x, const void *w, const void *g, const
 
 // Records a failed CUDA call for rmsnorm_last_cuda_error().
 int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+// SM count of the current device (cached with the device's other set-up).
+int current_sm_count(int *sm) {
+    DevInfo dev;
+    const int st = current_device(&dev);
+    if (st == RMSNORM_OK) *sm = dev.sm_count;
+    return st;
+}
 
 }  // namespace rmsn

@@ -110,6 +110,22 @@ def config4(D: int, rows: int = 16384) -> Case:
     return Case(4, "c4_r%d_d%d_bf16" % (rows, D), rows, D, dt, 1e-6, 0.0, x, w, res, g)
 
 
+def config4_on_device(D: int, device, rows: int = 16384) -> Case:
+    """Configuration 4 drawn directly on `device` with a seeded CUDA generator:
+    the same distributions as config4() (whose CPU draws the tests use), for
+    benchmarks that need the inputs only in device memory."""
+    gen = torch.Generator(device=device).manual_seed(1000 + 100 * 4 + (PREFILL_D.index(D) if D in PREFILL_D else D))
+    dt = torch.bfloat16
+
+    def normal(shape, mean=0.0, std=1.0):
+        return torch.randn(shape, generator=gen, device=device, dtype=torch.float32) * std + mean
+    x = normal((rows, D)).to(dt)
+    res = normal((rows, D)).to(dt)
+    w = normal((D,), 1.0, 0.02).to(dt)
+    g = normal((rows, D)).to(dt)
+    return Case(4, "c4_r%d_d%d_bf16" % (rows, D), rows, D, dt, 1e-6, 0.0, x, w, res, g)
+
+
 def outlier_rows(rows: int, gen: torch.Generator):
     """Indices of the rows scaled by 1e3 and by 1e-4: round(1% of rows) each,
     taken from one seeded permutation."""
