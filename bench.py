@@ -192,8 +192,8 @@ def measured_peak():
 
 # Files that define the staged kernels and their launch plans: a change to any
 # of them invalidates recorded DRAM traffic.
-STAGED_SOURCES = ("api.cu", "common.cuh", "plan.h", "launch_staged.cuh", "staged.cuh",
-                  "staged_bf16.cu", "staged_f16.cu")
+STAGED_SOURCES = ("common.cuh", "plan.h", "planner.h", "launch_util.h", "launch_staged.cuh",
+                  "staged.cuh", "staged_bf16.cu", "staged_f16.cu")
 
 
 def source_hash(files=STAGED_SOURCES):
@@ -324,6 +324,26 @@ def time_device(step: Step, steps: int, warmup: int, sampler: ClockSampler):
     return total_ms, per_op_us, sampler.summary(t0, t1)
 
 
+def bind_to_gpu_numa_node(device_index: int) -> None:
+    """Run this process on the CPUs next to the GPU (sysfs local_cpulist of
+    its PCI function) so that pinned host buffers are allocated in the GPU's
+    NUMA node; a no-op where the information is missing."""
+    try:
+        props = torch.cuda.get_device_properties(device_index)
+        bus = "%04x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        with open("/sys/bus/pci/devices/%s/local_cpulist" % bus) as f:
+            text = f.read().strip()
+        cpus = set()
+        for part in text.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        cpus &= os.sched_getaffinity(0)
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+    except Exception:
+        pass
+
+
 def time_e2e(cases, device, steps: int, warmup: int):
     """The step through the public Python API with pinned host buffers: every
     step copies its inputs (x, residual, g, w of both D) host->device and its
@@ -332,6 +352,7 @@ def time_e2e(cases, device, steps: int, warmup: int):
     compute and step k-2's download overlap, as a user streaming batches
     would arrange it; the timed region ends when the last download is done."""
     import rmsnorm_fwd_bwd_add_gb300 as rn
+    bind_to_gpu_numa_node(device.index if device.index is not None else 0)
     ins = ("x", "res", "g", "w")
     outs = ("out", "nr", "gx", "gw")
     host = {}

@@ -1,0 +1,191 @@
+// planner.h -- the dispatch table: which kernel, launch shape and ring depth
+// a problem gets.  A pure function of (mode, rows, D, alignment, SM count)
+// plus the RMSNORM_TUNE override, so the VJP's summation order, and with it
+// gw's bits, is fixed for a given device.
+//   * unaligned pointers or D*2 not a multiple of 16 -> generic tier;
+//   * rows <= DECODE_ROWS (decode: one token per sequence)  -> direct tier;
+//   * D <= 16384 -> staged tier (TMA bulk ring): sub-warp/warp per row for
+//     D <= 1024, CTA per row above;
+//   * longer rows -> direct tier (forward up to 32768, VJP up to 16384), then
+//     generic.
+#pragma once
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "common.cuh"
+#include "plan.h"
+
+namespace rmsn {
+namespace planner {
+
+constexpr int64_t DECODE_ROWS = 8;
+// Shared-memory budget of one CTA when two share an SM (228 KB per SM, 1 KB
+// reserved per CTA), and when one CTA has the SM to itself (227 KB opt-in).
+constexpr size_t SMEM_TWO_PER_SM = 110 * 1024;
+constexpr size_t SMEM_THREE_PER_SM = 72 * 1024;
+constexpr size_t SMEM_ONE_PER_SM = 225 * 1024;
+// Target bytes of one tensor's tile in the sub-warp/warp-per-row shape.
+constexpr size_t SMALL_TILE_BYTES = 16 * 1024;
+// Bytes of tiles in flight per SM the ring is sized for.  Measured on GB300
+// (rows 16384, D 4096 and 8192): more read-ahead than this starves the
+// kernel's own writes and lowers the bandwidth, less leaves HBM idle.  The
+// forward writes as much as it reads and wants ~64 KB; the VJP (two bytes
+// read per byte written) ~96 KB.
+constexpr size_t INFLIGHT_FWD = 64 * 1024;
+constexpr size_t INFLIGHT_VJP = 96 * 1024;
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+
+// Overrides of the staged tier's choices, read once from RMSNORM_TUNE
+// ("cfg=N,cps=N,stages=N", any subset) for tuning sweeps.  Unset, the plan
+// is a pure function of the problem and the device.
+struct Tuning {
+    int cfg = -1;    // staged configuration index
+    int cps = 0;     // CTAs per SM (capped by what the registers allow)
+    int stages = 0;  // maximum ring depth
+};
+
+inline Tuning parse_tuning() {
+    Tuning t;
+    const char *env = std::getenv("RMSNORM_TUNE");
+    if (!env) return t;
+    char buf[128];
+    std::snprintf(buf, sizeof(buf), "%s", env);
+    for (char *tok = std::strtok(buf, ","); tok; tok = std::strtok(nullptr, ",")) {
+        int v = 0;
+        if (std::sscanf(tok, "cfg=%d", &v) == 1 && v >= 0 && v < N_STAGED_CFG) t.cfg = v;
+        else if (std::sscanf(tok, "cps=%d", &v) == 1 && v >= 1 && v <= 3) t.cps = v;
+        else if (std::sscanf(tok, "stages=%d", &v) == 1 && v >= 2 && v <= MAX_STAGES) t.stages = v;
+    }
+    return t;
+}
+
+inline const Tuning &tuning() {
+    static const Tuning t = parse_tuning();
+    return t;
+}
+
+// Ring depth for a stage of `per_stage` bytes with `cps` CTAs per SM: one
+// stage being consumed plus enough in flight to reach the mode's target
+// (at least one).  An explicit RMSNORM_TUNE stages= wins.
+inline int ring_stages(int mode, size_t per_stage, int cps) {
+    if (tuning().stages) return tuning().stages;
+    const size_t target = is_vjp(mode) ? INFLIGHT_VJP : INFLIGHT_FWD;
+    const size_t per_sm_stage = per_stage * (size_t)cps;
+    const int ahead = (int)std::max<size_t>(1, (target + per_sm_stage / 2) / per_sm_stage);
+    return std::min(MAX_STAGES, 1 + ahead);
+}
+
+inline bool plan_staged(int mode, int64_t rows, int D, int sm_count, int ci, Plan *p) {
+    const StagedCfg &c = STAGED_CFGS[ci];
+    const Tuning &tu = tuning();
+    const int ntens = input_tensors(mode);
+    const size_t row_bytes = (size_t)D * 2;
+    const int max_stages = tu.stages ? tu.stages : MAX_STAGES;
+    const int cps_max = staged_max_ctas_per_sm(mode, c.nt, c.g, c.v);
+    int cps = tu.cps ? std::min(tu.cps, cps_max) : staged_ctas_per_sm(mode, c.nt, c.g, c.v);
+    p->tier = TIER_STAGED;
+    p->cfg = ci;
+    p->nt = c.nt;
+    p->g = c.g;
+    p->v = c.v;
+    if (c.g < c.nt) {
+        // Several rows per tile; shuffle-only reductions.
+        const int ng = c.nt / c.g;
+        const int64_t rpg_max =
+            std::max<int64_t>(1, (int64_t)(SMALL_TILE_BYTES / (ng * row_bytes)));
+        const int64_t want_tiles = (int64_t)sm_count * cps * 2;
+        const int64_t rpg =
+            std::min(rpg_max, std::max<int64_t>(1, ceil_div(rows, ng * want_tiles)));
+        p->tile_rows = (int)(ng * rpg);
+        p->stage_bytes = (uint32_t)(p->tile_rows * row_bytes);
+        const size_t per_stage = (size_t)ntens * p->stage_bytes;
+        cps = std::min(cps, 2);
+        const size_t cap = cps == 2 ? SMEM_TWO_PER_SM : SMEM_ONE_PER_SM;
+        p->stages = (int)std::min<size_t>(std::min<size_t>(max_stages, cap / per_stage),
+                                          ring_stages(mode, per_stage, cps));
+        if (p->stages < 2) return false;
+        p->smem = STAGED_HEADER_BYTES + (size_t)p->stages * per_stage;
+        if (is_vjp(mode))  // the cross-group gw sum reuses the ring
+            p->smem = std::max(p->smem, (size_t)STAGED_HEADER_BYTES + (size_t)ng * D * 4);
+    } else {
+        // One row per tile, the whole CTA on it.  Two CTAs per SM when the
+        // registers allow it and each can hold three stages, else one CTA
+        // with at least two; the depth then follows the in-flight target.
+        p->tile_rows = 1;
+        p->stage_bytes = (uint32_t)row_bytes;
+        const size_t per_stage = (size_t)ntens * row_bytes;
+        const int64_t s3 = (int64_t)(SMEM_THREE_PER_SM / per_stage);
+        const int64_t s2 = (int64_t)(SMEM_TWO_PER_SM / per_stage);
+        const int64_t s1 = (int64_t)(SMEM_ONE_PER_SM / per_stage);
+        if (cps == 3 && s3 >= 2) {
+            p->stages = (int)std::min<int64_t>(std::min<int64_t>(max_stages, s3),
+                                               ring_stages(mode, per_stage, 3));
+        } else if (cps >= 2 && s2 >= 3) {
+            cps = 2;
+            p->stages = (int)std::min<int64_t>(std::min<int64_t>(max_stages, s2),
+                                               ring_stages(mode, per_stage, 2));
+        } else if (s1 >= 2) {
+            cps = 1;
+            p->stages = (int)std::min<int64_t>(std::min<int64_t>(max_stages, s1),
+                                               ring_stages(mode, per_stage, 1));
+        } else {
+            return false;
+        }
+        p->smem = STAGED_HEADER_BYTES + (size_t)p->stages * per_stage;
+    }
+    p->num_tiles = ceil_div(rows, p->tile_rows);
+    p->grid = (int)std::min<int64_t>(p->num_tiles, (int64_t)sm_count * cps);
+    return true;
+}
+
+inline Plan make_plan(int mode, int64_t rows, int D, bool aligned, int sm_count) {
+    Plan p{};
+    const int nv = D / 8;
+    if (aligned && rows > DECODE_ROWS) {
+        const int forced = tuning().cfg;
+        if (forced >= 0 && nv <= STAGED_CFGS[forced].max_nv &&
+            !(is_vjp(mode) && forced == STAGED_CFG_WIDE) &&
+            plan_staged(mode, rows, D, sm_count, forced, &p))
+            return p;
+        for (int ci = 0; ci < STAGED_CFG_WIDE; ++ci) {
+            if (nv <= STAGED_CFGS[ci].max_nv) {
+                if (plan_staged(mode, rows, D, sm_count, ci, &p)) return p;
+                break;
+            }
+        }
+    }
+    if (aligned) {
+        for (int ci = 0; ci < N_DIRECT_CFG; ++ci) {
+            const DirectCfg &c = DIRECT_CFGS[ci];
+            if (nv <= c.max_nv && !(is_vjp(mode) && c.v > 2)) {
+                p = Plan{};
+                p.tier = TIER_DIRECT;
+                p.cfg = ci;
+                p.nt = c.nt;
+                p.g = c.nt;
+                p.v = c.v;
+                p.tile_rows = 1;
+                p.num_tiles = rows;
+                const int64_t resident = std::max(1, 2048 / c.nt);
+                p.grid = (int)std::min<int64_t>(rows, (int64_t)sm_count * resident);
+                return p;
+            }
+        }
+    }
+    p = Plan{};
+    p.tier = TIER_GENERIC;
+    p.nt = GENERIC_NT;
+    p.g = GENERIC_NT;
+    p.tile_rows = 1;
+    p.num_tiles = rows;
+    p.grid = (int)std::min<int64_t>(rows, (int64_t)sm_count * 8);
+    return p;
+}
+
+}  // namespace planner
+}  // namespace rmsn
