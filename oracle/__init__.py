@@ -19,7 +19,8 @@ Sources (web pages, by title and section):
   * "RMSNormVJP backward writes a full {n_rows, D} gw_temp intermediate",
     POC section (eager fp32 reference and the gradient check) -- the VJP.
   * "Fused residual-add RMSNorm and fused RoPE + KV-append decode kernels",
-    Background, third bullet -- the gated activation silu(x[:d]) * x[d:2d].
+    Background, third bullet -- the gated activation silu(x[:d]) * x[d:2d];
+    second bullet and Task item 3 -- rope on q and k with the KV-cache append.
 """
 from __future__ import annotations
 
@@ -72,6 +73,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.rmsnorm_oracle_fused_vjp.restype = None
     lib.rmsnorm_oracle_gated_silu.argtypes = [_dp, _dp, ctypes.c_int64, ctypes.c_int64]
     lib.rmsnorm_oracle_gated_silu.restype = None
+    _ip = ctypes.POINTER(ctypes.c_int64)
+    lib.rmsnorm_oracle_rope_kv_append.argtypes = [_dp, _dp, _dp, _ip, _ip, _dp, _dp, _dp, _dp,
+                                                  ctypes.c_double, ctypes.c_int, ctypes.c_int64,
+                                                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+    lib.rmsnorm_oracle_rope_kv_append.restype = None
     return lib
 
 
@@ -157,6 +163,31 @@ class Oracle:
         return out
 
 
+    def rope_kv_append(self, q, k, v, positions, slots, k_cache, v_cache, base=10000.0,
+                       interleaved=False, cos_sin=None):
+        """Returns (q_out, k_cache', v_cache'); the given caches are copied,
+        not modified.  q: (T, Hq, Dh); k, v: (T, Hkv, Dh); caches
+        (num_slots, Hkv, Dh); cos_sin: optional (max_pos, Dh) table."""
+        q = self._arr(q)
+        T, Hq, Dh = q.shape
+        k = self._arr(k)
+        Hkv = k.shape[1]
+        v = self._arr(v, k.shape)
+        kc = np.array(k_cache, dtype=np.float64, copy=True, order="C")
+        vc = np.array(v_cache, dtype=np.float64, copy=True, order="C")
+        pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+        sl = np.ascontiguousarray(np.asarray(slots, dtype=np.int64))
+        assert pos.shape == (T,) and sl.shape == (T,)
+        cs = None if cos_sin is None else self._arr(cos_sin)
+        q_out = np.empty_like(q)
+        ip = ctypes.POINTER(ctypes.c_int64)
+        self._lib.rmsnorm_oracle_rope_kv_append(
+            self._ptr(q), self._ptr(k), self._ptr(v), pos.ctypes.data_as(ip), sl.ctypes.data_as(ip),
+            self._ptr(q_out), self._ptr(kc), self._ptr(vc), self._ptr(cs), self.scalar(base),
+            1 if interleaved else 0, T, Hq, Hkv, Dh)
+        return q_out, kc, vc
+
+
 _ORACLE = None
 
 
@@ -182,3 +213,9 @@ def fused_vjp(h, w, g_out, eps, weight_bias=0.0, g_residual=None):
 
 def gated_silu(x):
     return load().gated_silu(x)
+
+
+def rope_kv_append(q, k, v, positions, slots, k_cache, v_cache, base=10000.0, interleaved=False,
+                   cos_sin=None):
+    return load().rope_kv_append(q, k, v, positions, slots, k_cache, v_cache, base, interleaved,
+                                 cos_sin)

@@ -143,3 +143,74 @@ void rmsnorm_oracle_gated_silu(const double *x, double *out, int64_t rows, int64
         }
     }
 }
+
+/*
+ * Rotary embedding of q and k plus the KV-cache append of the decode loop
+ * ("Fused residual-add RMSNorm and fused RoPE + KV-append decode kernels",
+ * Background, second bullet, and Task item 3: rope applied to q and k, k and v
+ * written into the cache slab or a paged pool block, cos/sin from a
+ * precomputed cache or computed on the fly).
+ *
+ * For token t at absolute position p = positions[t] and pair index
+ * i in [0, Dh/2), the angle is  theta_i = p * base^(-2i/Dh)  (or, when
+ * cos_sin is given, cos/sin are read from row p of that table: Dh/2 cosines
+ * then Dh/2 sines).  A pair (x_a, x_b) rotates to
+ *     (x_a cos - x_b sin,  x_b cos + x_a sin),
+ * with (a, b) = (i, i + Dh/2) (rotate-half layout) or (2i, 2i + 1)
+ * (interleaved, when interleaved != 0).
+ *   q_out[t, h, :]            = rope(q[t, h, :])          for h < Hq
+ *   k_cache[slots[t], h, :]   = rope(k[t, h, :])          for h < Hkv
+ *   v_cache[slots[t], h, :]   = v[t, h, :]
+ * A negative slot writes nothing to the caches.  Shapes: q, q_out
+ * [T, Hq, Dh]; k, v [T, Hkv, Dh]; caches [num_slots, Hkv, Dh]; positions and
+ * slots [T].  Rows of the caches that no token writes are left as they are.
+ */
+static void rope_pair_cs(const double *cos_sin, double base, int64_t p, int64_t i, int64_t Dh,
+                         double *c, double *s)
+{
+    if (cos_sin) {
+        *c = cos_sin[p * Dh + i];
+        *s = cos_sin[p * Dh + Dh / 2 + i];
+    } else {
+        double theta = (double)p * pow(base, -2.0 * (double)i / (double)Dh);
+        *c = cos(theta);
+        *s = sin(theta);
+    }
+}
+
+static void rope_vector(const double *x, double *y, const double *cos_sin, double base,
+                        int64_t p, int64_t Dh, int interleaved)
+{
+    for (int64_t i = 0; i < Dh / 2; ++i) {
+        int64_t ia = interleaved ? 2 * i : i;
+        int64_t ib = interleaved ? 2 * i + 1 : i + Dh / 2;
+        double c, s;
+        rope_pair_cs(cos_sin, base, p, i, Dh, &c, &s);
+        double xa = x[ia], xb = x[ib];
+        y[ia] = xa * c - xb * s;
+        y[ib] = xb * c + xa * s;
+    }
+}
+
+void rmsnorm_oracle_rope_kv_append(const double *q, const double *k, const double *v,
+                                   const int64_t *positions, const int64_t *slots,
+                                   double *q_out, double *k_cache, double *v_cache,
+                                   const double *cos_sin, double base, int interleaved,
+                                   int64_t T, int64_t Hq, int64_t Hkv, int64_t Dh)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t p = positions[t];
+        for (int64_t h = 0; h < Hq; ++h)
+            rope_vector(q + (t * Hq + h) * Dh, q_out + (t * Hq + h) * Dh, cos_sin, base, p, Dh,
+                        interleaved);
+        int64_t slot = slots[t];
+        if (slot < 0)
+            continue;
+        for (int64_t h = 0; h < Hkv; ++h) {
+            rope_vector(k + (t * Hkv + h) * Dh, k_cache + (slot * Hkv + h) * Dh, cos_sin, base,
+                        p, Dh, interleaved);
+            for (int64_t j = 0; j < Dh; ++j)
+                v_cache[(slot * Hkv + h) * Dh + j] = v[(t * Hkv + h) * Dh + j];
+        }
+    }
+}

@@ -344,6 +344,98 @@ def pin_gated_silu(orc):
     _close(orc.gated_silu(xs)[1], orc.gated_silu(xs[1:2])[0], 0, 0, "row 1 alone")
 
 
+def _rope(orc, x, positions, base=10000.0, interleaved=False, cos_sin=None):
+    """rope of x (T, H, Dh) at the given positions through the oracle (q path)."""
+    T, H, Dh = x.shape
+    kc = np.zeros((1, 1, Dh))
+    q_out, _, _ = orc.rope_kv_append(x, np.zeros((T, 1, Dh)), np.zeros((T, 1, Dh)), positions,
+                                     -np.ones(T, np.int64), kc, kc, base, interleaved, cos_sin)
+    return q_out
+
+
+def pin_rope(orc):
+    """Rotary embedding: position 0 is the identity; norms are kept; the
+    score <rope(q, m), rope(k, n)> depends only on n - m; rope(rope(x, a), b)
+    = rope(x, a + b); closed forms where theta is simple (Dh = 2: theta = p;
+    Dh = 4, base 100: theta_1 = p / 10, with cos/sin from the math library);
+    the interleaved layout is the rotate-half layout under the even/odd
+    permutation; a table of the same cos/sin gives the same result."""
+    import math
+    rng = _rng(22)
+    for inter in (False, True):
+        x = rng.normal(size=(3, 2, 8))
+        _close(_rope(orc, x, [0, 0, 0], interleaved=inter), x, 0, 0, "rope at 0")
+        y = _rope(orc, x, [3, 1000, 123456], interleaved=inter)
+        _close(np.linalg.norm(y, axis=2), np.linalg.norm(x, axis=2), 1e-13, 0, "norm kept")
+        q = rng.normal(size=(1, 1, 16))
+        k = rng.normal(size=(1, 1, 16))
+        s1 = np.sum(_rope(orc, q, [7], interleaved=inter) * _rope(orc, k, [19], interleaved=inter))
+        s2 = np.sum(_rope(orc, q, [1007], interleaved=inter) * _rope(orc, k, [1019], interleaved=inter))
+        _close(s1, s2, 1e-11, 1e-12, "relative position")
+        a = _rope(orc, _rope(orc, x, [5, 40, 7], interleaved=inter), [11, 2, 300], interleaved=inter)
+        _close(a, _rope(orc, x, [16, 42, 307], interleaved=inter), 1e-12, 1e-13, "composition")
+    # closed forms
+    y = _rope(orc, np.array([[[1.0, 0.0]]]), [1])
+    _close(y[0, 0], [math.cos(1.0), math.sin(1.0)], 1e-15, 1e-16, "Dh=2, p=1")
+    y = _rope(orc, np.array([[[0.0, 2.0, 0.0, 0.0]]]), [5], base=100.0)
+    # pair (1, 3): (x1, x3) = (2, 0) turns by theta_1 = 5 * 100^(-1/2) = 0.5
+    _close(y[0, 0], [0.0, 2 * math.cos(0.5), 0.0, 2 * math.sin(0.5)], 1e-15, 1e-16, "Dh=4, base 100")
+    # interleaved = rotate-half under the even/odd permutation
+    x = rng.normal(size=(2, 3, 12))
+    perm = np.concatenate([np.arange(0, 12, 2), np.arange(1, 12, 2)])
+    half = _rope(orc, x[:, :, perm], [9, 77])
+    inter = _rope(orc, x, [9, 77], interleaved=True)
+    _close(inter[:, :, perm], half, 1e-14, 1e-15, "layouts")
+    # table path
+    Dh, base = 8, 500.0
+    tab = np.zeros((64, Dh))
+    for p in range(64):
+        for i in range(Dh // 2):
+            ang = p * math.pow(base, -2.0 * i / Dh)
+            tab[p, i], tab[p, Dh // 2 + i] = math.cos(ang), math.sin(ang)
+    x = rng.normal(size=(3, 2, Dh))
+    _close(_rope(orc, x, [0, 17, 63], base=base, cos_sin=tab),
+           _rope(orc, x, [0, 17, 63], base=base), 1e-13, 1e-14, "table = on the fly")
+
+
+def pin_kv_append(orc):
+    """The cache append: token t's rotated k and its v land in row slots[t];
+    a negative slot writes nothing; rows no token names keep their contents;
+    q's rotation does not depend on the slots; a ring cache (slot = position
+    mod window) holds the same rows as the dense slab's last window."""
+    rng = _rng(23)
+    T, Hq, Hkv, Dh, S = 5, 4, 2, 8, 9
+    q = rng.normal(size=(T, Hq, Dh))
+    k = rng.normal(size=(T, Hkv, Dh))
+    v = rng.normal(size=(T, Hkv, Dh))
+    pos = np.array([3, 4, 5, 6, 7])
+    slots = np.array([8, -1, 0, 2, 5])
+    kc0 = rng.normal(size=(S, Hkv, Dh))
+    vc0 = rng.normal(size=(S, Hkv, Dh))
+    qo, kc, vc = orc.rope_kv_append(q, k, v, pos, slots, kc0, vc0)
+    untouched = [r for r in range(S) if r not in slots]
+    _close(kc[untouched], kc0[untouched], 0, 0, "untouched k rows")
+    _close(vc[untouched], vc0[untouched], 0, 0, "untouched v rows")
+    for t in range(T):
+        if slots[t] >= 0:
+            _close(vc[slots[t]], v[t], 0, 0, "v copied")
+            # the cached k is k rotated like a q row at the same position
+            _close(kc[slots[t]], _rope(orc, k[t:t + 1], [pos[t]])[0], 0, 0, "k rotated")
+    qo2, _, _ = orc.rope_kv_append(q, k, v, pos, -np.ones(T, np.int64), kc0, vc0)
+    _close(qo, qo2, 0, 0, "q independent of slots")
+    # ring of window 4 vs dense slab
+    T = 10
+    k = rng.normal(size=(T, 1, Dh))
+    v = rng.normal(size=(T, 1, Dh))
+    pos = np.arange(100, 100 + T)
+    z = np.zeros((T, 1, Dh))
+    _, kd, vd = orc.rope_kv_append(z, k, v, pos, np.arange(T), np.zeros((T, 1, Dh)), np.zeros((T, 1, Dh)))
+    _, kr, vr = orc.rope_kv_append(z, k, v, pos, pos % 4, np.zeros((4, 1, Dh)), np.zeros((4, 1, Dh)))
+    for t in range(T - 4, T):
+        _close(kr[pos[t] % 4], kd[t], 0, 0, "ring k")
+        _close(vr[pos[t] % 4], vd[t], 0, 0, "ring v")
+
+
 ALL_PINS = [
     pin_worked_examples,
     pin_constant_rows,
@@ -359,4 +451,6 @@ ALL_PINS = [
     pin_scaled_weight,
     pin_fused_vjp_finite_differences,
     pin_gated_silu,
+    pin_rope,
+    pin_kv_append,
 ]

@@ -49,6 +49,16 @@ MUTANTS = [
     ("silu_no_gate", "out[i * d + j] = silu * b[j];", "out[i * d + j] = silu;", 0),
     ("silu_row_stride", "const double *a = x + i * 2 * d;", "const double *a = x + i * d;", 0),
     ("silu_second_half_offset", "const double *b = a + d;", "const double *b = a + d - 1;", 0),
+    ("rope_sin_sign", "y[ia] = xa * c - xb * s;", "y[ia] = xa * c + xb * s;", 0),
+    ("rope_second_sign", "y[ib] = xb * c + xa * s;", "y[ib] = xb * c - xa * s;", 0),
+    ("rope_exponent", "pow(base, -2.0 * (double)i / (double)Dh)", "pow(base, -1.0 * (double)i / (double)Dh)", 0),
+    ("rope_half_offset", "int64_t ib = interleaved ? 2 * i + 1 : i + Dh / 2;",
+     "int64_t ib = interleaved ? 2 * i + 1 : Dh - 1 - i;", 0),
+    ("rope_table_swapped", "*c = cos_sin[p * Dh + i];", "*c = cos_sin[p * Dh + Dh / 2 + i];", 0),
+    ("rope_token_for_position", "int64_t p = positions[t];", "int64_t p = t;", 0),
+    ("kv_v_rotated", "v_cache[(slot * Hkv + h) * Dh + j] = v[(t * Hkv + h) * Dh + j];",
+     "v_cache[(slot * Hkv + h) * Dh + j] = k_cache[(slot * Hkv + h) * Dh + j];", 0),
+    ("kv_slot_is_token", "int64_t slot = slots[t];", "int64_t slot = slots[t] < 0 ? -1 : t % 4;", 0),
 ]
 
 
