@@ -85,6 +85,8 @@ typedef enum {
 
 /* Bits of the device status word. */
 #define RMSNORM_DEVSTATUS_WAIT_TIMEOUT 1u
+#define RMSNORM_DEVSTATUS_BAD_INDEX 2u /* rmsnorm_rope_kv_append: a position or
+                                          slot out of range (that token skipped) */
 
 /*
  * Fused residual-add RMSNorm forward.
@@ -173,6 +175,40 @@ int rmsnorm_vjp_ws(const void *x, const void *w, const void *g, float eps,
 int rmsnorm_gated_silu(const void *x, void *out, int64_t rows, int64_t d, int dtype,
                        void *stream);
 
+/*
+ * Rotary embedding of q and k fused with the KV-cache append.  Source: "Fused
+ * residual-add RMSNorm and fused RoPE + KV-append decode kernels", Background,
+ * second bullet, and Task item 3 (rope on q and k, k and v written into the
+ * cache slab or a paged pool block in the same kernel; cos/sin from a
+ * precomputed cache or computed on the fly).
+ *   q        [T, Hq, Dh] dtype;  q_out [T, Hq, Dh] dtype (may be q: in place).
+ *   k, v     [T, Hkv, Dh] dtype.
+ *   positions, slots  [T] int64, device memory: token t's absolute position
+ *            and the cache row it goes to (negative: not written).  A dense
+ *            slab uses slot = position (a ring / sliding window: position mod
+ *            window); a paged pool [blocks, block_size, Hkv, Dh] uses
+ *            slot = block * block_size + offset.
+ *   k_cache, v_cache  [num_slots, Hkv, Dh] dtype: row slots[t] receives the
+ *            rotated k and the v of token t; other rows are untouched.
+ *   cos_sin  [max_pos, Dh] fp32 device table (Dh/2 cosines then Dh/2 sines of
+ *            each position), or NULL: theta_i = position * rope_base^(-2i/Dh)
+ *            computed on the fly (about 1e-8 rad of error up to 1e6).
+ *   interleaved  0: pairs (i, i + Dh/2) (rotate-half); 1: pairs (2i, 2i + 1).
+ * Arithmetic in fp32, each output rounded once.  Dh even, at most 1024;
+ * Dh % 16 == 0 with 16-byte aligned pointers takes the vectorised kernel.
+ * Positions outside [0, max_pos) (or negative) and slots >= num_slots are
+ * detected on the device: the token's outputs are skipped (nothing out of
+ * range is touched) and RMSNORM_DEVSTATUS_BAD_INDEX is set.  The caches must
+ * not overlap each other, the inputs or q_out.  T == 0 is a no-op.
+ * (rmsnorm_ is this library's symbol prefix.)
+ */
+int rmsnorm_rope_kv_append(const void *q, const void *k, const void *v,
+                           const int64_t *positions, const int64_t *slots, void *q_out,
+                           void *k_cache, void *v_cache, const float *cos_sin,
+                           int64_t max_pos, float rope_base, int interleaved, int64_t T,
+                           int64_t Hq, int64_t Hkv, int64_t Dh, int64_t num_slots, int dtype,
+                           void *stream);
+
 /* Size of the fixed device array behind rmsnorm_vjp_noalloc: 16 MiB. */
 #define RMSNORM_VJP_NOALLOC_MAX_BYTES ((size_t)16 << 20)
 
@@ -214,7 +250,8 @@ int rmsnorm_last_cuda_error(void);
  * Reads the device status word of the current device into *bits (a mask of
  * RMSNORM_DEVSTATUS_* flags set by kernels since the last clear) and clears it
  * when `clear` is non-zero.  Synchronises the device: diagnostics only.
- * Returns RMSNORM_ERR_TIMEOUT when the timeout bit is set.
+ * Returns RMSNORM_ERR_TIMEOUT when the timeout bit is set, else
+ * RMSNORM_ERR_INVALID_ARG when the bad-index bit is set.
  */
 int rmsnorm_device_status(unsigned int *bits, int clear);
 

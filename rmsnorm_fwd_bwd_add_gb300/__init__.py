@@ -11,6 +11,7 @@ include/rmsnorm.h (librmsnorm_gb300.so), with these thin Python bindings:
                   reaches new_residual in the same pass).
   fused_add_rmsnorm, rms_norm -- torch.autograd wrappers.
   rmsnorm_gated_silu -- the decode loop's gated activation silu(x[:d]) * x[d:].
+  rmsnorm_rope_kv_append -- rotary embedding of q and k with the KV-cache append.
 
 PyTorch supplies device memory and streams only.
 """
@@ -21,12 +22,13 @@ from .api import (  # noqa: F401
     rmsnorm_fused_vjp,
     rmsnorm_fwd,
     rmsnorm_gated_silu,
+    rmsnorm_rope_kv_append,
     rmsnorm_status_string,
     rmsnorm_vjp,
     rmsnorm_vjp_workspace_size,
     rmsnorm_vjp_ws,
 )
-from ._native import DEVSTATUS_WAIT_TIMEOUT, MAX_D, RmsnormError  # noqa: F401
+from ._native import DEVSTATUS_BAD_INDEX, DEVSTATUS_WAIT_TIMEOUT, MAX_D, RmsnormError  # noqa: F401
 from .autograd import fused_add_rmsnorm, rms_norm  # noqa: F401
 
 __all__ = [
@@ -34,6 +36,7 @@ __all__ = [
     "rmsnorm_vjp",
     "rmsnorm_fused_vjp",
     "rmsnorm_gated_silu",
+    "rmsnorm_rope_kv_append",
     "fused_add_rmsnorm",
     "rms_norm",
     "rmsnorm_vjp_ws",

@@ -18,6 +18,7 @@ EXPORTS = (
     "rmsnorm_vjp",
     "rmsnorm_fused_vjp",
     "rmsnorm_gated_silu",
+    "rmsnorm_rope_kv_append",
     "rmsnorm_vjp_workspace_size",
     "rmsnorm_vjp_ws",
     "rmsnorm_vjp_noalloc",
@@ -37,6 +38,7 @@ STATUS = {
     5: "RMSNORM_ERR_TIMEOUT",
 }
 DEVSTATUS_WAIT_TIMEOUT = 1
+DEVSTATUS_BAD_INDEX = 2
 MAX_D = 1 << 24
 VJP_NOALLOC_MAX_BYTES = 16 << 20
 
@@ -70,6 +72,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.rmsnorm_fused_vjp.restype = _i
     lib.rmsnorm_gated_silu.argtypes = [_vp, _vp, _i64, _i64, _i, _vp]
     lib.rmsnorm_gated_silu.restype = _i
+    lib.rmsnorm_rope_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _f,
+                                           _i, _i64, _i64, _i64, _i64, _i64, _i, _vp]
+    lib.rmsnorm_rope_kv_append.restype = _i
     lib.rmsnorm_vjp_workspace_size.argtypes = [_i64, _i64, _i]
     lib.rmsnorm_vjp_workspace_size.restype = ctypes.c_size_t
     lib.rmsnorm_vjp_ws.argtypes = [_vp, _vp, _vp, _f, _f, _vp, _vp, _i64, _i64, _i, _vp,

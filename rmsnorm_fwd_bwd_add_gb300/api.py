@@ -192,6 +192,50 @@ def rmsnorm_gated_silu(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, s
     return out
 
 
+def rmsnorm_rope_kv_append(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                           positions: torch.Tensor, slots: torch.Tensor, k_cache: torch.Tensor,
+                           v_cache: torch.Tensor, *, rope_base: float = 10000.0,
+                           cos_sin: Optional[torch.Tensor] = None, interleaved: bool = False,
+                           q_out: Optional[torch.Tensor] = None, stream=None):
+    """Rotates q (into q_out; pass q_out=q for in place) and k, and writes k and
+    v into rows `slots` of the caches.  q: [T, Hq, Dh]; k, v: [T, Hkv, Dh];
+    positions, slots: [T] int64 CUDA tensors; caches [num_slots, Hkv, Dh];
+    cos_sin: optional [max_pos, Dh] float32 table.  Returns q_out."""
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape:
+        raise ValueError("q must be [T, Hq, Dh] and k, v [T, Hkv, Dh]")
+    T, Hq, Dh = q.shape
+    Hkv = k.shape[1]
+    if k.shape[0] != T or k.shape[2] != Dh:
+        raise ValueError("k and v must be [T, Hkv, Dh] with q's T and Dh")
+    code = _dtype_code(q)
+    for name, t in (("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache)):
+        if t.dtype != q.dtype or t.device != q.device or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous %s tensor on %s" % (name, q.dtype, q.device))
+    if not q.is_cuda or not q.is_contiguous():
+        raise ValueError("q must be a contiguous CUDA tensor")
+    if k_cache.dim() != 3 or k_cache.shape[1:] != (Hkv, Dh) or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [num_slots, Hkv, Dh]")
+    for name, t in (("positions", positions), ("slots", slots)):
+        if t.dtype != torch.int64 or t.shape != (T,) or t.device != q.device or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous [T] int64 tensor on %s" % (name, q.device))
+    max_pos = 0
+    if cos_sin is not None:
+        if (cos_sin.dtype != torch.float32 or cos_sin.dim() != 2 or cos_sin.shape[1] != Dh
+                or cos_sin.device != q.device or not cos_sin.is_contiguous()):
+            raise ValueError("cos_sin must be a contiguous [max_pos, Dh] float32 tensor")
+        max_pos = cos_sin.shape[0]
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    _check_like("q_out", q_out, q)
+    with _OnDevice(q.device):
+        st = _native.lib().rmsnorm_rope_kv_append(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(slots), _ptr(q_out), _ptr(k_cache),
+            _ptr(v_cache), _ptr(cos_sin), max_pos, rope_base, 1 if interleaved else 0, T, Hq, Hkv,
+            Dh, k_cache.shape[0], code, _stream(q.device, stream))
+    _native.check("rmsnorm_rope_kv_append", st)
+    return q_out
+
+
 def rmsnorm_vjp_workspace_size(rows: int, D: int, dtype: torch.dtype) -> int:
     """Bytes of scratch rmsnorm_vjp_ws needs on the current device."""
     return int(_native.lib().rmsnorm_vjp_workspace_size(rows, D, _DTYPES[dtype]))
@@ -223,10 +267,12 @@ def rmsnorm_vjp_ws(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float
 
 
 def rmsnorm_device_status(clear: bool = True) -> int:
-    """Device status bits of the current device (synchronises)."""
+    """Device status bits of the current device (synchronises).  The bits are
+    returned, not raised: the status the C call derives from them (timeout,
+    bad index) is not an error of the call itself."""
     bits = ctypes.c_uint(0)
     st = _native.lib().rmsnorm_device_status(ctypes.byref(bits), 1 if clear else 0)
-    if st not in (0, 5):
+    if st != 0 and not (bits.value and st in (1, 5)):
         _native.check("rmsnorm_device_status", st)
     return int(bits.value)
 

@@ -348,7 +348,9 @@ int rmsnorm_device_status(unsigned int *bits, int clear) {
         e = cudaDeviceSynchronize();
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    return (*bits & RMSNORM_DEVSTATUS_WAIT_TIMEOUT) ? RMSNORM_ERR_TIMEOUT : RMSNORM_OK;
+    if (*bits & RMSNORM_DEVSTATUS_WAIT_TIMEOUT) return RMSNORM_ERR_TIMEOUT;
+    if (*bits & RMSNORM_DEVSTATUS_BAD_INDEX) return RMSNORM_ERR_INVALID_ARG;
+    return RMSNORM_OK;
 }
 
 int rmsnorm_debug_inject(int64_t drop_tile, int64_t budget_cycles) {
@@ -375,7 +377,7 @@ const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype
 
 }  // extern "C"
 
-// ---- helpers for the entry points of noalloc.cu and gated.cu -----------------
+// ---- helpers for the entry points of noalloc.cu, gated.cu and rope.cu --------
 namespace rmsn {
 
 // Bytes of gw scratch rmsnorm_vjp_ws needs for exactly these pointers on the
@@ -392,6 +394,14 @@ size_t vjp_partials_bytes_for(const void *x, const void *w, const void *g, const
 
 // Records a failed CUDA call for rmsnorm_last_cuda_error().
 int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+// Device address of the current device's status word.
+int current_status_word(unsigned int **status) {
+    DevInfo dev;
+    const int st = current_device(&dev);
+    if (st == RMSNORM_OK) *status = dev.status;
+    return st;
+}
 
 // SM count of the current device (cached with the device's other set-up).
 int current_sm_count(int *sm) {
