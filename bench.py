@@ -56,6 +56,11 @@ def gate_bytes(rows, d, s=ITEM):
     return 3 * rows * d * s
 
 
+def rope_bytes(T, Hq, Hkv, Dh, s=ITEM):
+    """Rope + append: q read and written, k and v read and written once."""
+    return (2 * Hq + 4 * Hkv) * T * Dh * s + 16 * T
+
+
 def fused_vjp_bytes(rows, D, s=ITEM):
     """The two-output op's VJP: h, g_out and g_residual read, g_h written."""
     return 4 * rows * D * s + D * s + 4 * D
@@ -500,12 +505,45 @@ def run_reference(args):
     return 0
 
 
+def run_rope(args, rn, dev):
+    """rope + KV append with Llama-3-8B heads (32 q, 8 kv, head 128): --rows
+    tokens at positions 50000.., slots = positions mod 2 * rows."""
+    T, Hq, Hkv, Dh = args.rows, 32, 8, 128
+    gen = torch.Generator(device=dev).manual_seed(7)
+    q = torch.randn(T, Hq, Dh, device=dev, generator=gen).to(torch.bfloat16)
+    k = torch.randn(T, Hkv, Dh, device=dev, generator=gen).to(torch.bfloat16)
+    v = torch.randn(T, Hkv, Dh, device=dev, generator=gen).to(torch.bfloat16)
+    pos = torch.arange(50000, 50000 + T, device=dev)
+    slots = pos % (2 * T)
+    kc = torch.zeros(2 * T, Hkv, Dh, device=dev, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    q_out = torch.empty_like(q)
+
+    def once():
+        rn.rmsnorm_rope_kv_append(q, k, v, pos, slots, kc, vc, rope_base=500000.0, q_out=q_out)
+    for _ in range(max(1, args.warmup)):
+        once()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.reps):
+        once()
+    b.record()
+    torch.cuda.synchronize()
+    us = 1e3 * a.elapsed_time(b) / args.reps
+    print("op=rope tokens=%d heads=%d/%d Dh=%d us=%.2f GB/s=%.1f" % (
+        T, Hq, Hkv, Dh, us, rope_bytes(T, Hq, Hkv, Dh) / us / 1e3), flush=True)
+    return 0
+
+
 def run_single_op(args):
     """One op on a case of the prefill recipe (for ncu captures of one kernel)."""
     from rmsnorm_fwd_bwd_add_gb300 import build, workloads as W
     import rmsnorm_fwd_bwd_add_gb300 as rn
     build.build()
     dev = torch.device("cuda", 0)
+    if args.op == "rope":
+        return run_rope(args, rn, dev)
     c = W.config4_on_device(args.D, dev, args.rows)
     x, res, w, g = c.x, c.residual, c.w, c.g
     out, nr, gx = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
@@ -636,7 +674,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=("fwd", "vjp", "fvjp", "gate"),
+    ap.add_argument("--op", choices=("fwd", "vjp", "fvjp", "gate", "rope"),
                     help="profiling mode: run one op of the prefill recipe at --rows x --D "
                          "(--reps launches after --warmup) and print its mean time; no JSON line")
     ap.add_argument("--rows", type=int, default=8192)

@@ -4,15 +4,16 @@
 // writes k and v into the cache slab or a paged pool block, with cos/sin
 // from a precomputed table or computed on the fly).
 //
-// Persistent CTAs walk the tokens.  For each token the CTA first fills a
-// shared-memory table of the Dh/2 (cos, sin) pairs of its position -- read from
-// the caller's table or computed -- and then every q and k head of the token
-// rotates with it; v is copied.  Vectorised threads own 8 rotation pairs each
+// Persistent CTAs walk groups of four consecutive tokens.  For each group the
+// CTA first fills a shared-memory table of the Dh/2 (cos, sin) pairs of each
+// token's position -- read from the caller's table or computed -- and then
+// every q and k head of those tokens rotates with it; v is copied.  Vectorised threads own 8 rotation pairs each
 // (two 16-byte vectors in the rotate-half layout, one in the interleaved one).
 //
-// On-the-fly angles without FP64 in the loop: theta_i = p * base^(-2i/Dh).
-// base^(-2i/Dh) is computed once per CTA in double and split into a hi + lo
-// pair of floats; per token p * (hi + lo) is formed as a double-float
+// On-the-fly angles without FP64 on the device: theta_i = p * base^(-2i/Dh).
+// base^(-2i/Dh) is computed on the host in double (cached per thread for the
+// last base and Dh) and split into a hi + lo pair of floats passed with the
+// launch; per token p * (hi + lo) is formed as a double-float
 // (an exact product error from fmaf), reduced modulo 2 pi with 2 pi split in
 // two floats (Cody-Waite reduction), and sincosf takes the reduced angle:
 // about 1e-8 rad of error at p = 1e6, where a plain float product is off by
@@ -24,6 +25,7 @@
 #include "rmsnorm.h"
 
 #include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 #include "launch_util.h"
@@ -41,6 +43,7 @@ using namespace rmsn;
 constexpr int ROPE_NT = 256;
 constexpr int ROPE_CTAS_PER_SM = 4;
 constexpr int ROPE_MAX_DH = 1024;
+constexpr int ROPE_TOKENS_PER_ITER = 4;  // tokens a CTA handles between barriers
 constexpr unsigned int DEVSTATUS_BAD_INDEX = 2u;
 
 constexpr double TWO_PI = 6.283185307179586476925286766559;
@@ -49,6 +52,7 @@ constexpr float TWO_PI_LO = (float)(TWO_PI - (double)TWO_PI_HI);
 constexpr float INV_TWO_PI = (float)(1.0 / TWO_PI);
 
 struct RopeArgs {
+    float2 inv[ROPE_MAX_DH / 2];  // (hi, lo) floats of base^(-2i/Dh), from the host in double
     const void *q, *k, *v;
     const int64_t *positions, *slots;
     void *q_out, *k_cache, *v_cache;
@@ -75,18 +79,13 @@ __device__ __forceinline__ float reduced_angle(int64_t p, float inv_hi, float in
 
 template <typename T, bool INTERLEAVED, bool VEC>
 __global__ void __launch_bounds__(ROPE_NT, ROPE_CTAS_PER_SM) rope_kv_kernel(const RopeArgs a) {
-    __shared__ float2 inv[ROPE_MAX_DH / 2];  // (hi, lo) of base^(-2i/Dh)
-    __shared__ float2 cs[ROPE_MAX_DH / 2];   // (cos, sin) of the current token
+    constexpr int TPI = ROPE_TOKENS_PER_ITER;
+    __shared__ float2 cs[TPI][ROPE_MAX_DH / 2];   // (cos, sin) of the group's tokens
+    __shared__ int64_t s_slot[TPI];
+    __shared__ int s_flags[TPI];                  // bit 0: position valid, bit 1: write k/v
     const int tid = threadIdx.x;
     const int Dh = a.Dh, half = Dh / 2;
     const bool table = a.cos_sin != nullptr;
-    if (!table) {
-        for (int i = tid; i < half; i += ROPE_NT) {
-            const double f = pow((double)a.base, -2.0 * (double)i / (double)Dh);
-            const float hi = (float)f;
-            inv[i] = make_float2(hi, (float)(f - (double)hi));
-        }
-    }
     griddep_wait();  // programmatic dependent: no global access before this
 
     const T *q = static_cast<const T *>(a.q);
@@ -102,29 +101,48 @@ __global__ void __launch_bounds__(ROPE_NT, ROPE_CTAS_PER_SM) rope_kv_kernel(cons
     const int rot_units = half / PAIRS;
     const int v_units = VEC ? Dh / 8 : Dh;
     const int nq = a.Hq * rot_units, nk = a.Hkv * rot_units, nv = a.Hkv * v_units;
+    const int per_token = nq + nk + nv;
 
-    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-        const int64_t p = a.positions[t];
-        const int64_t slot = a.slots[t];
-        const bool pos_ok = p >= 0 && (!table || p < a.max_pos);
-        const bool slot_ok = slot < a.num_slots;  // negative: not written
-        if ((!pos_ok || !slot_ok) && tid == 0) atomicOr(a.status, DEVSTATUS_BAD_INDEX);
-        if (pos_ok) {
-            for (int i = tid; i < half; i += ROPE_NT) {
-                float c, s;
+    // CTA b takes the groups of TPI consecutive tokens b, b + grid, ...
+    for (int64_t t0 = (int64_t)blockIdx.x * TPI; t0 < a.T; t0 += (int64_t)gridDim.x * TPI) {
+        if (tid < TPI) {
+            const int64_t t = t0 + tid;
+            int flags = 0;
+            int64_t slot = -1;
+            if (t < a.T) {
+                const int64_t p = a.positions[t];
+                slot = a.slots[t];
+                const bool pos_ok = p >= 0 && (!table || p < a.max_pos);
+                const bool slot_ok = slot < a.num_slots;  // negative: not written
+                if (!pos_ok || !slot_ok) atomicOr(a.status, DEVSTATUS_BAD_INDEX);
+                flags = (pos_ok ? 1 : 0) | (pos_ok && slot_ok && slot >= 0 ? 2 : 0);
+            }
+            s_slot[tid] = slot;
+            s_flags[tid] = flags;
+        }
+        __syncthreads();
+        for (int e = tid; e < TPI * half; e += ROPE_NT) {
+            const int j = e / half, i = e - j * half;
+            if (s_flags[j] & 1) {
+                const int64_t p = a.positions[t0 + j];
+                float c, sn;
                 if (table) {
                     c = a.cos_sin[p * Dh + i];
-                    s = a.cos_sin[p * Dh + half + i];
+                    sn = a.cos_sin[p * Dh + half + i];
                 } else {
-                    sincosf(reduced_angle(p, inv[i].x, inv[i].y), &s, &c);
+                    sincosf(reduced_angle(p, a.inv[i].x, a.inv[i].y), &sn, &c);
                 }
-                cs[i] = make_float2(c, s);
+                cs[j][i] = make_float2(c, sn);
             }
         }
         __syncthreads();
-        const bool write_kv = pos_ok && slot_ok && slot >= 0;
-        const int n_items = pos_ok ? nq + (write_kv ? nk + nv : 0) : 0;
-        for (int it = tid; it < n_items; it += ROPE_NT) {
+        for (int e = tid; e < TPI * per_token; e += ROPE_NT) {
+            const int j = e / per_token, it = e - j * per_token;
+            const int flags = s_flags[j];
+            if (!(flags & 1) || (it >= nq && !(flags & 2))) continue;
+            const int64_t t = t0 + j;
+            const int64_t slot = s_slot[j];
+            const float2 *csj = cs[j];
             if (it < nq + nk) {
                 const bool is_q = it < nq;
                 const int u = is_q ? it : it - nq;
@@ -138,10 +156,10 @@ __global__ void __launch_bounds__(ROPE_NT, ROPE_CTAS_PER_SM) rope_kv_kernel(cons
                     unpack8<T>(*reinterpret_cast<const uint4 *>(src + i0), x1);
                     unpack8<T>(*reinterpret_cast<const uint4 *>(src + half + i0), x2);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 c0 = cs[i0 + 2 * e], c1 = cs[i0 + 2 * e + 1];
-                        y1[e] = make_float2(x1[e].x * c0.x - x2[e].x * c0.y, x1[e].y * c1.x - x2[e].y * c1.y);
-                        y2[e] = make_float2(x2[e].x * c0.x + x1[e].x * c0.y, x2[e].y * c1.x + x1[e].y * c1.y);
+                    for (int m = 0; m < 4; ++m) {
+                        const float2 c0 = csj[i0 + 2 * m], c1 = csj[i0 + 2 * m + 1];
+                        y1[m] = make_float2(x1[m].x * c0.x - x2[m].x * c0.y, x1[m].y * c1.x - x2[m].y * c1.y);
+                        y2[m] = make_float2(x2[m].x * c0.x + x1[m].x * c0.y, x2[m].y * c1.x + x1[m].y * c1.y);
                     }
                     *reinterpret_cast<uint4 *>(dst + i0) = pack8<T>(y1);
                     *reinterpret_cast<uint4 *>(dst + half + i0) = pack8<T>(y2);
@@ -150,16 +168,16 @@ __global__ void __launch_bounds__(ROPE_NT, ROPE_CTAS_PER_SM) rope_kv_kernel(cons
                     float2 x[4], y[4];
                     unpack8<T>(*reinterpret_cast<const uint4 *>(src + j0), x);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 cc = cs[c * 4 + e];
-                        y[e] = make_float2(x[e].x * cc.x - x[e].y * cc.y, x[e].y * cc.x + x[e].x * cc.y);
+                    for (int m = 0; m < 4; ++m) {
+                        const float2 cc = csj[c * 4 + m];
+                        y[m] = make_float2(x[m].x * cc.x - x[m].y * cc.y, x[m].y * cc.x + x[m].x * cc.y);
                     }
                     *reinterpret_cast<uint4 *>(dst + j0) = pack8<T>(y);
                 } else {
                     const int ia = INTERLEAVED ? 2 * c : c;
                     const int ib = INTERLEAVED ? 2 * c + 1 : c + half;
                     const float xa = Cvt<T>::load1(src + ia), xb = Cvt<T>::load1(src + ib);
-                    const float2 cc = cs[c];
+                    const float2 cc = csj[c];
                     Cvt<T>::store1(dst + ia, xa * cc.x - xb * cc.y);
                     Cvt<T>::store1(dst + ib, xb * cc.x + xa * cc.y);
                 }
@@ -174,7 +192,7 @@ __global__ void __launch_bounds__(ROPE_NT, ROPE_CTAS_PER_SM) rope_kv_kernel(cons
                     dst[c] = src[c];
             }
         }
-        __syncthreads();  // cs is rewritten for the next token
+        __syncthreads();  // cs, s_slot and s_flags are rewritten for the next group
     }
     griddep_launch_dependents();
 }
@@ -184,6 +202,24 @@ cudaError_t launch_rope_t(const RopeArgs &a, bool vec, int grid, cudaStream_t s)
     if (vec)
         return launch_pdl(rope_kv_kernel<T, INTERLEAVED, true>, dim3(grid), dim3(ROPE_NT), 0, s, a);
     return launch_pdl(rope_kv_kernel<T, INTERLEAVED, false>, dim3(grid), dim3(ROPE_NT), 0, s, a);
+}
+
+// base^(-2i/Dh) for i < Dh/2 as (hi, lo) float pairs; the last (base, Dh) of
+// the calling thread is kept, as a model calls with the same pair every layer.
+void inverse_frequencies(float base, int Dh, float2 *inv) {
+    thread_local float last_base = -1.f;
+    thread_local int last_dh = -1;
+    thread_local float2 last[ROPE_MAX_DH / 2];
+    if (base != last_base || Dh != last_dh) {
+        for (int i = 0; i < Dh / 2; ++i) {
+            const double f = std::pow((double)base, -2.0 * (double)i / (double)Dh);
+            const float hi = (float)f;
+            last[i] = make_float2(hi, (float)(f - (double)hi));
+        }
+        last_base = base;
+        last_dh = Dh;
+    }
+    std::copy(last, last + Dh / 2, inv);
 }
 
 bool al16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -233,6 +269,7 @@ extern "C" int rmsnorm_rope_kv_append(const void *q, const void *k, const void *
     int st = current_sm_count(&sm);
     if (st == RMSNORM_OK) st = current_status_word(&status);
     if (st != RMSNORM_OK) return st;
+    static_assert(sizeof(RopeArgs) < 8192, "kernel parameters stay small");
     RopeArgs a{};
     a.q = q; a.k = k; a.v = v;
     a.positions = positions; a.slots = slots;
@@ -241,9 +278,11 @@ extern "C" int rmsnorm_rope_kv_append(const void *q, const void *k, const void *
     a.T = T; a.num_slots = num_slots;
     a.Hq = (int)Hq; a.Hkv = (int)Hkv; a.Dh = (int)Dh;
     a.status = status;
+    if (!cos_sin) inverse_frequencies(rope_base, (int)Dh, a.inv);
     const bool vec = Dh % 16 == 0 && al16(q) && al16(q_out) && (Hkv == 0 ||
                      (al16(k) && al16(v) && al16(k_cache) && al16(v_cache)));
-    const int grid = (int)std::min<int64_t>(T, (int64_t)sm * ROPE_CTAS_PER_SM);
+    const int64_t groups = (T + ROPE_TOKENS_PER_ITER - 1) / ROPE_TOKENS_PER_ITER;
+    const int grid = (int)std::min<int64_t>(groups, (int64_t)sm * ROPE_CTAS_PER_SM);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (dtype == RMSNORM_F16)
