@@ -21,6 +21,8 @@ Sources (web pages, by title and section):
   * "Fused residual-add RMSNorm and fused RoPE + KV-append decode kernels",
     Background, third bullet -- the gated activation silu(x[:d]) * x[d:2d];
     second bullet and Task item 3 -- rope on q and k with the KV-cache append.
+  * The same two pages' rsqrt(mean(h^2) + eps) factor -- rstd, the per-row
+    scale a forward can hand to the backward, and the VJP that takes it.
 """
 from __future__ import annotations
 
@@ -73,6 +75,12 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.rmsnorm_oracle_fused_vjp.restype = None
     lib.rmsnorm_oracle_gated_silu.argtypes = [_dp, _dp, ctypes.c_int64, ctypes.c_int64]
     lib.rmsnorm_oracle_gated_silu.restype = None
+    lib.rmsnorm_oracle_rstd.argtypes = [_dp, _dp, ctypes.c_double, _dp, ctypes.c_int64,
+                                        ctypes.c_int64]
+    lib.rmsnorm_oracle_rstd.restype = None
+    lib.rmsnorm_oracle_vjp_rstd.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_double, _dp, _dp,
+                                            ctypes.c_int64, ctypes.c_int64]
+    lib.rmsnorm_oracle_vjp_rstd.restype = None
     _ip = ctypes.POINTER(ctypes.c_int64)
     lib.rmsnorm_oracle_rope_kv_append.argtypes = [_dp, _dp, _dp, _ip, _ip, _dp, _dp, _dp, _dp,
                                                   ctypes.c_double, ctypes.c_int, ctypes.c_int64,
@@ -133,6 +141,31 @@ class Oracle:
                                      self._ptr(gx), self._ptr(gw), rows, D)
         return gx, gw
 
+    def rstd(self, x, eps, residual=None):
+        """Per-row 1 / sqrt(mean(h^2) + eps) of h = x + residual (or x), shape
+        (rows,)."""
+        x = self._arr(x)
+        rows, D = x.shape
+        res = None if residual is None else self._arr(residual, (rows, D))
+        out = np.empty((rows,), np.float64)
+        self._lib.rmsnorm_oracle_rstd(self._ptr(x), self._ptr(res), self.scalar(eps),
+                                      self._ptr(out), rows, D)
+        return out
+
+    def vjp_rstd(self, x, w, g, rstd, weight_bias=0.0):
+        """The VJP with the per-row scale rstd (shape (rows,)) supplied instead
+        of recomputed; returns (gx, gw)."""
+        x = self._arr(x)
+        rows, D = x.shape
+        w = self._arr(w, (D,))
+        g = self._arr(g, (rows, D))
+        rstd = self._arr(rstd, (rows,))
+        gx = np.empty((rows, D), np.float64)
+        gw = np.empty((D,), np.float64)
+        self._lib.rmsnorm_oracle_vjp_rstd(self._ptr(x), self._ptr(w), self._ptr(g),
+                                          self._ptr(rstd), self.scalar(weight_bias),
+                                          self._ptr(gx), self._ptr(gw), rows, D)
+        return gx, gw
 
     def fused_vjp(self, h, w, g_out, eps, weight_bias=0.0, g_residual=None):
         """VJP of the two-output fused op at h = x + residual: returns (g_h, gw),
@@ -205,6 +238,14 @@ def fwd(x, w, eps, weight_bias=0.0, residual=None):
 
 def vjp(x, w, g, eps, weight_bias=0.0):
     return load().vjp(x, w, g, eps, weight_bias)
+
+
+def rstd(x, eps, residual=None):
+    return load().rstd(x, eps, residual)
+
+
+def vjp_rstd(x, w, g, rstd, weight_bias=0.0):
+    return load().vjp_rstd(x, w, g, rstd, weight_bias)
 
 
 def fused_vjp(h, w, g_out, eps, weight_bias=0.0, g_residual=None):

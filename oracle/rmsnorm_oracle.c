@@ -214,3 +214,58 @@ void rmsnorm_oracle_rope_kv_append(const double *q, const double *k, const doubl
         }
     }
 }
+
+/*
+ * The per-row scale of the forward on its own ("Fused residual-add RMSNorm
+ * and fused RoPE + KV-append decode kernels", Background, FusedAddRMSNorm
+ * bullet: the rsqrt of the mean square plus eps; "RMSNormVJP backward writes
+ * a full {n_rows, D} gw_temp intermediate", POC section: the same rsqrt factor
+ * in the eager reference):
+ *     rstd_i = 1 / sqrt((1/D) * sum_j h_j^2 + eps),   h = x + residual, or x.
+ * The forward multiplies row i by exactly this value, so a backward pass can
+ * take it instead of summing h^2 again.
+ */
+void rmsnorm_oracle_rstd(const double *x, const double *residual, double eps,
+                         double *rstd, int64_t rows, int64_t D)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        double sq = 0.0;
+        for (int64_t j = 0; j < D; ++j) {
+            double hv = residual ? x[i * D + j] + residual[i * D + j] : x[i * D + j];
+            sq += hv * hv;
+        }
+        rstd[i] = 1.0 / sqrt(sq / (double)D + eps);
+    }
+}
+
+/*
+ * The VJP with each row's scale supplied (rstd[i], as the forward saved it)
+ * instead of recomputed from h.  Per row, with rho = rstd[i] and
+ * w'_j = weight_bias + w_j:
+ *     dot   = sum_j g_j * w'_j * h_j
+ *     gx_k  = rho * g_k * w'_k - (rho^3 / D) * h_k * dot
+ *     gw_k += g_k * h_k * rho           (summed over rows, ascending)
+ * With rstd[i] = 1 / sqrt(mean(h_i^2) + eps) this is rmsnorm_oracle_vjp; eps
+ * enters only through rstd.  gw is overwritten.
+ */
+void rmsnorm_oracle_vjp_rstd(const double *x, const double *w, const double *g,
+                             const double *rstd, double weight_bias, double *gx,
+                             double *gw, int64_t rows, int64_t D)
+{
+    for (int64_t j = 0; j < D; ++j)
+        gw[j] = 0.0;
+
+    for (int64_t i = 0; i < rows; ++i) {
+        const double rho = rstd[i];
+        double dg = 0.0;
+        for (int64_t j = 0; j < D; ++j)
+            dg += g[i * D + j] * (weight_bias + w[j]) * x[i * D + j];
+
+        const double k3 = rho * rho * rho / (double)D;
+        for (int64_t j = 0; j < D; ++j) {
+            gx[i * D + j] = rho * g[i * D + j] * (weight_bias + w[j])
+                            - k3 * x[i * D + j] * dg;
+            gw[j] += g[i * D + j] * x[i * D + j] * rho;
+        }
+    }
+}

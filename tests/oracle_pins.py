@@ -436,6 +436,60 @@ def pin_kv_append(orc):
         _close(vr[pos[t] % 4], vd[t], 0, 0, "ring v")
 
 
+def pin_rstd(orc):
+    """rstd is 1 / sqrt(||h||^2 / D + eps), written with a library norm, for
+    h = x + residual and h = x; a constant row c gives 1 / sqrt(c^2 + eps);
+    and the forward's out is exactly h * rstd * (weight_bias + w)."""
+    rng = _rng(21)
+    for R, D in ((4, 16), (3, 257), (1, 1)):
+        x = rng.normal(size=(R, D)) * rng.uniform(0.1, 10, size=(R, 1))
+        res = rng.normal(size=(R, D))
+        eps = 1e-3
+        for r in (None, res):
+            h = x if r is None else x + r
+            got = orc.rstd(x, eps, r)
+            nrm = np.linalg.norm(h, axis=1)
+            _close(got, 1.0 / np.sqrt(nrm ** 2 / D + orc.scalar(eps)), 1e-13, 0,
+                   "rstd R=%d D=%d" % (R, D))
+            w = rng.normal(1.0, 0.2, size=D)
+            out, _ = orc.fwd(x, w, eps, 0.75, r)
+            _close(out, h * got[:, None] * (0.75 + w), 1e-14, 1e-300, "out = h rstd w'")
+    c = np.array([[2.5] * 6, [-0.125] * 6])
+    _close(orc.rstd(c, 0.5), [1 / np.sqrt(6.25 + 0.5), 1 / np.sqrt(0.015625 + 0.5)], 1e-15, 0,
+           "constant rows")
+
+
+def pin_vjp_rstd(orc):
+    """The VJP with a supplied per-row scale rho: a hand-worked two-row example
+    (w' = [1, 2], rho = 0.5 and 2), D = 1's closed form
+    gx = g w' rho (1 - rho^2 h^2), gw = g h rho, and the plain VJP when rho is
+    the forward's rstd."""
+    h = np.array([[1.0, 2.0], [0.0, 3.0]])
+    g = np.array([[1.0, 0.0], [2.0, 1.0]])
+    w = np.array([0.5, 1.5])  # w' = weight_bias + w = [1, 2] with weight_bias 0.5
+    # row 0: dot = 1*1*1 = 1, rho^3/D = 1/16: gx = [1/2 - 1/16, -2/16]
+    # row 1: dot = 1*2*3 = 6, rho^3/D = 4:    gx = [4, 4 - 72]
+    # gw = [1*1*0.5 + 2*0*2, 0*2*0.5 + 1*3*2] = [0.5, 6]
+    gx, gw = orc.vjp_rstd(h, w, g, [0.5, 2.0], 0.5)
+    _close(gx, [[0.4375, -0.125], [4.0, -68.0]], 0, 0, "worked example gx")
+    _close(gw, [0.5, 6.0], 0, 0, "worked example gw")
+    a, gg, ww, rho = np.array([[-1.5], [0.75]]), np.array([[2.0], [-3.0]]), 0.25, np.array([0.3, 1.7])
+    gx, gw = orc.vjp_rstd(a, np.array([ww]), gg, rho, 0.0)
+    want = gg * ww * rho[:, None] * (1 - rho[:, None] ** 2 * a ** 2)
+    _close(gx, want, 1e-14, 1e-16, "D=1 gx")
+    _close(gw, [np.sum(gg[:, 0] * a[:, 0] * rho)], 1e-14, 0, "D=1 gw")
+    rng = _rng(22)
+    R, D = 5, 37
+    x = rng.normal(size=(R, D)) * rng.uniform(0.5, 4, size=(R, 1))
+    w = rng.normal(1.0, 0.2, size=D)
+    g = rng.normal(size=(R, D))
+    for eps, wb in ((1e-5, 0.0), (0.25, 1.0)):
+        gx0, gw0 = orc.vjp(x, w, g, eps, wb)
+        gx1, gw1 = orc.vjp_rstd(x, w, g, orc.rstd(x, eps), wb)
+        _close(gx1, gx0, 1e-12, 1e-15, "vjp_rstd(rstd) = vjp gx")
+        _close(gw1, gw0, 1e-12, 1e-15, "vjp_rstd(rstd) = vjp gw")
+
+
 ALL_PINS = [
     pin_worked_examples,
     pin_constant_rows,
@@ -453,4 +507,6 @@ ALL_PINS = [
     pin_gated_silu,
     pin_rope,
     pin_kv_append,
+    pin_rstd,
+    pin_vjp_rstd,
 ]

@@ -58,6 +58,17 @@ MUTANTS = [
     ("rope_token_for_position", "int64_t p = positions[t];", "int64_t p = t;", 0),
     ("kv_v_rotated", "v_cache[(slot * Hkv + h) * Dh + j] = v[(t * Hkv + h) * Dh + j];",
      "v_cache[(slot * Hkv + h) * Dh + j] = k_cache[(slot * Hkv + h) * Dh + j];", 0),
+    ("rstd_eps_dropped", "rstd[i] = 1.0 / sqrt(sq / (double)D + eps);",
+     "rstd[i] = 1.0 / sqrt(sq / (double)D);", 0),
+    ("rstd_residual_ignored", "double hv = residual ? x[i * D + j] + residual[i * D + j] : x[i * D + j];",
+     "double hv = x[i * D + j];", 0),
+    ("vjp_rstd_row0_scale", "const double rho = rstd[i];", "const double rho = rstd[0];", 0),
+    ("vjp_rstd_rho_squared", "rho * rho * rho / (double)D", "rho * rho / (double)D", 0),
+    ("vjp_rstd_gw_missing_rho", "gw[j] += g[i * D + j] * x[i * D + j] * rho;",
+     "gw[j] += g[i * D + j] * x[i * D + j];", 0),
+    ("vjp_rstd_dot_without_weight", "dg += g[i * D + j] * (weight_bias + w[j]) * x[i * D + j];",
+     "dg += g[i * D + j] * x[i * D + j];", 0),
+    ("vjp_rstd_gx_sign", "- k3 * x[i * D + j] * dg;", "+ k3 * x[i * D + j] * dg;", 0),
     ("kv_slot_is_token", "int64_t slot = slots[t];", "int64_t slot = slots[t] < 0 ? -1 : t % 4;", 0),
 ]
 
