@@ -26,23 +26,31 @@
  *     gx_j = r * g_j * w'_j - (r^3 / D) * h_j * dot
  *     gw_j = sum over rows of g_j * h_j * r
  *
- * Numerics: inputs and outputs are fp16 or bf16; all arithmetic is fp32; every
- * fp16/bf16 output element is rounded once, to nearest-even, from fp32.  h is
- * normalised unrounded (the fp32 sum), new_residual is its rounding.  gw is
- * fp32 and bit-identical from run to run on the same device for the same
- * (rows, D, dtype): its summation order is fixed and does not depend on timing.
+ * Numerics: inputs and outputs are fp16, bf16 or fp32; all arithmetic is fp32;
+ * every fp16/bf16 output element is rounded once, to nearest-even, from fp32.
+ * h is normalised unrounded (the fp32 sum), new_residual is its rounding.  gw
+ * is fp32 and bit-identical from run to run on the same device for the same
+ * (rows, D, dtype, strides): its summation order is fixed and does not depend
+ * on timing.
  *
- * Layout and ownership: every tensor is a dense row-major device buffer owned
- * by the caller: x, residual, out, new_residual, g, gx are [rows, D] of dtype;
- * w is [D] of dtype; gw is [D] fp32.  Pointers must be device pointers of the
+ * Layout and ownership: every tensor is a row-major device buffer owned by the
+ * caller: x, residual, out, new_residual, g, gx are [rows, D] of dtype, dense
+ * (rows D elements apart) for rmsnorm_fwd / rmsnorm_vjp / rmsnorm_fused_vjp,
+ * or with a row stride of their own (>= D elements; elements of a row are
+ * contiguous) for rmsnorm_fwd_ex / rmsnorm_vjp_ex; w is [D] of dtype, dense;
+ * gw and rstd are fp32, dense.  Pointers must be device pointers of the
  * current device (cudaGetDevice) and `stream` a cudaStream_t of that device
  * (NULL = legacy default stream), passed as void*.  Any alignment is accepted;
- * 16-byte aligned pointers with D * 2 a multiple of 16 take the fast kernels.
+ * 16-byte aligned pointers and row strides with D * sizeof(element) a
+ * multiple of 16 take the fast kernels.
  *
- * Aliasing: an output may be the very same buffer as an input of the same
- * shape (out == x, new_residual == residual, gx == g, ...): every element is
- * read before the same thread writes it.  Any other overlap, and any overlap
- * of two outputs, is rejected with RMSNORM_ERR_INVALID_ARG.
+ * Aliasing: an output may be the very same tensor as an input (same pointer
+ * and row stride: out == x, new_residual == residual, gx == g, ...): every
+ * element is read before the same thread writes it.  Any other overlap, and
+ * any overlap of two outputs, is rejected with RMSNORM_ERR_INVALID_ARG.  For
+ * tensors with equal row strides the test is exact, so the disjoint halves of
+ * one [rows, 2D] buffer are accepted as two tensors of row stride 2D; tensors
+ * with different strides must not share their address ranges.
  *
  * Asynchrony and errors: calls enqueue work on `stream` and return without
  * synchronising.  Every call returns an rmsnorm_status_t and never aborts.
@@ -65,7 +73,9 @@ extern "C" {
 
 typedef enum {
     RMSNORM_F16 = 0,  /* IEEE binary16 */
-    RMSNORM_BF16 = 1  /* bfloat16 */
+    RMSNORM_BF16 = 1, /* bfloat16 */
+    RMSNORM_F32 = 2   /* IEEE binary32 (norm entry points only; the gate and
+                         the rotary embedding take fp16 or bf16) */
 } rmsnorm_dtype_t;
 
 typedef enum {
@@ -73,7 +83,8 @@ typedef enum {
     RMSNORM_ERR_INVALID_ARG = 1,  /* null pointer, D <= 0, rows < 0, bad dtype,
                                      eps < 0 or not finite, weight_bias not
                                      finite, residual/new_residual mismatch,
-                                     overlapping buffers, too small workspace */
+                                     row stride < D, overlapping buffers, too
+                                     small workspace */
     RMSNORM_ERR_UNSUPPORTED = 2,  /* D > RMSNORM_MAX_D, or rows * D overflows */
     RMSNORM_ERR_CUDA = 3,         /* a CUDA runtime call failed */
     RMSNORM_ERR_NO_MEMORY = 4,    /* scratch allocation failed */
@@ -143,6 +154,40 @@ int rmsnorm_vjp(const void *x, const void *w, const void *g, float eps,
 int rmsnorm_fused_vjp(const void *h, const void *w, const void *g_out,
                       const void *g_residual, float eps, float weight_bias, void *g_h,
                       float *gw, int64_t rows, int64_t D, int dtype, void *stream);
+
+/*
+ * The forward with row strides and the per-row scale.  As rmsnorm_fwd, plus:
+ *   ld_x, ld_residual, ld_out, ld_new_residual  row strides in elements
+ *                (>= D; ignored for a NULL tensor and when rows == 1).
+ *   rstd         [rows] fp32, receives r_i = 1 / sqrt(mean(h_i^2) + eps), the
+ *                value row i was multiplied by, for reuse by rmsnorm_vjp_ex;
+ *                or NULL.
+ * Sources: the forward's definition above (the rsqrt factor of the
+ * FusedAddRMSNorm bullet); the pages do not name strided rows or a saved
+ * rstd: they are the layout of a slice of a wider buffer and the scalar a
+ * backward pass would otherwise recompute.  rmsnorm_fwd is this call with
+ * every stride D and rstd NULL.
+ */
+int rmsnorm_fwd_ex(const void *x, int64_t ld_x, const void *residual, int64_t ld_residual,
+                   const void *w, float eps, float weight_bias, void *out, int64_t ld_out,
+                   void *new_residual, int64_t ld_new_residual, float *rstd, int64_t rows,
+                   int64_t D, int dtype, void *stream);
+
+/*
+ * The VJP (plain, or of the two-output fused op) with row strides and an
+ * optional saved per-row scale.  As rmsnorm_fused_vjp (g_residual NULL gives
+ * rmsnorm_vjp), plus:
+ *   ld_x, ld_g, ld_g_residual, ld_gx  row strides in elements (>= D).
+ *   rstd   [rows] fp32 or NULL.  Given, row i uses r = rstd[i] in place of
+ *          1 / sqrt(mean(x_i^2) + eps) (eps is then unused); pass what
+ *          rmsnorm_fwd_ex wrote for the same rows.  It saves the sum of
+ *          squares (arithmetic only: the same bytes move either way).
+ * gw scratch comes from the library's pool as for rmsnorm_vjp.
+ */
+int rmsnorm_vjp_ex(const void *x, int64_t ld_x, const void *w, const void *g, int64_t ld_g,
+                   const void *g_residual, int64_t ld_g_residual, const float *rstd, float eps,
+                   float weight_bias, void *gx, int64_t ld_gx, float *gw, int64_t rows, int64_t D,
+                   int dtype, void *stream);
 
 /*
  * Bytes of scratch rmsnorm_vjp_ws needs for this problem on the current

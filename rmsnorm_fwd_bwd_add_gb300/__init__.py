@@ -9,6 +9,9 @@ include/rmsnorm.h (librmsnorm_gb300.so), with these thin Python bindings:
                   the kernels (deterministic, no [rows, D] temporary).
   rmsnorm_fused_vjp -- VJP of the two-output fused op (adds the gradient that
                   reaches new_residual in the same pass).
+  rmsnorm_fwd_ex, rmsnorm_vjp_ex -- the same on rows a stride apart, with the
+                  forward's per-row scale (rstd) written and reused.
+  fp16, bf16 and fp32 tensors.
   fused_add_rmsnorm, rms_norm -- torch.autograd wrappers.
   rmsnorm_gated_silu -- the decode loop's gated activation silu(x[:d]) * x[d:].
   rmsnorm_rope_kv_append -- rotary embedding of q and k with the KV-cache append.
@@ -21,10 +24,12 @@ from .api import (  # noqa: F401
     rmsnorm_device_status,
     rmsnorm_fused_vjp,
     rmsnorm_fwd,
+    rmsnorm_fwd_ex,
     rmsnorm_gated_silu,
     rmsnorm_rope_kv_append,
     rmsnorm_status_string,
     rmsnorm_vjp,
+    rmsnorm_vjp_ex,
     rmsnorm_vjp_workspace_size,
     rmsnorm_vjp_ws,
 )
@@ -35,6 +40,8 @@ __all__ = [
     "rmsnorm_fwd",
     "rmsnorm_vjp",
     "rmsnorm_fused_vjp",
+    "rmsnorm_fwd_ex",
+    "rmsnorm_vjp_ex",
     "rmsnorm_gated_silu",
     "rmsnorm_rope_kv_append",
     "fused_add_rmsnorm",

@@ -17,6 +17,8 @@ EXPORTS = (
     "rmsnorm_fwd",
     "rmsnorm_vjp",
     "rmsnorm_fused_vjp",
+    "rmsnorm_fwd_ex",
+    "rmsnorm_vjp_ex",
     "rmsnorm_gated_silu",
     "rmsnorm_rope_kv_append",
     "rmsnorm_vjp_workspace_size",
@@ -70,6 +72,12 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.rmsnorm_vjp.restype = _i
     lib.rmsnorm_fused_vjp.argtypes = [_vp, _vp, _vp, _vp, _f, _f, _vp, _vp, _i64, _i64, _i, _vp]
     lib.rmsnorm_fused_vjp.restype = _i
+    lib.rmsnorm_fwd_ex.argtypes = [_vp, _i64, _vp, _i64, _vp, _f, _f, _vp, _i64, _vp, _i64, _vp,
+                                   _i64, _i64, _i, _vp]
+    lib.rmsnorm_fwd_ex.restype = _i
+    lib.rmsnorm_vjp_ex.argtypes = [_vp, _i64, _vp, _vp, _i64, _vp, _i64, _vp, _f, _f, _vp, _i64,
+                                   _vp, _i64, _i64, _i, _vp]
+    lib.rmsnorm_vjp_ex.restype = _i
     lib.rmsnorm_gated_silu.argtypes = [_vp, _vp, _i64, _i64, _i, _vp]
     lib.rmsnorm_gated_silu.restype = _i
     lib.rmsnorm_rope_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _f,

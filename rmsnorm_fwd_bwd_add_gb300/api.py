@@ -4,9 +4,10 @@ Every function checks dtype, device, contiguity and shape, then passes raw
 pointers and the current CUDA stream to librmsnorm_gb300.so.  All arithmetic
 runs in the library's CUDA kernels; nothing here computes.
 
-Tensors: x, residual, g are [..., D] fp16 or bf16 CUDA tensors, contiguous;
-w is [D] of the same dtype; gw is [D] fp32.  Leading dimensions are flattened
-into rows.
+Tensors: x, residual, g are [..., D] fp16, bf16 or fp32 CUDA tensors,
+contiguous (the *_ex functions also take rows a stride apart: a slice of a
+wider buffer); w is [D] of the same dtype; gw and rstd are fp32.  Leading
+dimensions are flattened into rows.
 """
 from __future__ import annotations
 
@@ -17,14 +18,16 @@ import torch
 
 from . import _native
 
-_DTYPES = {torch.float16: 0, torch.bfloat16: 1}
+_DTYPES = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
 
 
-def _dtype_code(t: torch.Tensor) -> int:
-    try:
-        return _DTYPES[t.dtype]
-    except KeyError:
-        raise TypeError("unsupported dtype %s (fp16 or bf16)" % t.dtype) from None
+def _dtype_code(t: torch.Tensor, allowed=(0, 1, 2)) -> int:
+    code = _DTYPES.get(t.dtype)
+    if code is None or code not in allowed:
+        names = {0: "fp16", 1: "bf16", 2: "fp32"}
+        raise TypeError("unsupported dtype %s (%s)" % (
+            t.dtype, " or ".join(names[c] for c in allowed))) from None
+    return code
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -86,6 +89,47 @@ class _OnDevice:
         if self.prev is not None:
             torch.cuda.set_device(self.prev)
         return False
+
+
+def _rows_ld(name: str, t: torch.Tensor) -> Tuple[int, int, int]:
+    """(rows, D, row stride in elements) of a [..., D] CUDA tensor whose rows
+    are contiguous and whose leading dimensions flatten to one row stride."""
+    if t.dim() < 1:
+        raise ValueError("%s must have at least one dimension" % name)
+    if not t.is_cuda:
+        raise ValueError("tensors must be CUDA tensors (there is no CPU path)")
+    D = t.shape[-1]
+    rows = t.numel() // D if D else 0
+    if D > 1 and t.stride(-1) != 1:
+        raise ValueError("%s: the elements of a row must be contiguous" % name)
+    lead = [(n, st) for n, st in zip(t.shape[:-1], t.stride()[:-1]) if n != 1]
+    if rows <= 1 or not lead:
+        return rows, D, D
+    for (n0, st0), (n1, st1) in zip(lead, lead[1:]):
+        if st0 != st1 * n1:
+            raise ValueError("%s: leading dimensions do not flatten to one row stride" % name)
+    if lead[-1][1] < D:
+        raise ValueError("%s: rows overlap (row stride %d < D = %d)" % (name, lead[-1][1], D))
+    return rows, D, lead[-1][1]
+
+
+def rows_layout_ok(t: torch.Tensor) -> bool:
+    """Whether the *_ex functions take t's layout as it is (contiguous rows,
+    one row stride >= D); callers copy other tensors with .contiguous()."""
+    try:
+        _rows_ld("t", t)
+    except ValueError:
+        return False
+    return True
+
+
+def _check_rows_like(name: str, t: torch.Tensor, ref: torch.Tensor) -> int:
+    """Checks dtype, device and shape against ref; returns t's row stride."""
+    if t.dtype != ref.dtype or t.device != ref.device:
+        raise ValueError("%s must be %s on %s" % (name, ref.dtype, ref.device))
+    if t.shape != ref.shape:
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(ref.shape), tuple(t.shape)))
+    return _rows_ld(name, t)[2]
 
 
 def _check_w(w: torch.Tensor, x: torch.Tensor, D: int) -> None:
@@ -178,7 +222,7 @@ def rmsnorm_gated_silu(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, s
         raise ValueError("the last dimension of x must be even (2d)")
     rows, two_d = _rows_d(x)
     d = two_d // 2
-    code = _dtype_code(x)
+    code = _dtype_code(x, (0, 1))
     if out is None:
         out = torch.empty(*x.shape[:-1], d, dtype=x.dtype, device=x.device)
     if (out.dtype != x.dtype or out.device != x.device or out.shape != (*x.shape[:-1], d)
@@ -207,7 +251,7 @@ def rmsnorm_rope_kv_append(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     Hkv = k.shape[1]
     if k.shape[0] != T or k.shape[2] != Dh:
         raise ValueError("k and v must be [T, Hkv, Dh] with q's T and Dh")
-    code = _dtype_code(q)
+    code = _dtype_code(q, (0, 1))
     for name, t in (("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache)):
         if t.dtype != q.dtype or t.device != q.device or not t.is_contiguous():
             raise ValueError("%s must be a contiguous %s tensor on %s" % (name, q.dtype, q.device))
@@ -234,6 +278,79 @@ def rmsnorm_rope_kv_append(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
             Dh, k_cache.shape[0], code, _stream(q.device, stream))
     _native.check("rmsnorm_rope_kv_append", st)
     return q_out
+
+
+def _check_rstd(rstd: torch.Tensor, rows: int, device: torch.device) -> None:
+    if (rstd.dtype != torch.float32 or rstd.numel() != rows or rstd.device != device
+            or not rstd.is_contiguous()):
+        raise ValueError("rstd must be a contiguous float32 tensor of %d elements on %s" % (
+            rows, device))
+
+
+def rmsnorm_fwd_ex(x: torch.Tensor, w: torch.Tensor, eps: float, weight_bias: float = 0.0,
+                   residual: Optional[torch.Tensor] = None, *, out: Optional[torch.Tensor] = None,
+                   new_residual: Optional[torch.Tensor] = None, rstd=None, stream=None):
+    """The forward on rows a stride apart (each of x, residual, out,
+    new_residual may be a slice of a wider buffer), optionally writing the
+    per-row scale.  rstd: None (not written), True (allocated here) or a
+    [rows] float32 tensor.  Returns (out, new_residual, rstd); new outputs
+    are allocated dense."""
+    rows, D, ld_x = _rows_ld("x", x)
+    code = _dtype_code(x)
+    _check_w(w, x, D)
+    ld_r = ld_n = D
+    if residual is not None:
+        ld_r = _check_rows_like("residual", residual, x)
+        if new_residual is None:
+            new_residual = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+        ld_n = _check_rows_like("new_residual", new_residual, x)
+    elif new_residual is not None:
+        raise ValueError("new_residual given without residual")
+    if out is None:
+        out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    ld_o = _check_rows_like("out", out, x)
+    if rstd is True:
+        rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    if rstd is not None:
+        _check_rstd(rstd, rows, x.device)
+    with _OnDevice(x.device):
+        st = _native.lib().rmsnorm_fwd_ex(_ptr(x), ld_x, _ptr(residual), ld_r, _ptr(w), eps,
+                                          weight_bias, _ptr(out), ld_o, _ptr(new_residual), ld_n,
+                                          _ptr(rstd), rows, D, code, _stream(x.device, stream))
+    _native.check("rmsnorm_fwd_ex", st)
+    return out, new_residual, rstd
+
+
+def rmsnorm_vjp_ex(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float,
+                   weight_bias: float = 0.0, g_residual: Optional[torch.Tensor] = None, *,
+                   rstd: Optional[torch.Tensor] = None, gx: Optional[torch.Tensor] = None,
+                   gw: Optional[torch.Tensor] = None, stream=None):
+    """The VJP (of the fused op when g_residual is given) on rows a stride
+    apart, optionally with the forward's per-row scale rstd ([rows] float32)
+    in place of recomputing it.  Returns (gx, gw)."""
+    rows, D, ld_x = _rows_ld("x", x)
+    code = _dtype_code(x)
+    _check_w(w, x, D)
+    ld_g = _check_rows_like("g", g, x)
+    ld_gr = D
+    if g_residual is not None:
+        ld_gr = _check_rows_like("g_residual", g_residual, x)
+    if gx is None:
+        gx = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    ld_gx = _check_rows_like("gx", gx, x)
+    if gw is None:
+        gw = torch.empty(D, dtype=torch.float32, device=x.device)
+    if (gw.dtype != torch.float32 or gw.shape != (D,) or gw.device != x.device
+            or not gw.is_contiguous()):
+        raise ValueError("gw must be a contiguous [%d] float32 tensor on %s" % (D, x.device))
+    if rstd is not None:
+        _check_rstd(rstd, rows, x.device)
+    with _OnDevice(x.device):
+        st = _native.lib().rmsnorm_vjp_ex(_ptr(x), ld_x, _ptr(w), _ptr(g), ld_g, _ptr(g_residual),
+                                          ld_gr, _ptr(rstd), eps, weight_bias, _ptr(gx), ld_gx,
+                                          _ptr(gw), rows, D, code, _stream(x.device, stream))
+    _native.check("rmsnorm_vjp_ex", st)
+    return gx, gw
 
 
 def rmsnorm_vjp_workspace_size(rows: int, D: int, dtype: torch.dtype) -> int:

@@ -1,11 +1,13 @@
 """torch.autograd wrappers over the C ABI.
 
 fused_add_rmsnorm(x, residual, w, eps, weight_bias) -> (out, new_residual)
-    forward: rmsnorm_fwd; backward: rmsnorm_fused_vjp on the saved
-    new_residual, giving one gradient for x and residual (they enter as a sum)
-    and gw.
+    forward: rmsnorm_fwd_ex, which also saves each row's scale (rstd);
+    backward: rmsnorm_vjp_ex on the saved new_residual with that rstd, giving
+    one gradient for x and residual (they enter as a sum) and gw.
 rms_norm(x, w, eps, weight_bias) -> out
-    forward: rmsnorm_fwd without a residual; backward: rmsnorm_vjp.
+    forward: rmsnorm_fwd_ex without a residual; backward: rmsnorm_vjp_ex.
+Inputs whose rows sit a stride apart (slices of wider buffers) are used in
+place; fp16, bf16 and fp32.
 
 The kernels accumulate gw in fp32; it is returned in w's dtype, as autograd
 expects a gradient of a parameter's own dtype.  Gradients that do not reach
@@ -20,29 +22,36 @@ from __future__ import annotations
 
 import torch
 
-from .api import rmsnorm_fused_vjp, rmsnorm_fwd, rmsnorm_vjp
+from .api import rmsnorm_fwd_ex, rmsnorm_vjp_ex, rows_layout_ok
+
+
+def _rows(t):
+    """t itself when the kernels take its layout (rows a stride apart), else a
+    dense copy (e.g. an expanded gradient of a sum)."""
+    return t if rows_layout_ok(t) else t.contiguous()
 
 
 class FusedAddRMSNormFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, x, residual, w, eps: float, weight_bias: float):
         ctx.set_materialize_grads(False)
-        out, new_res = rmsnorm_fwd(x.contiguous(), w.contiguous(), eps, weight_bias,
-                                   residual.contiguous())
-        ctx.save_for_backward(new_res, w)
+        out, new_res, rstd = rmsnorm_fwd_ex(_rows(x), w.contiguous(), eps, weight_bias,
+                                            _rows(residual), rstd=True)
+        ctx.save_for_backward(new_res, w, rstd)
         ctx.eps = eps
         ctx.weight_bias = weight_bias
         return out, new_res
 
     @staticmethod
     def backward(ctx, g_out, g_res):
-        new_res, w = ctx.saved_tensors
+        new_res, w, rstd = ctx.saved_tensors
         if g_out is None:
             g_h = None if g_res is None else g_res.contiguous()
             gw = torch.zeros_like(w) if ctx.needs_input_grad[2] else None
         else:
-            g_h, gw32 = rmsnorm_fused_vjp(new_res, w, g_out.contiguous(), ctx.eps, ctx.weight_bias,
-                                          None if g_res is None else g_res.contiguous())
+            g_h, gw32 = rmsnorm_vjp_ex(new_res, w.contiguous(), _rows(g_out), ctx.eps,
+                                       ctx.weight_bias, None if g_res is None else _rows(g_res),
+                                       rstd=rstd)
             gw = gw32.to(w.dtype) if ctx.needs_input_grad[2] else None
         gx = g_h if ctx.needs_input_grad[0] else None
         gr = g_h if ctx.needs_input_grad[1] else None
@@ -52,17 +61,18 @@ class FusedAddRMSNormFunction(torch.autograd.Function):
 class RMSNormFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, x, w, eps: float, weight_bias: float):
-        x = x.contiguous()
-        out, _ = rmsnorm_fwd(x, w.contiguous(), eps, weight_bias)
-        ctx.save_for_backward(x, w)
+        x = _rows(x)
+        out, _, rstd = rmsnorm_fwd_ex(x, w.contiguous(), eps, weight_bias, rstd=True)
+        ctx.save_for_backward(x, w, rstd)
         ctx.eps = eps
         ctx.weight_bias = weight_bias
         return out
 
     @staticmethod
     def backward(ctx, g_out):
-        x, w = ctx.saved_tensors
-        gx, gw32 = rmsnorm_vjp(x, w, g_out.contiguous(), ctx.eps, ctx.weight_bias)
+        x, w, rstd = ctx.saved_tensors
+        gx, gw32 = rmsnorm_vjp_ex(x, w.contiguous(), _rows(g_out), ctx.eps, ctx.weight_bias,
+                                  rstd=rstd)
         return (gx if ctx.needs_input_grad[0] else None,
                 gw32.to(w.dtype) if ctx.needs_input_grad[1] else None, None, None)
 

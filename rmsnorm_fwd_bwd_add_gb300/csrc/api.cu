@@ -97,14 +97,17 @@ int scratch_pool(cudaMemPool_t *out) {
     return RMSNORM_OK;
 }
 
-// Scalar and shape checks common to both operations.
+int esize_of(int dtype) { return dtype == RMSNORM_F32 ? 4 : 2; }
+
+// Scalar and shape checks common to every norm entry point.
 int check_common(int64_t rows, int64_t D, int dtype, float eps, float weight_bias) {
-    if (dtype != RMSNORM_F16 && dtype != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
+    if (dtype != RMSNORM_F16 && dtype != RMSNORM_BF16 && dtype != RMSNORM_F32)
+        return RMSNORM_ERR_INVALID_ARG;
     if (rows < 0 || D <= 0) return RMSNORM_ERR_INVALID_ARG;
     if (!(eps >= 0.f) || !std::isfinite(eps)) return RMSNORM_ERR_INVALID_ARG;
     if (!std::isfinite(weight_bias)) return RMSNORM_ERR_INVALID_ARG;
     if (D > RMSNORM_MAX_D) return RMSNORM_ERR_UNSUPPORTED;
-    if (rows > INT64_MAX / (2 * D)) return RMSNORM_ERR_UNSUPPORTED;
+    if (rows > INT64_MAX / (4 * D)) return RMSNORM_ERR_UNSUPPORTED;
     return RMSNORM_OK;
 }
 
@@ -114,13 +117,70 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     return pa < pb + nb && pb < pa + na;
 }
 
-// An output may coincide exactly with a same-sized input, or be disjoint.
-bool bad_alias(const void *out, size_t nout, const void *in, size_t nin) {
-    if (!overlaps(out, nout, in, nin)) return false;
-    return !(out == in && nout == nin);
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// A [rows, D] tensor of `es`-byte elements whose rows start `ld` elements
+// apart (ld >= D).  A single row has no stride; it is normalised to D so
+// that the same row under two strides compares equal.
+struct Mat {
+    const void *p;
+    int64_t ld;
+};
+
+Mat mat(const void *p, int64_t ld, int64_t rows, int64_t D) { return Mat{p, rows <= 1 ? D : ld}; }
+
+// Checks a stride and that the tensor's extent fits in the address space.
+int check_ld(int64_t ld, int64_t rows, int64_t D, int es) {
+    if (ld < D) return RMSNORM_ERR_INVALID_ARG;
+    if (rows > 1 && (rows - 1) > (INT64_MAX / es - D) / ld) return RMSNORM_ERR_UNSUPPORTED;
+    return RMSNORM_OK;
 }
 
-bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+size_t extent(const Mat &m, int64_t rows, int64_t D, int es) {
+    return (!m.p || rows == 0) ? 0 : (size_t)((rows - 1) * m.ld + D) * (size_t)es;
+}
+
+int64_t floor_div(int64_t a, int64_t b) {
+    const int64_t q = a / b;
+    return (a % b != 0 && ((a < 0) != (b < 0))) ? q - 1 : q;
+}
+
+// Whether two [rows, D] tensors share a byte.  With equal strides the test is
+// exact (rows i of a and j of b meet iff |(b - a) - (i - j) * ld| < the row's
+// bytes for some i - j in [-(rows - 1), rows - 1]), so interleaved tensors
+// such as the two halves of a [rows, 2D] buffer count as disjoint; with
+// different strides the whole extents are compared.
+bool mats_overlap(const Mat &a, const Mat &b, int64_t rows, int64_t D, int es) {
+    const size_t na = extent(a, rows, D, es), nb = extent(b, rows, D, es);
+    if (!overlaps(a.p, na, b.p, nb)) return false;
+    if (a.ld != b.ld) return true;
+    const int64_t L = a.ld * es, R = D * es;
+    const int64_t d = (int64_t)((uintptr_t)b.p - (uintptr_t)a.p);
+    const int64_t k0 = floor_div(d, L);
+    for (int64_t k : {k0, k0 + 1}) {
+        k = std::min<int64_t>(std::max<int64_t>(k, -(rows - 1)), rows - 1);
+        const int64_t off = d - k * L;
+        if (off > -R && off < R) return true;
+    }
+    return false;
+}
+
+// An output may be exactly an input (same pointer and stride: every element
+// is read before the thread that owns it writes it), or share no byte with it.
+bool bad_alias(const Mat &out, const Mat &in, int64_t rows, int64_t D, int es) {
+    if (!mats_overlap(out, in, rows, D, es)) return false;
+    return !(out.p == in.p && out.ld == in.ld);
+}
+
+// Whether a [rows, D] tensor overlaps a plain buffer of n bytes.
+bool mat_hits(const Mat &m, int64_t rows, int64_t D, int es, const void *p, size_t n) {
+    return overlaps(m.p, extent(m, rows, D, es), p, n);
+}
+
+// The vectorised tiers need 16-byte aligned rows: base and stride.
+bool rows_aligned(const Mat &m, int es) {
+    return !m.p || (aligned16(m.p) && (m.ld * es) % 16 == 0);
+}
 
 size_t partials_bytes(const Plan &p, int64_t D) {
     const size_t b = (size_t)p.grid * (size_t)D * sizeof(float);
@@ -152,63 +212,93 @@ KernelArgs base_args(const DevInfo &dev, const Plan &p, float eps, float wb, int
     return a;
 }
 
+// The operands of one VJP call: x (the normalised tensor), g (the gradient of
+// out), g_res (the gradient reaching new_residual of the fused op; null for
+// the plain VJP), gx, each with its row stride; w, gw; and the forward's
+// per-row rstd (null: recomputed from x).
+struct VjpOperands {
+    Mat x, g, g_res, gx;
+    const void *w;
+    float *gw;
+    const float *rstd;
+};
+
+VjpOperands dense_vjp(const void *x, const void *w, const void *g, const void *g_res, void *gx,
+                      float *gw, int64_t D) {
+    return VjpOperands{Mat{x, D}, Mat{g, D}, Mat{g_res, D}, Mat{gx, D}, w, gw, nullptr};
+}
+
 // Validation shared by the VJP entry points; *plan is filled on success when
-// rows > 0.  g_res (the gradient reaching new_residual of the fused op) is
-// null for the plain VJP.
-int vjp_prepare(const void *x, const void *w, const void *g, const void *g_res, float eps,
-                float weight_bias, void *gx, float *gw, int64_t rows, int64_t D, int dtype,
-                DevInfo *dev, Plan *plan) {
+// rows > 0.
+int vjp_prepare(const VjpOperands &o, float eps, float weight_bias, int64_t rows, int64_t D,
+                int dtype, DevInfo *dev, Plan *plan) {
     int st = check_common(rows, D, dtype, eps, weight_bias);
     if (st != RMSNORM_OK) return st;
-    if (!w || !gw) return RMSNORM_ERR_INVALID_ARG;
-    const size_t nw = (size_t)D * 2, ngw = (size_t)D * 4;
+    if (!o.w || !o.gw) return RMSNORM_ERR_INVALID_ARG;
+    const int es = esize_of(dtype);
+    const size_t nw = (size_t)D * es, ngw = (size_t)D * 4, nr = (size_t)rows * 4;
     if (rows > 0) {
-        if (!x || !g || !gx) return RMSNORM_ERR_INVALID_ARG;
-        const size_t n = (size_t)rows * (size_t)D * 2;
-        if (overlaps(gx, n, gw, ngw)) return RMSNORM_ERR_INVALID_ARG;
-        if (bad_alias(gx, n, x, n) || bad_alias(gx, n, g, n) || bad_alias(gx, n, g_res, n) ||
-            overlaps(gx, n, w, nw))
+        if (!o.x.p || !o.g.p || !o.gx.p) return RMSNORM_ERR_INVALID_ARG;
+        for (const Mat *m : {&o.x, &o.g, &o.g_res, &o.gx}) {
+            if (!m->p) continue;
+            st = check_ld(m->ld, rows, D, es);
+            if (st != RMSNORM_OK) return st;
+        }
+        const Mat x = mat(o.x.p, o.x.ld, rows, D), g = mat(o.g.p, o.g.ld, rows, D);
+        const Mat gr = mat(o.g_res.p, o.g_res.ld, rows, D), gx = mat(o.gx.p, o.gx.ld, rows, D);
+        if (bad_alias(gx, x, rows, D, es) || bad_alias(gx, g, rows, D, es) ||
+            bad_alias(gx, gr, rows, D, es))
             return RMSNORM_ERR_INVALID_ARG;
-        if (overlaps(gw, ngw, x, n) || overlaps(gw, ngw, g, n) || overlaps(gw, ngw, g_res, n))
+        if (mat_hits(gx, rows, D, es, o.gw, ngw) || mat_hits(gx, rows, D, es, o.w, nw) ||
+            mat_hits(gx, rows, D, es, o.rstd, nr))
             return RMSNORM_ERR_INVALID_ARG;
+        for (const Mat *m : {&x, &g, &gr})
+            if (mat_hits(*m, rows, D, es, o.gw, ngw)) return RMSNORM_ERR_INVALID_ARG;
+        if (overlaps(o.gw, ngw, o.rstd, nr)) return RMSNORM_ERR_INVALID_ARG;
     }
-    if (overlaps(gw, ngw, w, nw)) return RMSNORM_ERR_INVALID_ARG;
+    if (overlaps(o.gw, ngw, o.w, nw)) return RMSNORM_ERR_INVALID_ARG;
     st = current_device(dev);
     if (st != RMSNORM_OK) return st;
     if (rows > 0) {
-        const bool aligned = (D * 2) % 16 == 0 && aligned16(x) && aligned16(g) && aligned16(gx) &&
-                             aligned16(w) && (!g_res || aligned16(g_res));
-        *plan = make_plan(g_res ? MODE_VJP_ADD : MODE_VJP, rows, (int)D, aligned, dev->sm_count);
+        const bool aligned = (D * es) % 16 == 0 && aligned16(o.w) && rows_aligned(o.x, es) &&
+                             rows_aligned(o.g, es) && rows_aligned(o.gx, es) &&
+                             rows_aligned(o.g_res, es);
+        *plan = make_plan(o.g_res.p ? MODE_VJP_ADD : MODE_VJP, rows, (int)D, es, aligned,
+                          dev->sm_count);
     }
     return RMSNORM_OK;
 }
 
-int vjp_run(const void *x, const void *w, const void *g, const void *g_res, float eps,
-            float weight_bias, void *gx, float *gw, int64_t rows, int64_t D, int dtype,
-            const DevInfo &dev, const Plan &p, float *partials, cudaStream_t s) {
+int vjp_run(const VjpOperands &o, float eps, float weight_bias, int64_t rows, int64_t D,
+            int dtype, const DevInfo &dev, const Plan &p, float *partials, cudaStream_t s) {
     KernelArgs a = base_args(dev, p, eps, weight_bias, rows, D);
-    a.in0 = x;
-    a.in1 = g;
-    a.in2 = g_res;
-    a.w = w;
-    a.out0 = gx;
+    a.in0 = o.x.p;
+    a.ld_in0 = o.x.ld;
+    a.in1 = o.g.p;
+    a.ld_in1 = o.g.ld;
+    a.in2 = o.g_res.p;
+    a.ld_in2 = o.g_res.p ? o.g_res.ld : 0;
+    a.w = o.w;
+    a.out0 = const_cast<void *>(o.gx.p);
+    a.ld_out0 = o.gx.ld;
     a.out1 = nullptr;
     a.partials = partials;
-    cudaError_t e = launch_plan(dtype, g_res ? MODE_VJP_ADD : MODE_VJP, p, a, s);
+    a.rstd = const_cast<float *>(o.rstd);  // read only in the VJP kernels
+    cudaError_t e = launch_plan(dtype, o.g_res.p ? MODE_VJP_ADD : MODE_VJP, p, a, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    e = launch_gw_reduce(partials, gw, p.grid, (int)D, s);
+    e = launch_gw_reduce(partials, o.gw, p.grid, (int)D, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return RMSNORM_OK;
 }
 
 // The VJP with scratch from the library's stream-ordered pool.
-int vjp_pooled(const void *x, const void *w, const void *g, const void *g_res, float eps,
-               float weight_bias, void *gx, float *gw, int64_t rows, int64_t D, int dtype,
-               void *stream) {
+int vjp_pooled(const VjpOperands &o, float eps, float weight_bias, int64_t rows, int64_t D,
+               int dtype, void *stream) {
     DevInfo dev;
     Plan p{};
-    int st = vjp_prepare(x, w, g, g_res, eps, weight_bias, gx, gw, rows, D, dtype, &dev, &p);
+    int st = vjp_prepare(o, eps, weight_bias, rows, D, dtype, &dev, &p);
     if (st != RMSNORM_OK) return st;
+    float *gw = o.gw;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (rows == 0) {
         cudaError_t e = cudaMemsetAsync(gw, 0, (size_t)D * sizeof(float), s);
@@ -224,8 +314,7 @@ int vjp_pooled(const void *x, const void *w, const void *g, const void *g_res, f
         return RMSNORM_ERR_NO_MEMORY;
     }
     if (e != cudaSuccess) return cuda_fail(e);
-    st = vjp_run(x, w, g, g_res, eps, weight_bias, gx, gw, rows, D, dtype, dev, p,
-                 static_cast<float *>(ws), s);
+    st = vjp_run(o, eps, weight_bias, rows, D, dtype, dev, p, static_cast<float *>(ws), s);
     e = cudaFreeAsync(ws, s);
     if (st == RMSNORM_OK && e != cudaSuccess) st = cuda_fail(e);
     return st;
@@ -239,39 +328,64 @@ const char *tier_name(int t) {
 
 extern "C" {
 
-int rmsnorm_fwd(const void *x, const void *residual, const void *w, float eps, float weight_bias,
-                void *out, void *new_residual, int64_t rows, int64_t D, int dtype, void *stream) {
+int rmsnorm_fwd_ex(const void *x, int64_t ld_x, const void *residual, int64_t ld_residual,
+                   const void *w, float eps, float weight_bias, void *out, int64_t ld_out,
+                   void *new_residual, int64_t ld_new_residual, float *rstd, int64_t rows,
+                   int64_t D, int dtype, void *stream) {
     int st = check_common(rows, D, dtype, eps, weight_bias);
     if (st != RMSNORM_OK) return st;
     if (!w) return RMSNORM_ERR_INVALID_ARG;
     if (rows == 0) return RMSNORM_OK;
     if (!x || !out) return RMSNORM_ERR_INVALID_ARG;
     if ((residual == nullptr) != (new_residual == nullptr)) return RMSNORM_ERR_INVALID_ARG;
-    const size_t n = (size_t)rows * (size_t)D * 2, nw = (size_t)D * 2;
-    if (overlaps(out, n, new_residual, n)) return RMSNORM_ERR_INVALID_ARG;
-    if (bad_alias(out, n, x, n) || bad_alias(out, n, residual, n) || overlaps(out, n, w, nw))
-        return RMSNORM_ERR_INVALID_ARG;
-    if (bad_alias(new_residual, n, x, n) || bad_alias(new_residual, n, residual, n) ||
-        overlaps(new_residual, n, w, nw))
+    const int es = esize_of(dtype);
+    st = check_ld(ld_x, rows, D, es);
+    if (st == RMSNORM_OK) st = check_ld(ld_out, rows, D, es);
+    if (st == RMSNORM_OK && residual) st = check_ld(ld_residual, rows, D, es);
+    if (st == RMSNORM_OK && residual) st = check_ld(ld_new_residual, rows, D, es);
+    if (st != RMSNORM_OK) return st;
+    const Mat mx = mat(x, ld_x, rows, D), mo = mat(out, ld_out, rows, D);
+    const Mat mr = mat(residual, ld_residual, rows, D);
+    const Mat mn = mat(new_residual, ld_new_residual, rows, D);
+    const size_t nw = (size_t)D * es, nr = (size_t)rows * 4;
+    if (mats_overlap(mo, mn, rows, D, es)) return RMSNORM_ERR_INVALID_ARG;
+    for (const Mat *o : {&mo, &mn}) {
+        if (bad_alias(*o, mx, rows, D, es) || bad_alias(*o, mr, rows, D, es) ||
+            mat_hits(*o, rows, D, es, w, nw) || mat_hits(*o, rows, D, es, rstd, nr))
+            return RMSNORM_ERR_INVALID_ARG;
+    }
+    if (mat_hits(mx, rows, D, es, rstd, nr) || mat_hits(mr, rows, D, es, rstd, nr) ||
+        overlaps(rstd, nr, w, nw))
         return RMSNORM_ERR_INVALID_ARG;
 
     DevInfo dev;
     st = current_device(&dev);
     if (st != RMSNORM_OK) return st;
     const int mode = residual ? MODE_FWD_RES : MODE_FWD_NORES;
-    const bool aligned = (D * 2) % 16 == 0 && aligned16(x) && aligned16(w) && aligned16(out) &&
-                         (!residual || (aligned16(residual) && aligned16(new_residual)));
-    const Plan p = make_plan(mode, rows, (int)D, aligned, dev.sm_count);
+    const bool aligned = (D * es) % 16 == 0 && aligned16(w) && rows_aligned(mx, es) &&
+                         rows_aligned(mo, es) && rows_aligned(mr, es) && rows_aligned(mn, es);
+    const Plan p = make_plan(mode, rows, (int)D, es, aligned, dev.sm_count);
     KernelArgs a = base_args(dev, p, eps, weight_bias, rows, D);
     a.in0 = x;
+    a.ld_in0 = mx.ld;
     a.in1 = residual;
+    a.ld_in1 = residual ? mr.ld : 0;
     a.w = w;
     a.out0 = out;
+    a.ld_out0 = mo.ld;
     a.out1 = new_residual;
+    a.ld_out1 = new_residual ? mn.ld : 0;
     a.partials = nullptr;
+    a.rstd = rstd;
     cudaError_t e = launch_plan(dtype, mode, p, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return RMSNORM_OK;
+}
+
+int rmsnorm_fwd(const void *x, const void *residual, const void *w, float eps, float weight_bias,
+                void *out, void *new_residual, int64_t rows, int64_t D, int dtype, void *stream) {
+    return rmsnorm_fwd_ex(x, D, residual, D, w, eps, weight_bias, out, D, new_residual, D, nullptr,
+                          rows, D, dtype, stream);
 }
 
 size_t rmsnorm_vjp_workspace_size(int64_t rows, int64_t D, int dtype) {
@@ -279,8 +393,9 @@ size_t rmsnorm_vjp_workspace_size(int64_t rows, int64_t D, int dtype) {
     DevInfo dev;
     if (current_device(&dev) != RMSNORM_OK) return 0;
     // The plan depends on pointer alignment; cover both outcomes.
-    const Plan pa = make_plan(MODE_VJP, rows, (int)D, (D * 2) % 16 == 0, dev.sm_count);
-    const Plan pu = make_plan(MODE_VJP, rows, (int)D, false, dev.sm_count);
+    const int es = esize_of(dtype);
+    const Plan pa = make_plan(MODE_VJP, rows, (int)D, es, (D * es) % 16 == 0, dev.sm_count);
+    const Plan pu = make_plan(MODE_VJP, rows, (int)D, es, false, dev.sm_count);
     return std::max(partials_bytes(pa, D), partials_bytes(pu, D));
 }
 
@@ -289,7 +404,8 @@ int rmsnorm_vjp_ws(const void *x, const void *w, const void *g, float eps, float
                    size_t workspace_bytes, void *stream) {
     DevInfo dev;
     Plan p{};
-    int st = vjp_prepare(x, w, g, nullptr, eps, weight_bias, gx, gw, rows, D, dtype, &dev, &p);
+    const VjpOperands o = dense_vjp(x, w, g, nullptr, gx, gw, D);
+    int st = vjp_prepare(o, eps, weight_bias, rows, D, dtype, &dev, &p);
     if (st != RMSNORM_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (rows == 0) {
@@ -299,24 +415,35 @@ int rmsnorm_vjp_ws(const void *x, const void *w, const void *g, float eps, float
     const size_t need = partials_bytes(p, D);
     if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u) != 0)
         return RMSNORM_ERR_INVALID_ARG;
-    const size_t n = (size_t)rows * (size_t)D * 2;
+    const int es = esize_of(dtype);
+    const size_t n = (size_t)rows * (size_t)D * es;
     if (overlaps(workspace, need, x, n) || overlaps(workspace, need, g, n) ||
-        overlaps(workspace, need, gx, n) || overlaps(workspace, need, w, (size_t)D * 2) ||
+        overlaps(workspace, need, gx, n) || overlaps(workspace, need, w, (size_t)D * es) ||
         overlaps(workspace, need, gw, (size_t)D * 4))
         return RMSNORM_ERR_INVALID_ARG;
-    return vjp_run(x, w, g, nullptr, eps, weight_bias, gx, gw, rows, D, dtype, dev, p,
-                   static_cast<float *>(workspace), s);
+    return vjp_run(o, eps, weight_bias, rows, D, dtype, dev, p, static_cast<float *>(workspace), s);
 }
 
 int rmsnorm_vjp(const void *x, const void *w, const void *g, float eps, float weight_bias,
                 void *gx, float *gw, int64_t rows, int64_t D, int dtype, void *stream) {
-    return vjp_pooled(x, w, g, nullptr, eps, weight_bias, gx, gw, rows, D, dtype, stream);
+    return vjp_pooled(dense_vjp(x, w, g, nullptr, gx, gw, D), eps, weight_bias, rows, D, dtype,
+                      stream);
 }
 
 int rmsnorm_fused_vjp(const void *h, const void *w, const void *g_out, const void *g_residual,
                       float eps, float weight_bias, void *g_h, float *gw, int64_t rows, int64_t D,
                       int dtype, void *stream) {
-    return vjp_pooled(h, w, g_out, g_residual, eps, weight_bias, g_h, gw, rows, D, dtype, stream);
+    return vjp_pooled(dense_vjp(h, w, g_out, g_residual, g_h, gw, D), eps, weight_bias, rows, D,
+                      dtype, stream);
+}
+
+int rmsnorm_vjp_ex(const void *x, int64_t ld_x, const void *w, const void *g, int64_t ld_g,
+                   const void *g_residual, int64_t ld_g_residual, const float *rstd, float eps,
+                   float weight_bias, void *gx, int64_t ld_gx, float *gw, int64_t rows, int64_t D,
+                   int dtype, void *stream) {
+    const VjpOperands o{Mat{x, ld_x}, Mat{g, ld_g}, Mat{g_residual, ld_g_residual}, Mat{gx, ld_gx},
+                        w, gw, rstd};
+    return vjp_pooled(o, eps, weight_bias, rows, D, dtype, stream);
 }
 
 const char *rmsnorm_status_string(int status) {
@@ -368,7 +495,8 @@ const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype
     if (current_device(&dev) != RMSNORM_OK) return "no-device";
     const int mode = op == 1 ? (has_residual ? MODE_VJP_ADD : MODE_VJP)
                              : (has_residual ? MODE_FWD_RES : MODE_FWD_NORES);
-    const Plan p = make_plan(mode, rows, (int)D, aligned && (D * 2) % 16 == 0, dev.sm_count);
+    const int es = esize_of(dtype);
+    const Plan p = make_plan(mode, rows, (int)D, es, aligned && (D * es) % 16 == 0, dev.sm_count);
     std::snprintf(buf, sizeof(buf), "%s:cfg%d:nt%d:g%d:v%d:s%d:tr%d:grid%d:smem%zu",
                   tier_name(p.tier), p.cfg, p.nt, p.g, p.v, p.stages, p.tile_rows, p.grid,
                   p.smem);
@@ -387,9 +515,10 @@ size_t vjp_partials_bytes_for(const void *x, const void *w, const void *g, const
     if (check_common(rows, D, dtype, 0.f, 0.f) != RMSNORM_OK || rows == 0) return 0;
     DevInfo dev;
     if (current_device(&dev) != RMSNORM_OK) return 0;
+    const int es = esize_of(dtype);
     const bool aligned =
-        (D * 2) % 16 == 0 && aligned16(x) && aligned16(g) && aligned16(gx) && aligned16(w);
-    return partials_bytes(make_plan(MODE_VJP, rows, (int)D, aligned, dev.sm_count), D);
+        (D * es) % 16 == 0 && aligned16(x) && aligned16(g) && aligned16(gx) && aligned16(w);
+    return partials_bytes(make_plan(MODE_VJP, rows, (int)D, es, aligned, dev.sm_count), D);
 }
 
 // Records a failed CUDA call for rmsnorm_last_cuda_error().

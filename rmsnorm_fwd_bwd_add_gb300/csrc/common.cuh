@@ -1,7 +1,7 @@
 // common.cuh -- device helpers shared by the RMSNorm kernels (sm_103a).
 //
-// 16-byte vectors of eight fp16/bf16 values, fp32 conversion with
-// round-to-nearest-even, warp sums in a fixed order, and inline-PTX wrappers
+// 16-byte vectors of eight fp16/bf16 values (or four fp32), fp32 conversion
+// with round-to-nearest-even, warp sums in a fixed order, and inline-PTX wrappers
 // for mbarriers and the 1-D TMA bulk copy (cp.async.bulk) that stages rows
 // into shared memory.
 #pragma once
@@ -71,6 +71,15 @@ template <> struct Cvt<__nv_bfloat16> {
     }
 };
 
+template <> struct Cvt<float> {
+    static __device__ __forceinline__ float load1(const float *p) { return *p; }
+    static __device__ __forceinline__ void store1(float *p, float v) { *p = v; }
+};
+
+// Elements of T in one 16-byte vector, and the float2 pairs they fill.
+template <typename T> __host__ __device__ constexpr int vec_elems() { return 16 / (int)sizeof(T); }
+template <typename T> __host__ __device__ constexpr int vec_pairs() { return 8 / (int)sizeof(T); }
+
 template <typename T>
 __device__ __forceinline__ void unpack8(const uint4 &v, float f[8]) {
     float2 a = Cvt<T>::unpack2(v.x), b = Cvt<T>::unpack2(v.y);
@@ -107,6 +116,50 @@ __device__ __forceinline__ uint4 pack8(const float2 f[4]) {
     v.z = Cvt<T>::pack2(f[2].x, f[2].y);
     v.w = Cvt<T>::pack2(f[3].x, f[3].y);
     return v;
+}
+
+// One 16-byte vector of T <-> fp32, as float2 pairs (fp16/bf16: four pairs,
+// fp32: two) or as plain floats (eight or four).
+template <typename T>
+__device__ __forceinline__ void unpack_vec(const uint4 &v, float2 (&f)[vec_pairs<T>()]) {
+    if constexpr (sizeof(T) == 4) {
+        f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+    } else {
+        unpack8<T>(v, f);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack_vec(const float2 (&f)[vec_pairs<T>()]) {
+    if constexpr (sizeof(T) == 4) {
+        return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                          __float_as_uint(f[1].y));
+    } else {
+        return pack8<T>(f);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack_vec(const uint4 &v, float (&f)[vec_elems<T>()]) {
+    if constexpr (sizeof(T) == 4) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    } else {
+        unpack8<T>(v, f);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack_vec(const float (&f)[vec_elems<T>()]) {
+    if constexpr (sizeof(T) == 4) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    } else {
+        return pack8<T>(f);
+    }
 }
 
 // Packed fp32x2 arithmetic (one instruction for two lanes of work on sm_100+),

@@ -4,8 +4,8 @@
 // Used for decode-sized problems (a few rows, where a staging ring has
 // nothing to overlap and latency is all that matters: every thread issues its
 // 16-byte loads at once) and for aligned rows too long for the shared-memory
-// ring.  Each thread owns V vectors of 8 elements of the row (fixed across
-// rows); the sum of squares is a warp shuffle tree plus the warp totals added
+// ring.  Each thread owns V 16-byte vectors of the row (eight fp16/bf16 or
+// four fp32 elements each, fixed across rows); the sum of squares is a warp shuffle tree plus the warp totals added
 // in warp order through shared memory.  The VJP keeps its gw contributions in
 // registers and writes one partial row per CTA.
 //
@@ -26,13 +26,14 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
     constexpr int NTENS = input_tensors(MODE);
     constexpr bool VJP = is_vjp(MODE);
     constexpr bool ADD = (MODE == MODE_VJP_ADD);
+    constexpr int E = vec_elems<T>();
     __shared__ float red[2][NWARPS][2];
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int D = a.D;
-    const int NV = D >> 3;
+    const int NV = D / E;
     const float eps = a.eps;
     const float wb = a.weight_bias;
     const float Df = (float)D;
@@ -43,24 +44,27 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
     uint4 *out0 = static_cast<uint4 *>(a.out0);
     uint4 *out1 = static_cast<uint4 *>(a.out1);
 
-    float acc[VJP ? V : 1][8];
+    float acc[VJP ? V : 1][E];
 #pragma unroll
     for (int j = 0; j < (VJP ? V : 1); ++j)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+        for (int e = 0; e < E; ++e) acc[j][e] = 0.f;
+    // Row strides in vectors.
+    const int64_t l0 = a.ld_in0 / E, l1 = a.ld_in1 / E, l2 = a.ld_in2 / E;
+    const int64_t lo0 = a.ld_out0 / E, lo1 = a.ld_out1 / E;
 
     griddep_wait();  // programmatic dependent: no global access before this
     int it = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, ++it) {
-        const size_t base = (size_t)row * NV;
+        const float r_saved = (VJP && a.rstd) ? __ldg(a.rstd + row) : 0.f;
         uint4 v0[V], v1[V], v2[ADD ? V : 1];
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = tid + j * NT;
             if (vi < NV) {
-                v0[j] = ld_stream(in0 + base + vi);
-                if constexpr (NTENS >= 2) v1[j] = ld_stream(in1 + base + vi);
-                if constexpr (ADD) v2[j] = ld_stream(in2 + base + vi);
+                v0[j] = ld_stream(in0 + row * l0 + vi);
+                if constexpr (NTENS >= 2) v1[j] = ld_stream(in1 + row * l1 + vi);
+                if constexpr (ADD) v2[j] = ld_stream(in2 + row * l2 + vi);
             }
         }
         float sa = 0.f, sb = 0.f;
@@ -68,25 +72,25 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
         for (int j = 0; j < V; ++j) {
             const int vi = tid + j * NT;
             if (vi < NV) {
-                float f0[8];
-                unpack8<T>(v0[j], f0);
+                float f0[E];
+                unpack_vec<T>(v0[j], f0);
                 if constexpr (MODE == MODE_FWD_RES) {
-                    float f1[8];
-                    unpack8<T>(v1[j], f1);
+                    float f1[E];
+                    unpack_vec<T>(v1[j], f1);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < E; ++e) {
                         const float h = f0[e] + f1[e];
                         sa += h * h;
                     }
                 } else if constexpr (MODE == MODE_FWD_NORES) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) sa += f0[e] * f0[e];
+                    for (int e = 0; e < E; ++e) sa += f0[e] * f0[e];
                 } else {
-                    float f1[8], wf[8];
-                    unpack8<T>(v1[j], f1);
-                    unpack8<T>(__ldg(wg + vi), wf);
+                    float f1[E], wf[E];
+                    unpack_vec<T>(v1[j], f1);
+                    unpack_vec<T>(__ldg(wg + vi), wf);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < E; ++e) {
                         sa += f0[e] * f0[e];
                         sb += (f1[e] * (wb + wf[e])) * f0[e];
                     }
@@ -106,44 +110,49 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
             ss += red[it & 1][w][0];
             if constexpr (VJP) dot += red[it & 1][w][1];
         }
-        const float r = rsqrtf(ss / Df + eps);
+        float r = rsqrtf(ss / Df + eps);
+        if constexpr (VJP) {
+            if (a.rstd) r = r_saved;
+        } else {
+            if (a.rstd && tid == 0) a.rstd[row] = r;
+        }
         const float c = (r * r) * (dot / Df);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = tid + j * NT;
             if (vi < NV) {
-                float f0[8], wf[8], o[8];
-                unpack8<T>(v0[j], f0);
-                unpack8<T>(__ldg(wg + vi), wf);
+                float f0[E], wf[E], o[E];
+                unpack_vec<T>(v0[j], f0);
+                unpack_vec<T>(__ldg(wg + vi), wf);
                 if constexpr (MODE == MODE_FWD_RES) {
-                    float f1[8];
-                    unpack8<T>(v1[j], f1);
+                    float f1[E];
+                    unpack_vec<T>(v1[j], f1);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < E; ++e) {
                         f0[e] = f0[e] + f1[e];
                         o[e] = (f0[e] * r) * (wb + wf[e]);
                     }
-                    st_global(out1 + base + vi, pack8<T>(f0));
+                    st_global(out1 + row * lo1 + vi, pack_vec<T>(f0));
                 } else if constexpr (MODE == MODE_FWD_NORES) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] = (f0[e] * r) * (wb + wf[e]);
+                    for (int e = 0; e < E; ++e) o[e] = (f0[e] * r) * (wb + wf[e]);
                 } else {
-                    float f1[8];
-                    unpack8<T>(v1[j], f1);
+                    float f1[E];
+                    unpack_vec<T>(v1[j], f1);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < E; ++e) {
                         const float gwp = f1[e] * (wb + wf[e]);
                         o[e] = r * (gwp - f0[e] * c);
                         acc[j][e] += (f1[e] * f0[e]) * r;
                     }
                     if constexpr (ADD) {
-                        float f2[8];
-                        unpack8<T>(v2[j], f2);
+                        float f2[E];
+                        unpack_vec<T>(v2[j], f2);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = o[e] + f2[e];  // + g_new_residual
+                        for (int e = 0; e < E; ++e) o[e] = o[e] + f2[e];  // + g_new_residual
                     }
                 }
-                st_global(out0 + base + vi, pack8<T>(o));
+                st_global(out0 + row * lo0 + vi, pack_vec<T>(o));
             }
         }
     }
@@ -155,9 +164,11 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
         for (int j = 0; j < V; ++j) {
             const int vi = tid + j * NT;
             if (vi < NV) {
-                float4 *dst = reinterpret_cast<float4 *>(prow + (size_t)vi * 8);
-                dst[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
-                dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+                float4 *dst = reinterpret_cast<float4 *>(prow + (size_t)vi * E);
+#pragma unroll
+                for (int u = 0; u < E / 4; ++u)
+                    dst[u] = make_float4(acc[j][4 * u], acc[j][4 * u + 1], acc[j][4 * u + 2],
+                                         acc[j][4 * u + 3]);
             }
         }
     }

@@ -8,10 +8,16 @@ namespace rmsn {
 
 cudaError_t launch_staged_f16(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
 cudaError_t launch_staged_bf16(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
+cudaError_t launch_staged_f32(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
 
 cudaError_t launch_staged(int dtype, int mode, const Plan &p, const KernelArgs &a,
                           cudaStream_t s) {
-    return dtype == 0 ? launch_staged_f16(mode, p, a, s) : launch_staged_bf16(mode, p, a, s);
+    switch (dtype) {
+        case 0: return launch_staged_f16(mode, p, a, s);
+        case 1: return launch_staged_bf16(mode, p, a, s);
+        case 2: return launch_staged_f32(mode, p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 namespace {
@@ -68,12 +74,22 @@ cudaError_t generic_t(int mode, const Plan &p, const KernelArgs &a, cudaStream_t
 
 cudaError_t launch_direct(int dtype, int mode, const Plan &p, const KernelArgs &a,
                           cudaStream_t s) {
-    return dtype == 0 ? direct_t<__half>(mode, p, a, s) : direct_t<__nv_bfloat16>(mode, p, a, s);
+    switch (dtype) {
+        case 0: return direct_t<__half>(mode, p, a, s);
+        case 1: return direct_t<__nv_bfloat16>(mode, p, a, s);
+        case 2: return direct_t<float>(mode, p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_generic(int dtype, int mode, const Plan &p, const KernelArgs &a,
                            cudaStream_t s) {
-    return dtype == 0 ? generic_t<__half>(mode, p, a, s) : generic_t<__nv_bfloat16>(mode, p, a, s);
+    switch (dtype) {
+        case 0: return generic_t<__half>(mode, p, a, s);
+        case 1: return generic_t<__nv_bfloat16>(mode, p, a, s);
+        case 2: return generic_t<float>(mode, p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_gw_reduce(const float *partials, float *gw, int P, int D, cudaStream_t s) {

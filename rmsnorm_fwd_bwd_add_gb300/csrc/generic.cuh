@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a)
     T *out0 = static_cast<T *>(a.out0);
     T *out1 = static_cast<T *>(a.out1);
     float *prow = VJP ? a.partials + (size_t)blockIdx.x * D : nullptr;
+    const int64_t l0 = a.ld_in0, l1 = a.ld_in1, l2 = a.ld_in2, lo0 = a.ld_out0, lo1 = a.ld_out1;
 
     griddep_wait();  // programmatic dependent: no global access before this
     if constexpr (VJP)
@@ -47,17 +48,18 @@ __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a)
 
     int it = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, ++it) {
-        const size_t base = (size_t)row * D;
+        const T *x_row = in0 + row * l0;
+        const T *y_row = in1 + row * l1;  // residual or g
         float sa = 0.f, sb = 0.f;
         for (int c = tid; c < D; c += NT) {
-            const float x = Cvt<T>::load1(in0 + base + c);
+            const float x = Cvt<T>::load1(x_row + c);
             if constexpr (MODE == MODE_FWD_RES) {
-                const float h = x + Cvt<T>::load1(in1 + base + c);
+                const float h = x + Cvt<T>::load1(y_row + c);
                 sa += h * h;
             } else if constexpr (MODE == MODE_FWD_NORES) {
                 sa += x * x;
             } else {
-                const float g = Cvt<T>::load1(in1 + base + c);
+                const float g = Cvt<T>::load1(y_row + c);
                 sa += x * x;
                 sb += (g * (wb + Cvt<T>::load1(w + c))) * x;
             }
@@ -75,22 +77,28 @@ __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a)
             ss += red[it & 1][k][0];
             if constexpr (VJP) dot += red[it & 1][k][1];
         }
-        const float r = rsqrtf(ss / Df + eps);
+        float r = rsqrtf(ss / Df + eps);
+        if constexpr (VJP) {
+            if (a.rstd) r = a.rstd[row];
+        } else {
+            if (a.rstd && tid == 0) a.rstd[row] = r;
+        }
         const float cc = (r * r) * (dot / Df);
+        T *o_row = out0 + row * lo0;
         for (int c = tid; c < D; c += NT) {
-            const float x = Cvt<T>::load1(in0 + base + c);
+            const float x = Cvt<T>::load1(x_row + c);
             const float wp = wb + Cvt<T>::load1(w + c);
             if constexpr (MODE == MODE_FWD_RES) {
-                const float h = x + Cvt<T>::load1(in1 + base + c);
-                Cvt<T>::store1(out1 + base + c, h);
-                Cvt<T>::store1(out0 + base + c, (h * r) * wp);
+                const float h = x + Cvt<T>::load1(y_row + c);
+                Cvt<T>::store1(out1 + row * lo1 + c, h);
+                Cvt<T>::store1(o_row + c, (h * r) * wp);
             } else if constexpr (MODE == MODE_FWD_NORES) {
-                Cvt<T>::store1(out0 + base + c, (x * r) * wp);
+                Cvt<T>::store1(o_row + c, (x * r) * wp);
             } else {
-                const float g = Cvt<T>::load1(in1 + base + c);
+                const float g = Cvt<T>::load1(y_row + c);
                 float o = r * (g * wp - x * cc);
-                if constexpr (ADD) o = o + Cvt<T>::load1(in2 + base + c);  // + g_new_residual
-                Cvt<T>::store1(out0 + base + c, o);
+                if constexpr (ADD) o = o + Cvt<T>::load1(in2 + row * l2 + c);  // + g_new_residual
+                Cvt<T>::store1(o_row + c, o);
                 prow[c] += (g * x) * r;
             }
         }

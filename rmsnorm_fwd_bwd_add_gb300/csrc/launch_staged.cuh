@@ -6,14 +6,27 @@
 
 namespace rmsn {
 
-template <typename T, int MODE, int NT, int G, int V>
-cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
+template <typename T, int MODE, int NT, int G, int V, bool GEN>
+cudaError_t launch_staged_inst(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
     constexpr int MINB = staged_max_ctas_per_sm(MODE, NT, G, V);
     static std::atomic<uint64_t> smem_mask{0};
-    auto kern = staged_kernel<T, MODE, NT, G, V, MINB>;
+    auto kern = staged_kernel<T, MODE, NT, G, V, MINB, GEN>;
     cudaError_t e = allow_max_dynamic_smem((const void *)kern, smem_mask);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.grid), dim3(NT), p.smem, stream, a);
+}
+
+// The dense instance unless a tensor the mode uses has rows a stride apart
+// or rstd is given.
+template <typename T, int MODE, int NT, int G, int V>
+cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
+    const int64_t D = a.D;
+    bool gen = a.rstd != nullptr || a.ld_in0 != D || a.ld_out0 != D;
+    if constexpr (input_tensors(MODE) >= 2) gen = gen || a.ld_in1 != D;
+    if constexpr (input_tensors(MODE) == 3) gen = gen || a.ld_in2 != D;
+    if constexpr (MODE == MODE_FWD_RES) gen = gen || a.ld_out1 != D;
+    return gen ? launch_staged_inst<T, MODE, NT, G, V, true>(p, a, stream)
+               : launch_staged_inst<T, MODE, NT, G, V, false>(p, a, stream);
 }
 
 template <typename T, int MODE>

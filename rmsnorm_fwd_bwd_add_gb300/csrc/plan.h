@@ -33,6 +33,11 @@ struct KernelArgs {
     uint32_t stage_bytes;     // bytes of one full tile of one tensor
     long long wait_budget;    // SM cycles per bounded wait
     int64_t drop_tile;        // test hook: tile whose copy is never issued (-1: none)
+    // Row strides in elements (D for dense rows).
+    int64_t ld_in0, ld_in1, ld_in2, ld_out0, ld_out1;
+    // Per-row 1/sqrt(ms + eps), fp32 [rows] or null: written by the forward,
+    // read (instead of summing h^2) by the VJP.
+    float *rstd;
 };
 
 struct Plan {
@@ -40,7 +45,7 @@ struct Plan {
     int cfg;           // index into the tier's configuration table
     int nt;            // threads per CTA
     int g;             // threads per row
-    int v;             // 16-byte vectors per thread per row
+    int v;             // 16-byte vectors per thread per row (8 fp16/bf16 or 4 fp32 elements)
     int stages;
     int tile_rows;
     int64_t num_tiles;
@@ -90,7 +95,8 @@ constexpr int GENERIC_NT = 256;
 constexpr int STAGED_HEADER_BYTES = 640;  // 16 mbarriers (128 B) + reduction scratch (512 B)
 constexpr int MAX_STAGES = 8;
 
-// Launchers (one translation unit per tier / dtype).  dtype: 0 fp16, 1 bf16.
+// Launchers (one translation unit per tier / dtype).  dtype: 0 fp16, 1 bf16,
+// 2 fp32.
 cudaError_t launch_staged(int dtype, int mode, const Plan &plan, const KernelArgs &a,
                           cudaStream_t stream);
 cudaError_t launch_direct(int dtype, int mode, const Plan &plan, const KernelArgs &a,

@@ -1,8 +1,12 @@
 // planner.h -- the dispatch table: which kernel, launch shape and ring depth
-// a problem gets.  A pure function of (mode, rows, D, alignment, SM count)
-// plus the RMSNORM_TUNE override, so the VJP's summation order, and with it
-// gw's bits, is fixed for a given device.
-//   * unaligned pointers or D*2 not a multiple of 16 -> generic tier;
+// a problem gets.  A pure function of (mode, rows, D, element size,
+// alignment, SM count) plus the RMSNORM_TUNE override, so the VJP's summation
+// order, and with it gw's bits, is fixed for a given device.  The tiers work
+// in 16-byte vectors, so the thresholds below are in vectors (nv = D * esize
+// / 16) and bytes; the D figures quoted are for 2-byte elements (fp32 rows
+// reach each threshold at half the D).
+//   * unaligned pointers or row strides, or D * esize not a multiple of 16
+//     -> generic tier;
 //   * rows <= DECODE_ROWS (decode: one token per sequence)  -> direct tier;
 //   * D <= 16384 -> staged tier (TMA bulk ring): sub-warp/warp per row for
 //     D <= 1024, CTA per row above;
@@ -80,11 +84,11 @@ inline int ring_stages(int mode, size_t per_stage, int cps) {
     return std::min(MAX_STAGES, 1 + ahead);
 }
 
-inline bool plan_staged(int mode, int64_t rows, int D, int sm_count, int ci, Plan *p) {
+inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, int ci, Plan *p) {
     const StagedCfg &c = STAGED_CFGS[ci];
     const Tuning &tu = tuning();
     const int ntens = input_tensors(mode);
-    const size_t row_bytes = (size_t)D * 2;
+    const size_t row_bytes = (size_t)D * esize;
     const int max_stages = tu.stages ? tu.stages : MAX_STAGES;
     const int cps_max = staged_max_ctas_per_sm(mode, c.nt, c.g, c.v);
     int cps = tu.cps ? std::min(tu.cps, cps_max) : staged_ctas_per_sm(mode, c.nt, c.g, c.v);
@@ -143,18 +147,18 @@ inline bool plan_staged(int mode, int64_t rows, int D, int sm_count, int ci, Pla
     return true;
 }
 
-inline Plan make_plan(int mode, int64_t rows, int D, bool aligned, int sm_count) {
+inline Plan make_plan(int mode, int64_t rows, int D, int esize, bool aligned, int sm_count) {
     Plan p{};
-    const int nv = D / 8;
+    const int nv = (int)((int64_t)D * esize / 16);
     if (aligned && rows > DECODE_ROWS) {
         const int forced = tuning().cfg;
         if (forced >= 0 && nv <= STAGED_CFGS[forced].max_nv &&
             !(is_vjp(mode) && forced == STAGED_CFG_WIDE) &&
-            plan_staged(mode, rows, D, sm_count, forced, &p))
+            plan_staged(mode, rows, D, esize, sm_count, forced, &p))
             return p;
         for (int ci = 0; ci < STAGED_CFG_WIDE; ++ci) {
             if (nv <= STAGED_CFGS[ci].max_nv) {
-                if (plan_staged(mode, rows, D, sm_count, ci, &p)) return p;
+                if (plan_staged(mode, rows, D, esize, sm_count, ci, &p)) return p;
                 break;
             }
         }

@@ -1,13 +1,21 @@
 // staged.cuh -- persistent RMSNorm kernels that stage rows through a shared
 // memory ring with the 1-D TMA bulk copy (cp.async.bulk + mbarrier).
 //
-// Work unit: a tile of `tile_rows` consecutive rows.  Rows are contiguous, so
-// one tile of one tensor is ONE bulk copy.  CTA b owns tiles b, b + grid,
-// b + 2*grid, ... (a static assignment, so the VJP's gw partials are summed in
-// the same order on every run).  Thread 0 keeps `stages` tiles in flight;
-// every thread waits on the tile's mbarrier, converts its vectors of the row
-// from shared memory into fp32 registers once, and writes its outputs straight
-// to global memory.
+// Work unit: a tile of `tile_rows` consecutive rows.  Dense rows make one
+// tile of one tensor ONE bulk copy.  CTA b owns tiles b, b + grid, b + 2*grid,
+// ... (a static assignment, so the VJP's gw partials are summed in the same
+// order on every run).  Thread 0 keeps `stages` tiles in flight; every thread
+// waits on the tile's mbarrier, converts its vectors of the row from shared
+// memory into fp32 registers once, and writes its outputs straight to global
+// memory.  A 16-byte vector holds eight fp16/bf16 or four fp32 elements.
+//
+// GEN = true is the general instance: rows a stride apart (a tensor whose
+// tile is not contiguous is copied one row per lane of warp 0, which then
+// shares the producer's work; the tile is dense in shared memory either way)
+// and the per-row scale rstd (written by the forward, read by the VJP in place
+// of its own sum of squares).  GEN = false is the dense instance without
+// rstd; the launcher picks it whenever it applies, so the common case carries
+// none of the general case's address arithmetic or registers.
 //
 // Two shapes of work inside a tile:
 //   * G == NT ("CTA per row", D > 1024): one row per tile; each thread owns
@@ -36,10 +44,12 @@
 
 namespace rmsn {
 
-template <typename T, int MODE, int NT, int G, int V, int MINB>
+template <typename T, int MODE, int NT, int G, int V, int MINB, bool GEN>
 __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     constexpr int NWARPS = NT / 32;
     constexpr int NG = NT / G;  // rows processed side by side
+    constexpr int VP = vec_pairs<T>();   // float2 pairs per 16-byte vector
+    constexpr int EPV = vec_elems<T>();  // elements per 16-byte vector
     constexpr bool CTA_ROW = (G == NT);
     constexpr int NTENS = input_tensors(MODE);
     constexpr bool VJP = is_vjp(MODE);
@@ -58,7 +68,8 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     const int gid = tid / G;
     const int gl = tid % G;
     const int D = a.D;
-    const int NV = D >> 3;
+    const int NV = D / EPV;
+    const uint32_t row_bytes = (uint32_t)D * (uint32_t)sizeof(T);
     const int S = a.stages;
     const int TR = a.tile_rows;
     const int64_t rows = a.rows;
@@ -73,28 +84,46 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     const T *in2 = static_cast<const T *>(a.in2);
     uint4 *out0 = static_cast<uint4 *>(a.out0);
     uint4 *out1 = static_cast<uint4 *>(a.out1);
+    // Output row strides in vectors.
+    const int64_t lo0 = GEN ? a.ld_out0 / EPV : NV, lo1 = GEN ? a.ld_out1 / EPV : NV;
 
     auto stage_ptr = [&](int s, int tensor) -> unsigned char * {
         return ring + ((size_t)s * NTENS + tensor) * SB;
     };
 
-    // ---- producer (thread 0 only) ----
+    // ---- producer: thread 0 (GEN: every lane of warp 0; lane 0 alone for
+    // contiguous tiles) ----
     int64_t issued = 0;  // tiles of this CTA issued so far
     int issue_stage = 0;
     const uint64_t policy = l2_evict_first_policy();
+    auto copy_rows = [&](unsigned char *dst, const T *src, int64_t ld, int64_t row0, int nr,
+                         uint64_t *bar) {
+        if constexpr (!GEN) {
+            bulk_g2s(dst, src + row0 * D, (uint32_t)nr * row_bytes, bar, policy);
+        } else if (ld == D || nr == 1) {
+            if (lane == 0) bulk_g2s(dst, src + row0 * ld, (uint32_t)nr * row_bytes, bar, policy);
+        } else {
+            for (int q = lane; q < nr; q += 32)
+                bulk_g2s(dst + (size_t)q * row_bytes, src + (row0 + q) * ld, row_bytes, bar, policy);
+        }
+    };
     auto issue_next = [&]() {
         const int64_t t = (int64_t)blockIdx.x + issued * grid;
         if (t != a.drop_tile) {
             const int64_t row0 = t * TR;
-            const int64_t nr = min((int64_t)TR, rows - row0);
-            const uint32_t bytes = (uint32_t)(nr * D * (int64_t)sizeof(T));
+            const int nr = (int)min((int64_t)TR, rows - row0);
             uint64_t *bar = &full[issue_stage];
-            mbar_arrive_expect_tx(bar, bytes * NTENS);
-            bulk_g2s(stage_ptr(issue_stage, 0), in0 + row0 * D, bytes, bar, policy);
+            if constexpr (GEN) {
+                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nr * row_bytes * NTENS);
+                __syncwarp();  // the expected bytes are posted before any copy
+            } else {
+                mbar_arrive_expect_tx(bar, (uint32_t)nr * row_bytes * NTENS);
+            }
+            copy_rows(stage_ptr(issue_stage, 0), in0, a.ld_in0, row0, nr, bar);
             if constexpr (NTENS >= 2)
-                bulk_g2s(stage_ptr(issue_stage, 1), in1 + row0 * D, bytes, bar, policy);
+                copy_rows(stage_ptr(issue_stage, 1), in1, a.ld_in1, row0, nr, bar);
             if constexpr (NTENS == 3)
-                bulk_g2s(stage_ptr(issue_stage, 2), in2 + row0 * D, bytes, bar, policy);
+                copy_rows(stage_ptr(issue_stage, 2), in2, a.ld_in2, row0, nr, bar);
         }
         ++issued;
         issue_stage = issue_stage + 1 == S ? 0 : issue_stage + 1;
@@ -119,52 +148,53 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     // Launched as a programmatic dependent: nothing in global memory may be
     // touched before the previous kernel on the stream has completed.
     griddep_wait();
-    if (tid == 0) {
+    const bool producer = GEN ? warp == 0 : tid == 0;
+    if (producer) {
         const int64_t n0 = min((int64_t)S, nk);
         while (issued < n0) issue_next();
     }
 
     // w' = weight_bias + w for the columns this thread owns, in fp32.
-    float2 wp[V][4];
+    float2 wp[V][VP];
     {
         const float2 wb2 = make_float2(a.weight_bias, a.weight_bias);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = gl + j * G;
             const uint4 wv = vi < NV ? reinterpret_cast<const uint4 *>(a.w)[vi] : make_uint4(0, 0, 0, 0);
-            float2 wf[4];
-            unpack8<T>(wv, wf);
+            float2 wf[VP];
+            unpack_vec<T>(wv, wf);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) wp[j][q] = f2add(wb2, wf[q]);
+            for (int q = 0; q < VP; ++q) wp[j][q] = f2add(wb2, wf[q]);
         }
     }
-    float2 acc[VJP ? V : 1][4];
+    float2 acc[VJP ? V : 1][VP];
 #pragma unroll
     for (int j = 0; j < (VJP ? V : 1); ++j)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[j][q] = make_float2(0.f, 0.f);
+        for (int q = 0; q < VP; ++q) acc[j][q] = make_float2(0.f, 0.f);
 
     // One row: load this thread's vectors from the stage into fp32 (h = x +
     // residual, or x; the VJP also g), and its partial sum(h^2) and, for the
     // VJP, partial dot = sum(g * w' * x).
-    auto load_row = [&](const uint4 *r0, const uint4 *r1, float2 (&xa)[V][4],
-                        float2 (&xb)[V][4], float &sa, float &sb) {
+    auto load_row = [&](const uint4 *r0, const uint4 *r1, float2 (&xa)[V][VP],
+                        float2 (&xb)[V][VP], float &sa, float &sb) {
         float2 s2 = make_float2(0.f, 0.f), d2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = gl + j * G;
             if (vi < NV) {
-                unpack8<T>(r0[vi], xa[j]);
-                if constexpr (NTENS >= 2) unpack8<T>(r1[vi], xb[j]);
+                unpack_vec<T>(r0[vi], xa[j]);
+                if constexpr (NTENS >= 2) unpack_vec<T>(r1[vi], xb[j]);
                 if constexpr (MODE == MODE_FWD_RES) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) xa[j][q] = f2add(xa[j][q], xb[j][q]);  // h
+                    for (int q = 0; q < VP; ++q) xa[j][q] = f2add(xa[j][q], xb[j][q]);  // h
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) s2 = f2fma(xa[j][q], xa[j][q], s2);
+                for (int q = 0; q < VP; ++q) s2 = f2fma(xa[j][q], xa[j][q], s2);
                 if constexpr (VJP) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) d2 = f2fma(f2mul(xb[j][q], wp[j][q]), xa[j][q], d2);
+                    for (int q = 0; q < VP; ++q) d2 = f2fma(f2mul(xb[j][q], wp[j][q]), xa[j][q], d2);
                 }
             }
         }
@@ -174,9 +204,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
 
     // Outputs of one row from the registers load_row filled (the fused-op VJP
     // also reads its row of the new_residual gradient, r2, from the stage).
-    auto row_outputs = [&](const float2 (&xa)[V][4], const float2 (&xb)[V][4], const uint4 *r2,
+    auto row_outputs = [&](const float2 (&xa)[V][VP], const float2 (&xb)[V][VP], const uint4 *r2,
                            int64_t row, float r, float dot) {
-        const size_t base = (size_t)row * NV;
+        const size_t base0 = (size_t)(row * lo0), base1 = (size_t)(row * lo1);
         const float2 rr = make_float2(r, r);
         const float c = (r * r) * (dot / Df);  // r^2 * dot / D
         const float2 nc2 = make_float2(-c, -c);
@@ -184,26 +214,26 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
         for (int j = 0; j < V; ++j) {
             const int vi = gl + j * G;
             if (vi < NV) {
-                float2 o[4];
+                float2 o[VP];
                 if constexpr (VJP) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < VP; ++q) {
                         const float2 u = f2mul(xb[j][q], wp[j][q]);           // g w'
                         o[q] = f2mul(f2fma(xa[j][q], nc2, u), rr);             // r (g w' - x c)
                         acc[j][q] = f2fma(xb[j][q], f2mul(xa[j][q], rr), acc[j][q]);  // g x r
                     }
                     if constexpr (ADD) {
-                        float2 gr[4];
-                        unpack8<T>(r2[vi], gr);
+                        float2 gr[VP];
+                        unpack_vec<T>(r2[vi], gr);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) o[q] = f2add(o[q], gr[q]);  // + g_new_residual
+                        for (int q = 0; q < VP; ++q) o[q] = f2add(o[q], gr[q]);  // + g_new_residual
                     }
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) o[q] = f2mul(f2mul(xa[j][q], rr), wp[j][q]);
-                    if constexpr (MODE == MODE_FWD_RES) st_global(out1 + base + vi, pack8<T>(xa[j]));
+                    for (int q = 0; q < VP; ++q) o[q] = f2mul(f2mul(xa[j][q], rr), wp[j][q]);
+                    if constexpr (MODE == MODE_FWD_RES) st_global(out1 + base1 + vi, pack_vec<T>(xa[j]));
                 }
-                st_global(out0 + base + vi, pack8<T>(o));
+                st_global(out0 + base0 + vi, pack_vec<T>(o));
             }
         }
     };
@@ -213,8 +243,10 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     if constexpr (CTA_ROW) {
         for (int64_t k = 0; k < nk; ++k) {
             const int64_t row = (int64_t)blockIdx.x + k * grid;  // tile_rows == 1
+            // The VJP may be handed the forward's scale; fetch it early.
+            const float r_saved = (GEN && VJP && a.rstd) ? __ldg(a.rstd + row) : 0.f;
             const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_budget);
-            float2 xa[V][4], xb[V][4];
+            float2 xa[V][VP], xb[V][VP];
             float sa, sb;
             load_row(reinterpret_cast<const uint4 *>(stage_ptr(s, 0)),
                      reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS >= 2 ? 1 : 0)), xa, xb, sa,
@@ -229,11 +261,16 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
                 fail(k);
                 return;
             }
-            if (tid == 0 && k >= 1 && issued < nk) issue_next();
+            if (producer && k >= 1 && issued < nk) issue_next();
             float2 tot = lane < NWARPS ? rb[lane] : make_float2(0.f, 0.f);
             tot.x = group_sum<32>(tot.x);
             if constexpr (VJP) tot.y = group_sum<32>(tot.y);
-            const float r = rsqrtf(tot.x / Df + eps);
+            float r = rsqrtf(tot.x / Df + eps);
+            if constexpr (GEN && VJP) {
+                if (a.rstd) r = r_saved;
+            } else if constexpr (GEN) {
+                if (a.rstd && tid == 0) a.rstd[row] = r;
+            }
             row_outputs(xa, xb, reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS - 1)), row, r,
                         tot.y);
             if (++s == S) {
@@ -252,19 +289,26 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
             for (int qb = 0; qb < TR; qb += NG) {  // same trip count in every lane
                 const int q = qb + gid;
                 const bool valid = q < nr;
-                float2 xa[V][4], xb[V][4];
+                float2 xa[V][VP], xb[V][VP];
                 float sa = 0.f, sb = 0.f;
                 if (valid) load_row(t0 + (size_t)q * NV, t1 + (size_t)q * NV, xa, xb, sa, sb);
                 sa = group_sum<G>(sa);
                 if constexpr (VJP) sb = group_sum<G>(sb);
-                if (valid && ok)
-                    row_outputs(xa, xb, t2 + (size_t)q * NV, row0 + q, rsqrtf(sa / Df + eps), sb);
+                if (valid && ok) {
+                    float r = rsqrtf(sa / Df + eps);
+                    if constexpr (GEN && VJP) {
+                        if (a.rstd) r = __ldg(a.rstd + row0 + q);
+                    } else if constexpr (GEN) {
+                        if (a.rstd && gl == 0) a.rstd[row0 + q] = r;
+                    }
+                    row_outputs(xa, xb, t2 + (size_t)q * NV, row0 + q, r, sb);
+                }
             }
             if (__syncthreads_or(!ok)) {  // the whole tile is consumed
                 fail(k);
                 return;
             }
-            if (tid == 0 && issued < nk) issue_next();
+            if (producer && issued < nk) issue_next();
             if (++s == S) {
                 s = 0;
                 ph ^= 1u;
@@ -277,16 +321,19 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     griddep_launch_dependents();
     if constexpr (VJP) {
         float *prow = a.partials + (size_t)blockIdx.x * D;
+        // EPV consecutive fp32 columns of one vector's accumulators.
+        auto store_acc = [&](float *dst, int j) {
+#pragma unroll
+            for (int u = 0; u < VP / 2; ++u)
+                reinterpret_cast<float4 *>(dst)[u] =
+                    make_float4(acc[j][2 * u].x, acc[j][2 * u].y, acc[j][2 * u + 1].x, acc[j][2 * u + 1].y);
+        };
         if constexpr (CTA_ROW) {
             // Each column is owned by exactly one thread of the CTA.
 #pragma unroll
             for (int j = 0; j < V; ++j) {
                 const int vi = gl + j * G;
-                if (vi < NV) {
-                    float4 *dst = reinterpret_cast<float4 *>(prow + (size_t)vi * 8);
-                    dst[0] = make_float4(acc[j][0].x, acc[j][0].y, acc[j][1].x, acc[j][1].y);
-                    dst[1] = make_float4(acc[j][2].x, acc[j][2].y, acc[j][3].x, acc[j][3].y);
-                }
+                if (vi < NV) store_acc(prow + (size_t)vi * EPV, j);
             }
         } else {
             // NG groups own the same columns: add their registers in group
@@ -296,11 +343,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
 #pragma unroll
             for (int j = 0; j < V; ++j) {
                 const int vi = gl + j * G;
-                if (vi < NV) {
-                    float4 *dst = reinterpret_cast<float4 *>(buf + (size_t)gid * D + (size_t)vi * 8);
-                    dst[0] = make_float4(acc[j][0].x, acc[j][0].y, acc[j][1].x, acc[j][1].y);
-                    dst[1] = make_float4(acc[j][2].x, acc[j][2].y, acc[j][3].x, acc[j][3].y);
-                }
+                if (vi < NV) store_acc(buf + (size_t)gid * D + (size_t)vi * EPV, j);
             }
             __syncthreads();
             for (int col = tid; col < D; col += NT) {

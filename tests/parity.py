@@ -2,7 +2,10 @@
 
 Tolerances (normwise relative error ||gpu - oracle||_2 / ||oracle||_2, over a
 whole tensor and, for [rows, D] tensors, the worst single row):
-  bf16 outputs 4e-3, fp16 outputs 1e-3, fp32 gw 1e-5.
+  bf16 outputs 4e-3, fp16 outputs 1e-3, fp32 gw 1e-5, and 1e-5 for fp32
+  outputs and rstd too: an fp32 result carries the sum of squares' error
+  (at most about (terms per thread + tree depth) * 2^-24, ~2e-6 at D = 16384)
+  plus a few roundings of the products, far below 1e-5.
 bf16 keeps 8 significant bits (unit roundoff 2^-8 = 3.9e-3) and fp16 11
 (2^-11 = 4.9e-4); one correct rounding of an fp32 result that is itself within
 a few fp32 ulps of the exact value stays inside these bounds, a second
@@ -55,7 +58,8 @@ def assert_close(name: str, got: torch.Tensor, want: np.ndarray, dtype=None) -> 
 U32 = 2.0 ** -24
 # Half the spacing of the smallest subnormals: the absolute rounding error of
 # an output that underflows.
-HALF_SUBNORMAL = {torch.float16: 2.0 ** -25, torch.bfloat16: 2.0 ** -134}
+HALF_SUBNORMAL = {torch.float16: 2.0 ** -25, torch.bfloat16: 2.0 ** -134,
+                  torch.float32: 2.0 ** -150}
 
 
 def gx_term_magnitude(x, w, g, eps, wb):
