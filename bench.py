@@ -545,9 +545,36 @@ def run_single_op(args):
     if args.op == "rope":
         return run_rope(args, rn, dev)
     c = W.config4_on_device(args.D, dev, args.rows)
-    x, res, w, g = c.x, c.residual, c.w, c.g
-    out, nr, gx = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
+    dtype = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[args.dtype]
+    es = torch.empty(0, dtype=dtype).element_size()
+    x, res, w, g = (t.to(dtype) for t in (c.x, c.residual, c.w, c.g))
+    if args.layout == "strided":
+        # x and residual (and g and g_residual, out and new_residual) as the
+        # two halves of [rows, 2D] buffers: row stride 2D
+        xr = torch.cat([x, res], dim=1)
+        x, res = xr[:, :args.D], xr[:, args.D:]
+        gr = torch.cat([g, res], dim=1)
+        g, g_res = gr[:, :args.D], gr[:, args.D:]
+        ob = torch.empty_like(xr)
+        out, nr = ob[:, :args.D], ob[:, args.D:]
+        gx = torch.empty_like(xr)[:, :args.D]
+    elif args.layout == "padded":
+        # every tensor in its own buffer with rows of D + 64 elements
+        def padded(t):
+            buf = torch.empty(args.rows, args.D + 64, dtype=dtype, device=dev)
+            buf[:, :args.D] = t
+            return buf[:, :args.D]
+        x, res, g = padded(x), padded(res), padded(g)
+        g_res = res
+        out, nr, gx = padded(x), padded(x), padded(x)
+    else:
+        g_res = res
+        out, nr, gx = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
     gw = torch.empty(args.D, dtype=torch.float32, device=dev)
+    rstd = torch.empty(args.rows, dtype=torch.float32, device=dev) if args.rstd else None
+    if args.rstd and args.op == "vjp":
+        rn.rmsnorm_fwd_ex(x, w, c.eps, 0.0, rstd=rstd)  # a valid saved scale to read
+    general = args.rstd or args.layout != "dense" or args.dtype == "f32"
 
     if args.op == "gate":  # x = [a | b] of width 2D from the same draws
         xg = torch.cat([x, res], dim=1)
@@ -556,12 +583,18 @@ def run_single_op(args):
     def once():
         if args.op == "gate":
             rn.rmsnorm_gated_silu(xg, out=og)
+        elif args.op == "fwd" and general:
+            rn.rmsnorm_fwd_ex(x, w, c.eps, 0.0, res, out=out, new_residual=nr, rstd=rstd)
         elif args.op == "fwd":
             rn.rmsnorm_fwd(x, w, c.eps, 0.0, res, out=out, new_residual=nr)
+        elif args.op == "vjp" and general:
+            rn.rmsnorm_vjp_ex(x, w, g, c.eps, 0.0, rstd=rstd, gx=gx, gw=gw)
         elif args.op == "vjp":
             rn.rmsnorm_vjp(x, w, g, c.eps, 0.0, gx=gx, gw=gw)
+        elif general:
+            rn.rmsnorm_vjp_ex(x, w, g, c.eps, 0.0, g_res, rstd=rstd, gx=gx, gw=gw)
         else:
-            rn.rmsnorm_fused_vjp(x, w, g, c.eps, 0.0, res, g_h=gx, gw=gw)
+            rn.rmsnorm_fused_vjp(x, w, g, c.eps, 0.0, g_res, g_h=gx, gw=gw)
     for _ in range(args.warmup):
         once()
     torch.cuda.synchronize()
@@ -573,12 +606,15 @@ def run_single_op(args):
     torch.cuda.synchronize()
     us = 1e3 * a.elapsed_time(b) / args.reps
     nbytes = {"fwd": fwd_bytes, "vjp": vjp_bytes, "fvjp": fused_vjp_bytes,
-              "gate": gate_bytes}[args.op](args.rows, args.D)
+              "gate": gate_bytes}[args.op](args.rows, args.D, s=es)
+    if args.rstd and args.op != "gate":
+        nbytes += 4 * args.rows  # written by the forward, read by the VJP
     plan = ("gate" if args.op == "gate" else
             rn.rmsnorm_describe_dispatch("fwd" if args.op == "fwd" else "vjp", args.rows, args.D,
-                                         torch.bfloat16, args.op != "vjp"))
-    print("op=%s rows=%d D=%d plan=%s us=%.2f GB/s=%.1f" % (args.op, args.rows, args.D, plan, us,
-                                                          nbytes / us / 1e3), flush=True)
+                                         dtype, args.op != "vjp"))
+    print("op=%s dtype=%s layout=%s rstd=%d rows=%d D=%d plan=%s us=%.2f GB/s=%.1f" % (
+        args.op, args.dtype, args.layout, int(args.rstd), args.rows, args.D, plan, us,
+        nbytes / us / 1e3), flush=True)
     return 0
 
 
@@ -680,6 +716,13 @@ def main(argv=None):
     ap.add_argument("--rows", type=int, default=8192)
     ap.add_argument("--D", type=int, default=8192)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--dtype", choices=("bf16", "f16", "f32"), default="bf16",
+                    help="profiling mode: element type")
+    ap.add_argument("--layout", choices=("dense", "strided", "padded"), default="dense",
+                    help="profiling mode: strided = the tensors are halves of [rows, 2D] "
+                         "buffers; padded = rows of D + 64 elements")
+    ap.add_argument("--rstd", action="store_true",
+                    help="profiling mode: the forward writes rstd / the VJP reads it")
     ap.add_argument("--all-configs", action="store_true",
                     help="table of µs/call and GB/s for every workload configuration; no JSON line")
     args = ap.parse_args(argv)

@@ -9,9 +9,10 @@
 // memory into fp32 registers once, and writes its outputs straight to global
 // memory.  A 16-byte vector holds eight fp16/bf16 or four fp32 elements.
 //
-// GEN = true is the general instance: rows a stride apart (a tensor whose
-// tile is not contiguous is copied one row per lane of warp 0, which then
-// shares the producer's work; the tile is dense in shared memory either way)
+// GEN = true is the general instance: rows a stride apart (in the sub-warp
+// shape a tensor whose tile is not contiguous is copied one row at a time,
+// those copies spread over all threads of the CTA; the tile is dense in
+// shared memory either way)
 // and the per-row scale rstd (written by the forward, read by the VJP in place
 // of its own sum of squares).  GEN = false is the dense instance without
 // rstd; the launcher picks it whenever it applies, so the common case carries
@@ -51,6 +52,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     constexpr int VP = vec_pairs<T>();   // float2 pairs per 16-byte vector
     constexpr int EPV = vec_elems<T>();  // elements per 16-byte vector
     constexpr bool CTA_ROW = (G == NT);
+    // Tiles of several rows a stride apart take one copy per row, spread over
+    // the CTA's threads; a CTA-per-row tile is always a single copy.
+    constexpr bool SPREAD_COPIES = GEN && !CTA_ROW;
     constexpr int NTENS = input_tensors(MODE);
     constexpr bool VJP = is_vjp(MODE);
     constexpr bool ADD = (MODE == MODE_VJP_ADD);
@@ -91,42 +95,74 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
         return ring + ((size_t)s * NTENS + tensor) * SB;
     };
 
-    // ---- producer: thread 0 (GEN: every lane of warp 0; lane 0 alone for
-    // contiguous tiles) ----
+    // ---- producer ----
+    // Thread 0 posts a tile's expected bytes on its stage's mbarrier and
+    // issues its copies.  With SPREAD_COPIES thread 0 posts the bytes before
+    // the CTA barrier that ends the previous tile in that stage, and after the
+    // barrier every thread issues a share of the tile's copies.
     int64_t issued = 0;  // tiles of this CTA issued so far
     int issue_stage = 0;
     const uint64_t policy = l2_evict_first_policy();
-    auto copy_rows = [&](unsigned char *dst, const T *src, int64_t ld, int64_t row0, int nr,
-                         uint64_t *bar) {
-        if constexpr (!GEN) {
-            bulk_g2s(dst, src + row0 * D, (uint32_t)nr * row_bytes, bar, policy);
-        } else if (ld == D || nr == 1) {
-            if (lane == 0) bulk_g2s(dst, src + row0 * ld, (uint32_t)nr * row_bytes, bar, policy);
-        } else {
-            for (int q = lane; q < nr; q += 32)
-                bulk_g2s(dst + (size_t)q * row_bytes, src + (row0 + q) * ld, row_bytes, bar, policy);
+    // First row and row count of this CTA's tile number idx; false for the
+    // tile the test hook drops.
+    auto tile_of = [&](int64_t idx, int64_t &row0, int &nr) -> bool {
+        const int64_t t = (int64_t)blockIdx.x + idx * grid;
+        row0 = t * TR;
+        nr = (int)min((int64_t)TR, rows - row0);
+        return t != a.drop_tile;
+    };
+    auto post_expect = [&](int64_t idx, int stage) {
+        int64_t row0;
+        int nr;
+        if (tile_of(idx, row0, nr))
+            mbar_arrive_expect_tx(&full[stage], (uint32_t)nr * row_bytes * NTENS);
+    };
+    // Copies first, first + step, ... of the tile's (tensor, row) pairs; a
+    // tensor whose tile is contiguous goes as one copy, on its row 0's turn.
+    auto issue_copies = [&](int64_t idx, int stage, int first, int step) {
+        int64_t row0;
+        int nr;
+        if (!tile_of(idx, row0, nr)) return;
+        for (int c = first; c < NTENS * nr; c += step) {
+            const int tensor = c / nr, q = c - tensor * nr;
+            const T *src = tensor == 0 ? in0 : tensor == 1 ? in1 : in2;
+            const int64_t ld = tensor == 0 ? a.ld_in0 : tensor == 1 ? a.ld_in1 : a.ld_in2;
+            unsigned char *dst = stage_ptr(stage, tensor);
+            if (ld == D || nr == 1) {
+                if (q == 0)
+                    bulk_g2s(dst, src + row0 * ld, (uint32_t)nr * row_bytes, &full[stage], policy);
+            } else {
+                bulk_g2s(dst + (size_t)q * row_bytes, src + (row0 + q) * ld, row_bytes,
+                         &full[stage], policy);
+            }
         }
     };
-    auto issue_next = [&]() {
-        const int64_t t = (int64_t)blockIdx.x + issued * grid;
-        if (t != a.drop_tile) {
-            const int64_t row0 = t * TR;
-            const int nr = (int)min((int64_t)TR, rows - row0);
-            uint64_t *bar = &full[issue_stage];
-            if constexpr (GEN) {
-                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nr * row_bytes * NTENS);
-                __syncwarp();  // the expected bytes are posted before any copy
-            } else {
-                mbar_arrive_expect_tx(bar, (uint32_t)nr * row_bytes * NTENS);
-            }
-            copy_rows(stage_ptr(issue_stage, 0), in0, a.ld_in0, row0, nr, bar);
-            if constexpr (NTENS >= 2)
-                copy_rows(stage_ptr(issue_stage, 1), in1, a.ld_in1, row0, nr, bar);
-            if constexpr (NTENS == 3)
-                copy_rows(stage_ptr(issue_stage, 2), in2, a.ld_in2, row0, nr, bar);
-        }
+    auto advance = [&]() {
         ++issued;
         issue_stage = issue_stage + 1 == S ? 0 : issue_stage + 1;
+    };
+    auto issue_next = [&]() {  // thread 0, the whole tile
+        int64_t row0;
+        int nr;
+        if (tile_of(issued, row0, nr)) {
+            uint64_t *bar = &full[issue_stage];
+            const uint32_t bytes = (uint32_t)nr * row_bytes;
+            mbar_arrive_expect_tx(bar, bytes * NTENS);
+            if constexpr (!SPREAD_COPIES) {
+                // dense tiles, or CTA per row (one row: one copy per tensor);
+                // straight-line code, as thread 0 is on every row's critical path
+                const int64_t l0 = GEN ? a.ld_in0 : D, l1 = GEN ? a.ld_in1 : D;
+                const int64_t l2 = GEN ? a.ld_in2 : D;
+                bulk_g2s(stage_ptr(issue_stage, 0), in0 + row0 * l0, bytes, bar, policy);
+                if constexpr (NTENS >= 2)
+                    bulk_g2s(stage_ptr(issue_stage, 1), in1 + row0 * l1, bytes, bar, policy);
+                if constexpr (NTENS == 3)
+                    bulk_g2s(stage_ptr(issue_stage, 2), in2 + row0 * l2, bytes, bar, policy);
+            } else {
+                issue_copies(issued, issue_stage, 0, 1);
+            }
+        }
+        advance();
     };
     // Timeout exit: flag it, then wait (bounded) for this CTA's copies that
     // may still be landing in shared memory before the CTA retires.
@@ -148,10 +184,19 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     // Launched as a programmatic dependent: nothing in global memory may be
     // touched before the previous kernel on the stream has completed.
     griddep_wait();
-    const bool producer = GEN ? warp == 0 : tid == 0;
-    if (producer) {
+    {
         const int64_t n0 = min((int64_t)S, nk);
-        while (issued < n0) issue_next();
+        if constexpr (SPREAD_COPIES) {
+            if (tid == 0)
+                for (int64_t i = 0; i < n0; ++i) post_expect(i, (int)i);
+            __syncthreads();  // the expected bytes are posted before any copy
+            for (int64_t i = 0; i < n0; ++i) {
+                issue_copies(i, issue_stage, tid, NT);
+                advance();
+            }
+        } else if (tid == 0) {
+            while (issued < n0) issue_next();
+        }
     }
 
     // w' = weight_bias + w for the columns this thread owns, in fp32.
@@ -261,7 +306,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
                 fail(k);
                 return;
             }
-            if (producer && k >= 1 && issued < nk) issue_next();
+            if (tid == 0 && k >= 1 && issued < nk) issue_next();
             float2 tot = lane < NWARPS ? rb[lane] : make_float2(0.f, 0.f);
             tot.x = group_sum<32>(tot.x);
             if constexpr (VJP) tot.y = group_sum<32>(tot.y);
@@ -282,6 +327,11 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
         for (int64_t k = 0; k < nk; ++k) {
             const int64_t row0 = ((int64_t)blockIdx.x + k * grid) * TR;
             const int nr = (int)min((int64_t)TR, rows - row0);
+            // The VJP may be handed the forward's scale: fetch this thread's
+            // first row's early, and each next row's one row ahead.
+            float r_next = 0.f;
+            if constexpr (GEN && VJP)
+                if (a.rstd && gid < nr) r_next = __ldg(a.rstd + row0 + gid);
             const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_budget);
             const uint4 *t0 = reinterpret_cast<const uint4 *>(stage_ptr(s, 0));
             const uint4 *t1 = reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS >= 2 ? 1 : 0));
@@ -289,6 +339,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
             for (int qb = 0; qb < TR; qb += NG) {  // same trip count in every lane
                 const int q = qb + gid;
                 const bool valid = q < nr;
+                const float r_saved = r_next;
+                if constexpr (GEN && VJP)
+                    if (a.rstd && q + NG < nr) r_next = __ldg(a.rstd + row0 + q + NG);
                 float2 xa[V][VP], xb[V][VP];
                 float sa = 0.f, sb = 0.f;
                 if (valid) load_row(t0 + (size_t)q * NV, t1 + (size_t)q * NV, xa, xb, sa, sb);
@@ -297,18 +350,29 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
                 if (valid && ok) {
                     float r = rsqrtf(sa / Df + eps);
                     if constexpr (GEN && VJP) {
-                        if (a.rstd) r = __ldg(a.rstd + row0 + q);
+                        if (a.rstd) r = r_saved;
                     } else if constexpr (GEN) {
                         if (a.rstd && gl == 0) a.rstd[row0 + q] = r;
                     }
                     row_outputs(xa, xb, t2 + (size_t)q * NV, row0 + q, r, sb);
                 }
             }
+            // Thread 0 has seen the stage's phase complete (ok), so the next
+            // phase may take its expected bytes now.
+            if constexpr (SPREAD_COPIES)
+                if (tid == 0 && ok && issued < nk) post_expect(issued, issue_stage);
             if (__syncthreads_or(!ok)) {  // the whole tile is consumed
                 fail(k);
                 return;
             }
-            if (producer && issued < nk) issue_next();
+            if constexpr (SPREAD_COPIES) {
+                if (issued < nk) {
+                    issue_copies(issued, issue_stage, tid, NT);
+                    advance();
+                }
+            } else if (tid == 0 && issued < nk) {
+                issue_next();
+            }
             if (++s == S) {
                 s = 0;
                 ph ^= 1u;
