@@ -3,7 +3,10 @@
 // or rows longer than the vectorised tiers take), and the gw stage-2 sum.
 //
 // One CTA per row, grid-stride; pass 1 forms the sums, pass 2 re-reads the row
-// (from L1/L2) and writes the outputs.  The VJP accumulates each CTA's gw
+// (from L1/L2) and writes the outputs.  A thread's share of a row can be long
+// (65536 elements at D = 2^24), so its sums are compensated (Neumaier): the
+// error of r then stays at a few fp32 roundings at any D instead of growing
+// with the row length (a plain running sum left r off by 2e-5 at D = 2^24).  The VJP accumulates each CTA's gw
 // contributions in that CTA's own row of the partials buffer; thread t owns
 // columns t, t + NT, ..., so no two threads ever touch the same partial and
 // the order is fixed.
@@ -17,6 +20,14 @@
 #include "plan.h"
 
 namespace rmsn {
+
+// s + v into (s, c): s the running sum, c the running rounding error of it.
+__device__ __forceinline__ void neumaier_add(float &s, float &c, float v) {
+    const float t = __fadd_rn(s, v);
+    c = __fadd_rn(c, fabsf(s) >= fabsf(v) ? __fadd_rn(__fsub_rn(s, t), v)
+                                          : __fadd_rn(__fsub_rn(v, t), s));
+    s = t;
+}
 
 template <typename T, int MODE>
 __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a) {
@@ -50,20 +61,22 @@ __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a)
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, ++it) {
         const T *x_row = in0 + row * l0;
         const T *y_row = in1 + row * l1;  // residual or g
-        float sa = 0.f, sb = 0.f;
+        float sa = 0.f, sb = 0.f, ca = 0.f, cb = 0.f;
         for (int c = tid; c < D; c += NT) {
             const float x = Cvt<T>::load1(x_row + c);
             if constexpr (MODE == MODE_FWD_RES) {
                 const float h = x + Cvt<T>::load1(y_row + c);
-                sa += h * h;
+                neumaier_add(sa, ca, __fmul_rn(h, h));
             } else if constexpr (MODE == MODE_FWD_NORES) {
-                sa += x * x;
+                neumaier_add(sa, ca, __fmul_rn(x, x));
             } else {
                 const float g = Cvt<T>::load1(y_row + c);
-                sa += x * x;
-                sb += (g * (wb + Cvt<T>::load1(w + c))) * x;
+                neumaier_add(sa, ca, __fmul_rn(x, x));
+                neumaier_add(sb, cb, __fmul_rn(__fmul_rn(g, wb + Cvt<T>::load1(w + c)), x));
             }
         }
+        sa += ca;
+        sb += cb;
         sa = group_sum<32>(sa);
         if constexpr (VJP) sb = group_sum<32>(sb);
         if (lane == 0) {
