@@ -7,7 +7,7 @@
 // reduction.  The vectorised kernel gives each thread one 16-byte column of
 // the output (8 values) and walks the rows in steps of the grid's height with
 // four rows in flight (eight 16-byte loads per thread).  silu(a) = a / (1 +
-// expf(-a)) in fp32, the product rounded once.  Other shapes and alignments
+// e^-a) in fp32 (SFU exponential and reciprocal), the product rounded once.  Other shapes and alignments
 // take an element-wise kernel.
 #include "rmsnorm.h"
 
@@ -29,7 +29,12 @@ constexpr int GATE_NT = 256;
 constexpr int GATE_ROWS_IN_FLIGHT = 4;
 constexpr int GATE_CTAS_PER_SM = 4;  // registers capped at 64 so four fit
 
-__device__ __forceinline__ float silu(float a) { return a / (1.f + expf(-a)); }
+// silu(a) = a / (1 + e^-a) with the SFU's exponential and reciprocal
+// (__expf, __fdividef: a few ulp, far inside the fp16/bf16 rounding of the
+// output); the full-precision expf and division left the vectorised kernel
+// issue-bound at 85 % of the copy bandwidth.  For a < -87 the divisor
+// overflows and the result is 0 (the true value is below 1e-36 in magnitude).
+__device__ __forceinline__ float silu(float a) { return __fdividef(a, 1.f + __expf(-a)); }
 
 template <typename T>
 __global__ void __launch_bounds__(GATE_NT, GATE_CTAS_PER_SM) gated_silu_vec_kernel(const uint4 *x, uint4 *out,
