@@ -4,11 +4,19 @@
 // writes k and v into the cache slab or a paged pool block, with cos/sin
 // from a precomputed table or computed on the fly).
 //
-// Persistent CTAs walk groups of four consecutive tokens.  For each group the
-// CTA first fills a shared-memory table of the Dh/2 (cos, sin) pairs of each
-// token's position -- read from the caller's table or computed -- and then
-// every q and k head of those tokens rotates with it; v is copied.  Vectorised threads own 8 rotation pairs each
-// (two 16-byte vectors in the rotate-half layout, one in the interleaved one).
+// Vectorised shapes (Dh % 16 == 0, 16-byte aligned, up to 32 rotation units
+// per head) of at least 128 tokens run warp-wide: a warp takes one token (or one of up to eight parts
+// of it, when there are fewer tokens than warps), each lane owns one rotation
+// unit -- 8 pairs, two 16-byte vectors, in the rotate-half layout; 4 pairs,
+// one vector, interleaved -- of 32 / units heads at a time, and computes (or
+// reads) the cos/sin of its own pairs once for all of that token's q and k
+// heads.  No shared-memory table and no CTA barrier: every warp streams on
+// its own, two heads' loads in flight per lane.  Other shapes take a
+// CTA-wide kernel: persistent CTAs walk groups of four consecutive tokens,
+// fill a shared-memory table of the Dh/2 (cos, sin) pairs of each token's
+// position, and then rotate every q and k head of those tokens with it
+// (element-wise, or with vectors for Dh past the warp kernel's limit); v is
+// copied.
 //
 // On-the-fly angles without FP64 on the device: theta_i = p * base^(-2i/Dh).
 // base^(-2i/Dh) is computed on the host in double (cached per thread for the
@@ -42,6 +50,8 @@ using namespace rmsn;
 
 constexpr int ROPE_NT = 256;
 constexpr int ROPE_CTAS_PER_SM = 4;
+constexpr int ROPE_WARP_CTAS_PER_SM = 3;  // the warp kernel: 85 registers, no spills
+constexpr int64_t ROPE_WARP_MIN_TOKENS = 128;
 constexpr int ROPE_MAX_DH = 1024;
 constexpr int ROPE_TOKENS_PER_ITER = 4;  // tokens a CTA handles between barriers
 constexpr unsigned int DEVSTATUS_BAD_INDEX = 2u;
@@ -75,6 +85,142 @@ __device__ __forceinline__ float reduced_angle(int64_t p, float inv_hi, float in
     float r = fmaf(-kq, TWO_PI_HI, s);
     r = fmaf(-kq, TWO_PI_LO, r);
     return r + t;
+}
+
+// One rotation unit: PPU pairs of the head at src rotated into dst with the
+// lane's (cos, sin) pairs cs, from registers xa (and xb, rotate-half: the
+// vector half a head further on).
+template <typename T, bool INTERLEAVED>
+__device__ __forceinline__ void rotate_store(const uint4 &xa, const uint4 &xb, const float2 *cs,
+                                             T *dst, int half) {
+    if constexpr (!INTERLEAVED) {
+        float2 a1[4], a2[4], y1[4], y2[4];
+        unpack8<T>(xa, a1);
+        unpack8<T>(xb, a2);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float2 c0 = cs[2 * m], c1 = cs[2 * m + 1];
+            y1[m] = make_float2(a1[m].x * c0.x - a2[m].x * c0.y, a1[m].y * c1.x - a2[m].y * c1.y);
+            y2[m] = make_float2(a2[m].x * c0.x + a1[m].x * c0.y, a2[m].y * c1.x + a1[m].y * c1.y);
+        }
+        *reinterpret_cast<uint4 *>(dst) = pack8<T>(y1);
+        *reinterpret_cast<uint4 *>(dst + half) = pack8<T>(y2);
+    } else {
+        float2 x[4], y[4];
+        unpack8<T>(xa, x);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            y[m] = make_float2(x[m].x * cs[m].x - x[m].y * cs[m].y, x[m].y * cs[m].x + x[m].x * cs[m].y);
+        *reinterpret_cast<uint4 *>(dst) = pack8<T>(y);
+    }
+}
+
+// Rotates heads [0, H) of one token (src -> dst, head stride Dh): this lane's
+// unit c of heads h0 + hs, h0 + hs + step, ...; two heads' loads are issued
+// before either is stored (heads never share an address, so in place too).
+template <typename T, bool INTERLEAVED>
+__device__ __forceinline__ void rotate_heads(const T *src, T *dst, int H, int h_first, int step,
+                                             int Dh, int unit_off, const float2 *cs) {
+    const int half = Dh / 2;
+    for (int h = h_first; h < H; h += 2 * step) {
+        const int h2 = h + step;
+        const bool two = h2 < H;
+        const T *s1 = src + (int64_t)h * Dh + unit_off, *s2 = src + (int64_t)h2 * Dh + unit_off;
+        const uint4 a1 = *reinterpret_cast<const uint4 *>(s1);
+        uint4 b1 = a1, a2 = a1, b2 = a1;
+        if constexpr (!INTERLEAVED) b1 = *reinterpret_cast<const uint4 *>(s1 + half);
+        if (two) {
+            a2 = *reinterpret_cast<const uint4 *>(s2);
+            if constexpr (!INTERLEAVED) b2 = *reinterpret_cast<const uint4 *>(s2 + half);
+        }
+        rotate_store<T, INTERLEAVED>(a1, b1, cs, dst + (int64_t)h * Dh + unit_off, half);
+        if (two) rotate_store<T, INTERLEAVED>(a2, b2, cs, dst + (int64_t)h2 * Dh + unit_off, half);
+    }
+}
+
+template <typename T, bool INTERLEAVED>
+__global__ void __launch_bounds__(ROPE_NT, ROPE_WARP_CTAS_PER_SM) rope_warp_kernel(const RopeArgs a,
+                                                                                 int wpt) {
+    constexpr int PPU = INTERLEAVED ? 4 : 8;  // rotation pairs per unit
+    __shared__ float2 s_inv[ROPE_MAX_DH / 2];
+    const int Dh = a.Dh, half = Dh / 2;
+    const bool table = a.cos_sin != nullptr;
+    if (!table) {  // the lanes of a warp read different frequencies: from shared memory
+        for (int i = threadIdx.x; i < half; i += ROPE_NT) s_inv[i] = a.inv[i];
+        __syncthreads();
+    }
+    griddep_wait();  // programmatic dependent: no global access before this
+
+    const int lane = threadIdx.x & 31;
+    const int units = half / PPU;      // per head, at most 32 here
+    const int hpi = 32 / units;        // heads a warp covers per step
+    const int hs = lane / units, c = lane - hs * units;
+    const bool rot_lane = hs < hpi;
+    const int unit_off = INTERLEAVED ? c * 8 : c * PPU;  // first element of the unit
+    const T *q = static_cast<const T *>(a.q);
+    const T *k = static_cast<const T *>(a.k);
+    const uint4 *v = static_cast<const uint4 *>(a.v);
+    T *q_out = static_cast<T *>(a.q_out);
+    T *k_cache = static_cast<T *>(a.k_cache);
+    uint4 *v_cache = static_cast<uint4 *>(a.v_cache);
+    const int Hq = a.Hq, Hkv = a.Hkv;
+    const int v_vecs = Hkv * Dh / 8;   // 16-byte vectors of v per token
+
+    const int64_t n_items = a.T * wpt;
+    const int64_t n_warps = (int64_t)gridDim.x * (ROPE_NT / 32);
+    for (int64_t w = ((int64_t)blockIdx.x * ROPE_NT + threadIdx.x) >> 5; w < n_items; w += n_warps) {
+        const int64_t t = w / wpt;
+        const int part = (int)(w - t * wpt);
+        const int64_t p = a.positions[t];
+        const int64_t slot = a.slots[t];
+        const bool pos_ok = p >= 0 && (!table || p < a.max_pos);
+        const bool slot_ok = slot < a.num_slots;  // negative: not written
+        if ((!pos_ok || !slot_ok) && lane == 0 && part == 0) atomicOr(a.status, DEVSTATUS_BAD_INDEX);
+        if (!pos_ok) continue;
+        const bool write_kv = slot_ok && slot >= 0;
+
+        float2 cs[PPU];
+        if (rot_lane) {
+            const int i0 = c * PPU;
+            if (table) {
+                const float4 *row = reinterpret_cast<const float4 *>(a.cos_sin + p * Dh);
+#pragma unroll
+                for (int m = 0; m < PPU; m += 4) {
+                    const float4 cv = row[(i0 + m) / 4], sv = row[(half + i0 + m) / 4];
+                    cs[m] = make_float2(cv.x, sv.x);
+                    cs[m + 1] = make_float2(cv.y, sv.y);
+                    cs[m + 2] = make_float2(cv.z, sv.z);
+                    cs[m + 3] = make_float2(cv.w, sv.w);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < PPU; ++m) {
+                    const float2 f = s_inv[i0 + m];
+                    sincosf(reduced_angle(p, f.x, f.y), &cs[m].y, &cs[m].x);
+                }
+            }
+            const int step = wpt * hpi;
+            rotate_heads<T, INTERLEAVED>(q + t * Hq * (int64_t)Dh, q_out + t * Hq * (int64_t)Dh, Hq,
+                                         part * hpi + hs, step, Dh, unit_off, cs);
+            if (write_kv)
+                rotate_heads<T, INTERLEAVED>(k + t * Hkv * (int64_t)Dh,
+                                             k_cache + slot * Hkv * (int64_t)Dh, Hkv,
+                                             part * hpi + hs, step, Dh, unit_off, cs);
+        }
+        if (write_kv) {
+            const uint4 *vs = v + t * v_vecs;
+            uint4 *vd = v_cache + slot * v_vecs;
+            for (int i = part * 32 + lane; i < v_vecs; i += 2 * 32 * wpt) {
+                const int i2 = i + 32 * wpt;
+                const uint4 x1 = vs[i];
+                uint4 x2 = x1;
+                if (i2 < v_vecs) x2 = vs[i2];
+                vd[i] = x1;
+                if (i2 < v_vecs) vd[i2] = x2;
+            }
+        }
+    }
+    griddep_launch_dependents();
 }
 
 template <typename T, bool INTERLEAVED, bool VEC>
@@ -198,7 +344,24 @@ __global__ void __launch_bounds__(ROPE_NT, ROPE_CTAS_PER_SM) rope_kv_kernel(cons
 }
 
 template <typename T, bool INTERLEAVED>
-cudaError_t launch_rope_t(const RopeArgs &a, bool vec, int grid, cudaStream_t s) {
+cudaError_t launch_rope_t(const RopeArgs &a, bool vec, int sm, cudaStream_t s) {
+    const int64_t resident = (int64_t)sm * ROPE_CTAS_PER_SM;
+    const int units = INTERLEAVED ? a.Dh / 8 : a.Dh / 16;  // rotation units per head
+    // A warp computes its lanes' cos/sin one pair after another (a dependent
+    // chain of 4-8 sincosf): with a handful of tokens that latency shows
+    // (8 tokens: +1.7 us), so decode-sized calls keep the CTA-wide kernel,
+    // whose 256 threads compute a group's table side by side.
+    if (vec && units <= 32 && a.T >= ROPE_WARP_MIN_TOKENS) {
+        // warps per token: spread a few tokens over more warps (up to 8)
+        const int64_t resident_w = (int64_t)sm * ROPE_WARP_CTAS_PER_SM;
+        const int64_t warps = resident_w * (ROPE_NT / 32);
+        const int wpt = (int)std::max<int64_t>(1, std::min<int64_t>(8, warps / a.T));
+        const int64_t need = (a.T * wpt + ROPE_NT / 32 - 1) / (ROPE_NT / 32);
+        const int grid = (int)std::min<int64_t>(need, resident_w);
+        return launch_pdl(rope_warp_kernel<T, INTERLEAVED>, dim3(grid), dim3(ROPE_NT), 0, s, a, wpt);
+    }
+    const int64_t groups = (a.T + ROPE_TOKENS_PER_ITER - 1) / ROPE_TOKENS_PER_ITER;
+    const int grid = (int)std::min<int64_t>(groups, resident);
     if (vec)
         return launch_pdl(rope_kv_kernel<T, INTERLEAVED, true>, dim3(grid), dim3(ROPE_NT), 0, s, a);
     return launch_pdl(rope_kv_kernel<T, INTERLEAVED, false>, dim3(grid), dim3(ROPE_NT), 0, s, a);
@@ -279,17 +442,15 @@ extern "C" int rmsnorm_rope_kv_append(const void *q, const void *k, const void *
     a.Hq = (int)Hq; a.Hkv = (int)Hkv; a.Dh = (int)Dh;
     a.status = status;
     if (!cos_sin) inverse_frequencies(rope_base, (int)Dh, a.inv);
-    const bool vec = Dh % 16 == 0 && al16(q) && al16(q_out) && (Hkv == 0 ||
-                     (al16(k) && al16(v) && al16(k_cache) && al16(v_cache)));
-    const int64_t groups = (T + ROPE_TOKENS_PER_ITER - 1) / ROPE_TOKENS_PER_ITER;
-    const int grid = (int)std::min<int64_t>(groups, (int64_t)sm * ROPE_CTAS_PER_SM);
+    const bool vec = Dh % 16 == 0 && al16(q) && al16(q_out) && (!cos_sin || al16(cos_sin)) &&
+                     (Hkv == 0 || (al16(k) && al16(v) && al16(k_cache) && al16(v_cache)));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (dtype == RMSNORM_F16)
-        e = interleaved ? launch_rope_t<__half, true>(a, vec, grid, s)
-                        : launch_rope_t<__half, false>(a, vec, grid, s);
+        e = interleaved ? launch_rope_t<__half, true>(a, vec, sm, s)
+                        : launch_rope_t<__half, false>(a, vec, sm, s);
     else
-        e = interleaved ? launch_rope_t<__nv_bfloat16, true>(a, vec, grid, s)
-                        : launch_rope_t<__nv_bfloat16, false>(a, vec, grid, s);
+        e = interleaved ? launch_rope_t<__nv_bfloat16, true>(a, vec, sm, s)
+                        : launch_rope_t<__nv_bfloat16, false>(a, vec, sm, s);
     return e == cudaSuccess ? RMSNORM_OK : record_cuda_error(e);
 }
