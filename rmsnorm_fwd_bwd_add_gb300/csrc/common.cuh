@@ -258,4 +258,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Global -> shared 2-D tensor copy of one box of the tensor map at `tmap` (a
+// kernel parameter's address) with its first element at column x (x times
+// the element size a multiple of 16), row y; rows past the tensor's end are
+// zero-filled and still count toward the box's bytes on `bar`.  dst must be
+// 128-byte aligned.
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 }  // namespace rmsn

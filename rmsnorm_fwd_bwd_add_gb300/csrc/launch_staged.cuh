@@ -1,6 +1,8 @@
 // launch_staged.cuh -- picks the staged_kernel instance for a plan.
 #pragma once
 
+#include <type_traits>
+
 #include "launch_util.h"
 #include "staged.cuh"
 
@@ -16,8 +18,19 @@ cudaError_t launch_staged_inst(const Plan &p, const KernelArgs &a, cudaStream_t 
     return launch_pdl(kern, dim3(p.grid), dim3(NT), p.smem, stream, a);
 }
 
+// Column boxes for the tensor maps: the fewest boxes of equal width that
+// tile D, at most 256 elements wide (the TMA box limit) and a multiple of 16
+// bytes; 0 if four boxes do not do it.
+inline int tmap_boxes(int64_t D, int es) {
+    for (int n = 1; n <= 4; ++n)
+        if (D % n == 0 && D / n <= 256 && (D / n * es) % 16 == 0) return n;
+    return 0;
+}
+
 // The dense instance unless a tensor the mode uses has rows a stride apart
-// or rstd is given.
+// or rstd is given.  General sub-warp tiles go through 2-D tensor maps when
+// D splits into boxes (one copy per box instead of one per row), else one
+// bulk copy per row.
 template <typename T, int MODE, int NT, int G, int V>
 cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
     const int64_t D = a.D;
@@ -25,8 +38,32 @@ cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t s
     if constexpr (input_tensors(MODE) >= 2) gen = gen || a.ld_in1 != D;
     if constexpr (input_tensors(MODE) == 3) gen = gen || a.ld_in2 != D;
     if constexpr (MODE == MODE_FWD_RES) gen = gen || a.ld_out1 != D;
-    return gen ? launch_staged_inst<T, MODE, NT, G, V, true>(p, a, stream)
-               : launch_staged_inst<T, MODE, NT, G, V, false>(p, a, stream);
+    if (!gen) return launch_staged_inst<T, MODE, NT, G, V, false>(p, a, stream);
+    if constexpr (G == NT) {
+        return launch_staged_inst<T, MODE, NT, G, V, true>(p, a, stream);
+    } else {
+        constexpr int es = (int)sizeof(T);
+        constexpr int dtype = es == 4 ? 2 : std::is_same<T, __half>::value ? 0 : 1;
+        KernelArgs b = a;
+        b.box_cols = a.D;
+        b.use_tmap = 0;
+        const int n = tmap_boxes(D, es);
+        const int64_t box_bytes = n ? (int64_t)p.tile_rows * (D / n) * es : 0;
+        // every box lands 128-byte aligned; row coordinates fit in int32
+        if (n && box_bytes % 128 == 0 && p.tile_rows <= 256 && a.rows <= INT32_MAX) {
+            const void *ins[3] = {a.in0, a.in1, a.in2};
+            const int64_t lds[3] = {a.ld_in0, a.ld_in1, a.ld_in2};
+            bool ok = true;
+            for (int i = 0; i < input_tensors(MODE) && ok; ++i)
+                ok = encode_rows_tmap(&b.tmap[i], ins[i], a.rows, D, lds[i], dtype,
+                                      (int)(D / n), p.tile_rows);
+            if (ok) {
+                b.box_cols = (int)(D / n);
+                b.use_tmap = 1;
+            }
+        }
+        return launch_staged_inst<T, MODE, NT, G, V, true>(p, b, stream);
+    }
 }
 
 template <typename T, int MODE>

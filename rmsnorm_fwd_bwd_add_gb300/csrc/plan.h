@@ -2,6 +2,7 @@
 // (api.cu) and the per-tier launchers.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -38,6 +39,13 @@ struct KernelArgs {
     // Per-row 1/sqrt(ms + eps), fp32 [rows] or null: written by the forward,
     // read (instead of summing h^2) by the VJP.
     float *rstd;
+    // General sub-warp instance: tiles land in shared memory as column boxes
+    // [D / box_cols][tile_rows][box_cols] (box_cols == D: plain rows).  With
+    // use_tmap the inputs in0..in2 come through the 2-D tensor maps tmap[],
+    // one copy per box; without, one bulk copy per row.
+    int box_cols;
+    int use_tmap;
+    CUtensorMap tmap[3];
 };
 
 struct Plan {
@@ -104,5 +112,11 @@ cudaError_t launch_direct(int dtype, int mode, const Plan &plan, const KernelArg
 cudaError_t launch_generic(int dtype, int mode, const Plan &plan, const KernelArgs &a,
                            cudaStream_t stream);
 cudaError_t launch_gw_reduce(const float *partials, float *gw, int P, int D, cudaStream_t stream);
+
+// A 2-D tensor map of a [rows, D] tensor with row stride ld elements and
+// boxes of box_cols x box_rows elements (no swizzle, zero fill past the last
+// row).  False if the driver refuses it or the entry point is missing.
+bool encode_rows_tmap(CUtensorMap *map, const void *base, int64_t rows, int64_t D, int64_t ld,
+                      int dtype, int box_cols, int box_rows);
 
 }  // namespace rmsn

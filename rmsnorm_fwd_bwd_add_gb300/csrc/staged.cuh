@@ -46,7 +46,7 @@
 namespace rmsn {
 
 template <typename T, int MODE, int NT, int G, int V, int MINB, bool GEN>
-__global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
+__global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant__ KernelArgs a) {
     constexpr int NWARPS = NT / 32;
     constexpr int NG = NT / G;  // rows processed side by side
     constexpr int VP = vec_pairs<T>();   // float2 pairs per 16-byte vector
@@ -141,6 +141,25 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
         ++issued;
         issue_stage = issue_stage + 1 == S ? 0 : issue_stage + 1;
     };
+    // General sub-warp tiles through the tensor maps (thread 0): one 2-D copy
+    // per column box and tensor; a box past the last row is zero-filled and
+    // its bytes still arrive, so the whole tile is expected.
+    const int BC = SPREAD_COPIES ? a.box_cols : D;  // columns per box
+    const bool tmap_mode = SPREAD_COPIES && a.use_tmap;
+    auto issue_tmap = [&]() {
+        const int64_t t = (int64_t)blockIdx.x + issued * grid;
+        if (t != a.drop_tile) {
+            uint64_t *bar = &full[issue_stage];
+            const uint32_t box_bytes = (uint32_t)TR * (uint32_t)BC * (uint32_t)sizeof(T);
+            const int nbox = D / BC;
+            mbar_arrive_expect_tx(bar, box_bytes * (uint32_t)(nbox * NTENS));
+            for (int tensor = 0; tensor < NTENS; ++tensor)
+                for (int b = 0; b < nbox; ++b)
+                    tma_load_2d(stage_ptr(issue_stage, tensor) + (size_t)b * box_bytes,
+                                &a.tmap[tensor], b * BC, (int)(t * TR), bar, policy);
+        }
+        advance();
+    };
     auto issue_next = [&]() {  // thread 0, the whole tile
         int64_t row0;
         int nr;
@@ -187,12 +206,17 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
     {
         const int64_t n0 = min((int64_t)S, nk);
         if constexpr (SPREAD_COPIES) {
-            if (tid == 0)
-                for (int64_t i = 0; i < n0; ++i) post_expect(i, (int)i);
-            __syncthreads();  // the expected bytes are posted before any copy
-            for (int64_t i = 0; i < n0; ++i) {
-                issue_copies(i, issue_stage, tid, NT);
-                advance();
+            if (tmap_mode) {
+                if (tid == 0)
+                    while (issued < n0) issue_tmap();
+            } else {
+                if (tid == 0)
+                    for (int64_t i = 0; i < n0; ++i) post_expect(i, (int)i);
+                __syncthreads();  // the expected bytes are posted before any copy
+                for (int64_t i = 0; i < n0; ++i) {
+                    issue_copies(i, issue_stage, tid, NT);
+                    advance();
+                }
             }
         } else if (tid == 0) {
             while (issued < n0) issue_next();
@@ -219,6 +243,20 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
 #pragma unroll
         for (int q = 0; q < VP; ++q) acc[j][q] = make_float2(0.f, 0.f);
 
+    // Where vector j of a tile's row q sits in the stage: col[j] + q * row_step
+    // (general sub-warp instance: column boxes; otherwise plain rows, vi + q * NV).
+    int col[SPREAD_COPIES ? V : 1];
+    int row_step = NV;
+    if constexpr (SPREAD_COPIES) {
+        const int bwv = BC / EPV;  // vectors per box row
+        row_step = bwv;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int vi = gl + j * G, b = vi / bwv;
+            col[j] = b * (TR * bwv) + (vi - b * bwv);
+        }
+    }
+
     // One row: load this thread's vectors from the stage into fp32 (h = x +
     // residual, or x; the VJP also g), and its partial sum(h^2) and, for the
     // VJP, partial dot = sum(g * w' * x).
@@ -229,8 +267,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
         for (int j = 0; j < V; ++j) {
             const int vi = gl + j * G;
             if (vi < NV) {
-                unpack_vec<T>(r0[vi], xa[j]);
-                if constexpr (NTENS >= 2) unpack_vec<T>(r1[vi], xb[j]);
+                const int si = SPREAD_COPIES ? col[SPREAD_COPIES ? j : 0] : vi;
+                unpack_vec<T>(r0[si], xa[j]);
+                if constexpr (NTENS >= 2) unpack_vec<T>(r1[si], xb[j]);
                 if constexpr (MODE == MODE_FWD_RES) {
 #pragma unroll
                     for (int q = 0; q < VP; ++q) xa[j][q] = f2add(xa[j][q], xb[j][q]);  // h
@@ -269,7 +308,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
                     }
                     if constexpr (ADD) {
                         float2 gr[VP];
-                        unpack_vec<T>(r2[vi], gr);
+                        unpack_vec<T>(r2[SPREAD_COPIES ? col[SPREAD_COPIES ? j : 0] : vi], gr);
 #pragma unroll
                         for (int q = 0; q < VP; ++q) o[q] = f2add(o[q], gr[q]);  // + g_new_residual
                     }
@@ -344,7 +383,8 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
                     if (a.rstd && q + NG < nr) r_next = __ldg(a.rstd + row0 + q + NG);
                 float2 xa[V][VP], xb[V][VP];
                 float sa = 0.f, sb = 0.f;
-                if (valid) load_row(t0 + (size_t)q * NV, t1 + (size_t)q * NV, xa, xb, sa, sb);
+                if (valid)
+                    load_row(t0 + (size_t)q * row_step, t1 + (size_t)q * row_step, xa, xb, sa, sb);
                 sa = group_sum<G>(sa);
                 if constexpr (VJP) sb = group_sum<G>(sb);
                 if (valid && ok) {
@@ -354,19 +394,21 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const KernelArgs a) {
                     } else if constexpr (GEN) {
                         if (a.rstd && gl == 0) a.rstd[row0 + q] = r;
                     }
-                    row_outputs(xa, xb, t2 + (size_t)q * NV, row0 + q, r, sb);
+                    row_outputs(xa, xb, t2 + (size_t)q * row_step, row0 + q, r, sb);
                 }
             }
             // Thread 0 has seen the stage's phase complete (ok), so the next
             // phase may take its expected bytes now.
             if constexpr (SPREAD_COPIES)
-                if (tid == 0 && ok && issued < nk) post_expect(issued, issue_stage);
+                if (!tmap_mode && tid == 0 && ok && issued < nk) post_expect(issued, issue_stage);
             if (__syncthreads_or(!ok)) {  // the whole tile is consumed
                 fail(k);
                 return;
             }
             if constexpr (SPREAD_COPIES) {
-                if (issued < nk) {
+                if (tmap_mode) {
+                    if (tid == 0 && issued < nk) issue_tmap();
+                } else if (issued < nk) {
                     issue_copies(issued, issue_stage, tid, NT);
                     advance();
                 }
