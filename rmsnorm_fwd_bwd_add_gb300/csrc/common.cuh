@@ -259,8 +259,8 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 }
 
 // Global -> shared 2-D tensor copy of one box of the tensor map at `tmap` (a
-// kernel parameter's address) with its first element at column x (x times
-// the element size a multiple of 16), row y; rows past the tensor's end are
+// kernel parameter's address) with its first element at column x (in the
+// map's units; x times the unit size a multiple of 16 bytes), row y; rows past the tensor's end are
 // zero-filled and still count toward the box's bytes on `bar`.  dst must be
 // 128-byte aligned.
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y,

@@ -19,11 +19,12 @@ cudaError_t launch_staged_inst(const Plan &p, const KernelArgs &a, cudaStream_t 
 }
 
 // Column boxes for the tensor maps: the fewest boxes of equal width that
-// tile D, at most 256 elements wide (the TMA box limit) and a multiple of 16
-// bytes; 0 if four boxes do not do it.
+// tile D, at most 2 KB wide (256 units of 8 bytes, the TMA box limit) and a
+// multiple of 16 bytes; 0 if four boxes do not do it.  Rows of the sub-warp
+// shape (at most 2 KB) take one box.
 inline int tmap_boxes(int64_t D, int es) {
     for (int n = 1; n <= 4; ++n)
-        if (D % n == 0 && D / n <= 256 && (D / n * es) % 16 == 0) return n;
+        if (D % n == 0 && D / n * es <= 2048 && (D / n * es) % 16 == 0) return n;
     return 0;
 }
 

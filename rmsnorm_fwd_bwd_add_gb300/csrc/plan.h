@@ -114,8 +114,10 @@ cudaError_t launch_generic(int dtype, int mode, const Plan &plan, const KernelAr
 cudaError_t launch_gw_reduce(const float *partials, float *gw, int P, int D, cudaStream_t stream);
 
 // A 2-D tensor map of a [rows, D] tensor with row stride ld elements and
-// boxes of box_cols x box_rows elements (no swizzle, zero fill past the last
-// row).  False if the driver refuses it or the entry point is missing.
+// boxes of box_cols x box_rows elements, counted in 8-byte units (box rows of
+// up to 2 KB; no swizzle, zero fill past the last row; the x coordinate of a
+// copy is in 8-byte units too).  False if the driver refuses it or the entry
+// point is missing.
 bool encode_rows_tmap(CUtensorMap *map, const void *base, int64_t rows, int64_t D, int64_t ld,
                       int dtype, int box_cols, int box_rows);
 

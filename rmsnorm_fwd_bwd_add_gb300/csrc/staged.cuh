@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
             for (int tensor = 0; tensor < NTENS; ++tensor)
                 for (int b = 0; b < nbox; ++b)
                     tma_load_2d(stage_ptr(issue_stage, tensor) + (size_t)b * box_bytes,
-                                &a.tmap[tensor], b * BC, (int)(t * TR), bar, policy);
+                                &a.tmap[tensor], b * BC * (int)sizeof(T) / 8, (int)(t * TR), bar,
+                                policy);
         }
         advance();
     };

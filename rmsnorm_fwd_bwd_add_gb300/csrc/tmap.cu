@@ -36,14 +36,14 @@ bool encode_rows_tmap(CUtensorMap *map, const void *base, int64_t rows, int64_t 
     const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn || !base) return false;
     const int es = dtype == 2 ? 4 : 2;
-    const CUtensorMapDataType ty = dtype == 0   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                   : dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    if ((D * es) % 8 || (box_cols * es) % 8) return false;
+    // The copy only moves bytes, so the map counts 8-byte units: a box row
+    // can then span 256 of them (2 KB) instead of 256 elements.
+    const cuuint64_t dims[2] = {(cuuint64_t)(D * es / 8), (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};  // bytes between rows
-    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)(box_cols * es / 8), (cuuint32_t)box_rows};
     const cuuint32_t elem_strides[2] = {1, 1};
-    return fn(map, ty, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
