@@ -621,8 +621,11 @@ def run_single_op(args):
 def run_all_configs(args):
     """Every workload configuration, fwd and VJP: µs per call with L2 flushed
     before each call (cold), back to back (warm: small problems then live in
-    L2), and replayed from a CUDA graph of back-to-back calls (launch cost
-    amortised); GB/s of algorithmic bytes.  Prints one table row per case."""
+    L2), replayed from a CUDA graph of back-to-back calls (launch cost
+    amortised), and back to back over K copies of the problem's tensors whose
+    total is at least twice the L2 (rotating: sustained HBM bandwidth, no
+    reuse between calls; median of 20 repetitions of at least 1 ms); GB/s of
+    algorithmic bytes, cold and rotating.  Prints one table row per case."""
     from rmsnorm_fwd_bwd_add_gb300 import build, workloads as W
     import rmsnorm_fwd_bwd_add_gb300 as rn
     build.build()
@@ -635,8 +638,10 @@ def run_all_configs(args):
     cases += [W.config3()]
     cases += [W.config4(D) for D in W.PREFILL_D]
     cases += [W.config5(D, dt) for D in W.SWEEP_D for dt in (torch.float16, torch.bfloat16)]
-    print("%-22s %-4s %-62s %9s %9s %9s %9s" % ("case", "op", "plan", "cold_us", "warm_us",
-                                               "graph_us", "cold_GB/s"), flush=True)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    print("%-22s %-4s %-62s %9s %9s %9s %9s %9s %9s" % (
+        "case", "op", "plan", "cold_us", "warm_us", "graph_us", "rot_us", "cold_GB/s", "rot_GB/s"),
+        flush=True)
     for c in cases:
         x, w = c.x.to(dev), c.w.to(dev)
         res = c.residual.to(dev) if c.residual is not None else None
@@ -654,6 +659,27 @@ def run_all_configs(args):
             ops.append(("fvjp", lambda: rn.rmsnorm_fused_vjp(x, w, g, c.eps, c.weight_bias, res,
                                                              g_h=gx, gw=gw),
                         fused_vjp_bytes(c.rows, c.D, 2)))
+        # K copies of every [rows, D] tensor for the rotating measurement (at
+        # most 256: the decode shapes stay launch-bound whatever K is)
+        per_set = (5 if res is not None else 4) * x.numel() * x.element_size()
+        K = int(min(256, max(2, -(-2 * l2 // per_set))))
+
+        def stack(t):
+            return None if t is None else t.unsqueeze(0).repeat(K, *([1] * t.dim()))
+        xs, gs, rs = stack(x), stack(g), stack(res)
+        outs, gxs = torch.empty_like(xs), torch.empty_like(xs)
+        nrs = None if res is None else torch.empty_like(xs)
+        sets = [dict(x=xs[i], g=gs[i], out=outs[i], gx=gxs[i],
+                     res=None if rs is None else rs[i], nr=None if nrs is None else nrs[i])
+                for i in range(K)]
+        rot_ops = {
+            "fwd": lambda t: rn.rmsnorm_fwd(t["x"], w, c.eps, c.weight_bias, t["res"], out=t["out"],
+                                            new_residual=t["nr"]),
+            "vjp": lambda t: rn.rmsnorm_vjp_ws(t["x"], w, t["g"], c.eps, c.weight_bias, workspace=ws,
+                                               gx=t["gx"], gw=gw),
+            "fvjp": lambda t: rn.rmsnorm_fused_vjp(t["x"], w, t["g"], c.eps, c.weight_bias, t["res"],
+                                                   g_h=t["gx"], gw=gw),
+        }
         for name, f, nbytes in ops:
             for _ in range(5):
                 f()
@@ -692,11 +718,26 @@ def run_all_configs(args):
             torch.cuda.synchronize()
             graph_us = 1e3 * a.elapsed_time(b) / n
             cold_us = statistics.median(cold)
+            rf = rot_ops[name]
+            calls = K * max(1, -(-int(1000.0 / max(cold_us, 1.0)) // K))  # >= ~1 ms per repetition
+            for i in range(K):
+                rf(sets[i])
+            torch.cuda.synchronize()
+            rot = []
+            for _ in range(20):
+                a.record()
+                for i in range(calls):
+                    rf(sets[i % K])
+                b.record()
+                torch.cuda.synchronize()
+                rot.append(1e3 * a.elapsed_time(b) / calls)
+            rot_us = statistics.median(rot)
             plan = rn.rmsnorm_describe_dispatch("fwd" if name == "fwd" else "vjp", c.rows, c.D,
                                                 c.dtype, name != "vjp" and res is not None)
-            print("%-22s %-4s %-62s %9.2f %9.2f %9.2f %9.1f" % (c.name, name, plan, cold_us, warm,
-                                                             graph_us, nbytes / cold_us / 1e3),
-                  flush=True)
+            print("%-22s %-4s %-62s %9.2f %9.2f %9.2f %9.2f %9.1f %9.1f" % (
+                c.name, name, plan, cold_us, warm, graph_us, rot_us, nbytes / cold_us / 1e3,
+                nbytes / rot_us / 1e3), flush=True)
+        del sets, xs, gs, rs, outs, gxs, nrs
     return 0
 
 
