@@ -4,6 +4,7 @@
 #include <type_traits>
 
 #include "launch_util.h"
+#include "planner.h"
 #include "staged.cuh"
 
 namespace rmsn {
@@ -51,7 +52,8 @@ cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t s
         const int n = tmap_boxes(D, es);
         const int64_t box_bytes = n ? (int64_t)p.tile_rows * (D / n) * es : 0;
         // every box lands 128-byte aligned; row coordinates fit in int32
-        if (n && box_bytes % 128 == 0 && p.tile_rows <= 256 && a.rows <= INT32_MAX) {
+        if (n && box_bytes % 128 == 0 && p.tile_rows <= 256 && a.rows <= INT32_MAX &&
+            planner::tuning().tmap) {
             const void *ins[3] = {a.in0, a.in1, a.in2};
             const int64_t lds[3] = {a.ld_in0, a.ld_in1, a.ld_in2};
             bool ok = true;

@@ -45,12 +45,15 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 
 // Overrides of the staged tier's choices, read once from RMSNORM_TUNE
-// ("cfg=N,cps=N,stages=N", any subset) for tuning sweeps.  Unset, the plan
-// is a pure function of the problem and the device.
+// ("cfg=N,cps=N,stages=N,tmap=0", any subset) for tuning sweeps and for
+// testing the per-row copy path that strided sub-warp tiles take where no
+// tensor map can be made.  Unset, the plan is a pure function of the problem
+// and the device.
 struct Tuning {
-    int cfg = -1;    // staged configuration index
-    int cps = 0;     // CTAs per SM (capped by what the registers allow)
-    int stages = 0;  // maximum ring depth
+    int cfg = -1;     // staged configuration index
+    int cps = 0;      // CTAs per SM (capped by what the registers allow)
+    int stages = 0;   // maximum ring depth
+    bool tmap = true; // tensor maps for strided sub-warp tiles
 };
 
 inline Tuning parse_tuning() {
@@ -64,6 +67,7 @@ inline Tuning parse_tuning() {
         if (std::sscanf(tok, "cfg=%d", &v) == 1 && v >= 0 && v < N_STAGED_CFG) t.cfg = v;
         else if (std::sscanf(tok, "cps=%d", &v) == 1 && v >= 1 && v <= 3) t.cps = v;
         else if (std::sscanf(tok, "stages=%d", &v) == 1 && v >= 2 && v <= MAX_STAGES) t.stages = v;
+        else if (std::sscanf(tok, "tmap=%d", &v) == 1) t.tmap = v != 0;
     }
     return t;
 }

@@ -203,3 +203,18 @@ def test_fp32_dispatch_and_gw_determinism():
     _, a = rn.rmsnorm_vjp(*args)
     _, b = rn.rmsnorm_vjp(*args)
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_per_row_copy_fallback():
+    """Strided sub-warp tiles without tensor maps (the path taken where the
+    driver cannot make one): the strided and rstd cases above, rerun in a
+    child process with the maps switched off."""
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, RMSNORM_TUNE="tmap=0")
+    r = subprocess.run([sys.executable, "-m", "pytest", __file__, "-q", "-x", "-p", "no:cacheprovider",
+                        "-k", "test_strided_forward_and_vjp or test_vjp_with_supplied_rstd"],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout
