@@ -34,7 +34,7 @@ cudaError_t direct_mode(const Plan &p, const KernelArgs &a, cudaStream_t s) {
         case 0: return direct_one<T, MODE, 128, 1>(p, a, s);
         case 1: return direct_one<T, MODE, 256, 1>(p, a, s);
         case 2: return direct_one<T, MODE, 512, 1>(p, a, s);
-        case 3: return direct_one<T, MODE, 1024, 1>(p, a, s);
+        case 3: return direct_one<T, MODE, 512, 2>(p, a, s);  // measured: 1024 x 1 is 0.35 us slower
         case 4: return direct_one<T, MODE, 1024, 2>(p, a, s);
         case 5:
             // Four vectors of x and g per thread plus gw accumulators do not

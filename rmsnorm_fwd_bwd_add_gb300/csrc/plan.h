@@ -81,7 +81,7 @@ constexpr int STAGED_CFG_WIDE = 10;
 
 constexpr int N_DIRECT_CFG = 6;
 constexpr DirectCfg DIRECT_CFGS[N_DIRECT_CFG] = {
-    {128, 1, 128}, {256, 1, 256}, {512, 1, 512}, {1024, 1, 1024}, {1024, 2, 2048}, {1024, 4, 4096},
+    {128, 1, 128}, {256, 1, 256}, {512, 1, 512}, {512, 2, 1024}, {1024, 2, 2048}, {1024, 4, 4096},
 };
 
 // Most CTAs of a staged configuration that can share one SM, as the kernels'
