@@ -54,7 +54,7 @@ def _fwd(lib, x=1, res=None, w=1, eps=1e-6, wb=0.0, out=1, nr=None, rows=4, D=64
 
 def test_host_validation_without_gpu(lib):
     # every case below is rejected before the library touches CUDA
-    assert _fwd(lib, dtype=2) == 1
+    assert _fwd(lib, dtype=3) == 1
     assert _fwd(lib, D=0) == 1
     assert _fwd(lib, rows=-1) == 1
     assert _fwd(lib, eps=-1e-6) == 1
@@ -82,6 +82,48 @@ def test_host_validation_without_gpu(lib):
     assert lib.rmsnorm_vjp_workspace_size(4, 0, 0) == 0
     assert lib.rmsnorm_describe_dispatch(2, 4, 64, 0, 0, 1) == b"invalid"
     assert lib.rmsnorm_debug_inject(-1, 0) == 0
+
+
+def _fwd_ex(lib, x, ld_x, out, ld_out, res=None, ld_res=0, nr=None, ld_nr=0, rstd=None, w=1 << 40,
+            rows=8, D=64, dtype=1):
+    return lib.rmsnorm_fwd_ex(x, ld_x, res, ld_res, w, 1e-6, 0.0, out, ld_out, nr, ld_nr, rstd,
+                              rows, D, dtype, None)
+
+
+def test_strided_validation_without_gpu(lib):
+    """Row strides and rstd: rejections come before any CUDA call; layouts
+    that pass it reach the device query, which fails here without a GPU
+    (status 3), so they are only checked where no GPU is present."""
+    import torch
+    B, D, rows = 1 << 30, 64, 8
+    row = 2 * D * 2  # bytes of one row of a [rows, 2D] bf16 buffer
+    assert _fwd_ex(lib, B, D - 1, 1 << 32, D) == 1                       # row stride < D
+    assert _fwd_ex(lib, B, 2 * D, B + 16, 2 * D) == 1                     # shifted by 16 bytes
+    assert _fwd_ex(lib, B, 2 * D, B + D * 2 - 2, 2 * D) == 1              # last element shared
+    assert _fwd_ex(lib, B, 2 * D, B + D * 2, 3 * D) == 1                  # other stride, extents meet
+    assert _fwd_ex(lib, B, 2 * D, 1 << 32, D, rstd=B + row) == 1          # rstd inside x's span
+    assert _fwd_ex(lib, B, 2 * D, 1 << 32, D, rstd=(1 << 40) + 8) == 1    # rstd over w
+    assert _fwd_ex(lib, B, 2 * D, 1 << 32, D, res=B + D * 2, ld_res=2 * D,
+                   nr=B + 8, ld_nr=2 * D) == 1                             # new_residual over x
+    assert _fwd_ex(lib, B, 2 * D, 1 << 32, D, res=1 << 34, ld_res=D, nr=None) == 1
+    vjp = lib.rmsnorm_vjp_ex
+    gx = 1 << 32
+    # g_residual partly over gx; rstd over gx; rstd over gw
+    assert vjp(B, D, 1 << 40, 1 << 36, D, gx + 64, D, None, 1e-6, 0.0, gx, D, 1 << 38, rows, D, 1,
+               None) == 1
+    assert vjp(B, D, 1 << 40, 1 << 36, D, None, 0, gx + 32, 1e-6, 0.0, gx, D, 1 << 38, rows, D, 1,
+               None) == 1
+    assert vjp(B, D, 1 << 40, 1 << 36, D, None, 0, (1 << 38) + 4, 1e-6, 0.0, gx, D, 1 << 38, rows,
+               D, 1, None) == 1
+    assert vjp(B, D - 8, 1 << 40, 1 << 36, D, None, 0, None, 1e-6, 0.0, gx, D, 1 << 38, rows, D, 1,
+               None) == 1
+    if torch.cuda.is_available():
+        return  # the accepted layouts below would launch on made-up addresses
+    assert _fwd_ex(lib, B, 2 * D, B + D * 2, 2 * D) == 3                  # the other half: disjoint
+    assert _fwd_ex(lib, B + D * 2, 2 * D, B, 2 * D) == 3                  # and the other way round
+    assert _fwd_ex(lib, B, 2 * D, B, 2 * D) == 3                          # in place
+    assert _fwd_ex(lib, B, D, B, 5 * D, rows=1) == 3                      # one row: no stride
+    assert _fwd_ex(lib, B, 2 * D, 1 << 32, D, dtype=2) == 3               # fp32
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
