@@ -85,18 +85,30 @@ constexpr DirectCfg DIRECT_CFGS[N_DIRECT_CFG] = {
 };
 
 // Most CTAs of a staged configuration that can share one SM, as the kernels'
-// __launch_bounds__ promise it (registers per thread capped to fit).  A
-// CTA-per-row forward of up to 256 threads and two vectors fits three times
-// (85 registers); other CTAs of up to 256 threads twice (128 registers),
-// except the small-D VJP with three or four vectors per lane, which needs the
-// whole register file like every larger CTA.
+// __launch_bounds__ promise it (registers per thread capped to fit):
+// CTA-per-row forwards with two vectors per thread: 6 of 128 threads (85
+// registers) or 3 of 256 (85); CTA-per-row VJPs of 128 threads: 4 (128);
+// other CTAs of up to 256 threads 2 (128 registers), except the small-D VJP
+// with three or four vectors per lane, which needs the whole register file
+// like every larger CTA.
 constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
-    return (nt <= 256 && mode < 2 && g == nt && v <= 2) ? 3
-           : (nt <= 256 && !(mode >= 2 && v >= 3)) ? 2 : 1;
+    return (g == nt && mode < 2 && nt <= 128 && v <= 2)   ? 6
+           : (g == nt && mode < 2 && nt <= 256 && v <= 2) ? 3
+           : (g == nt && mode >= 2 && nt <= 128 && v <= 2) ? 4
+           : (nt <= 256 && !(mode >= 2 && v >= 3))        ? 2
+                                                           : 1;
 }
-// CTAs per SM the plan uses unless tuned otherwise.
+// CTAs per SM the plan uses unless tuned otherwise (measured on GB300,
+// bf16, 8192-32768 rows): 128-thread CTA-per-row CTAs as many as fit (6 for
+// the forward, 4 for the VJP: at D = 2048 the forward went from 5697 to 6406
+// GB/s and the VJP from 3522 to 5802 against two); the forward without a
+// residual (mode 1) three 256-thread CTAs (D = 3072: 4486 -> 5614); everything
+// else two, or one where only one fits (the forward with a residual at
+// D = 4096: 6394 with two, 6221 with three).
 constexpr int staged_ctas_per_sm(int mode, int nt, int g, int v) {
-    return staged_max_ctas_per_sm(mode, nt, g, v) >= 2 ? 2 : 1;
+    return (g == nt && nt <= 128) ? staged_max_ctas_per_sm(mode, nt, g, v)
+           : (g == nt && mode == 1 && staged_max_ctas_per_sm(mode, nt, g, v) >= 3) ? 3
+           : staged_max_ctas_per_sm(mode, nt, g, v) >= 2 ? 2 : 1;
 }
 
 constexpr int GENERIC_NT = 256;

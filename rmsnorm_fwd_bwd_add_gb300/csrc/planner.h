@@ -43,6 +43,14 @@ constexpr size_t INFLIGHT_VJP = 96 * 1024;
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Shared memory one CTA may take when `cps` CTAs share an SM.
+inline size_t smem_per_cta(int cps) {
+    return cps <= 1 ? SMEM_ONE_PER_SM
+           : cps == 2 ? SMEM_TWO_PER_SM
+           : cps == 3 ? SMEM_THREE_PER_SM
+                      : (size_t)(224 * 1024) / (size_t)cps - 2048;
+}
+
 
 // Overrides of the staged tier's choices, read once from RMSNORM_TUNE
 // ("cfg=N,cps=N,stages=N,tmap=0", any subset) for tuning sweeps and for
@@ -65,7 +73,7 @@ inline Tuning parse_tuning() {
     for (char *tok = std::strtok(buf, ","); tok; tok = std::strtok(nullptr, ",")) {
         int v = 0;
         if (std::sscanf(tok, "cfg=%d", &v) == 1 && v >= 0 && v < N_STAGED_CFG) t.cfg = v;
-        else if (std::sscanf(tok, "cps=%d", &v) == 1 && v >= 1 && v <= 3) t.cps = v;
+        else if (std::sscanf(tok, "cps=%d", &v) == 1 && v >= 1 && v <= 6) t.cps = v;
         else if (std::sscanf(tok, "stages=%d", &v) == 1 && v >= 2 && v <= MAX_STAGES) t.stages = v;
         else if (std::sscanf(tok, "tmap=%d", &v) == 1) t.tmap = v != 0;
     }
@@ -121,29 +129,24 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
         if (is_vjp(mode))  // the cross-group gw sum reuses the ring
             p->smem = std::max(p->smem, (size_t)STAGED_HEADER_BYTES + (size_t)ng * D * 4);
     } else {
-        // One row per tile, the whole CTA on it.  Two CTAs per SM when the
-        // registers allow it and each can hold three stages, else one CTA
-        // with at least two; the depth then follows the in-flight target.
+        // One row per tile, the whole CTA on it.  The requested CTAs per SM
+        // when each CTA's share of shared memory holds its stages (two with
+        // three or more CTAs, three with two), fewer otherwise, down to one
+        // CTA with at least two; the depth then follows the in-flight target.
         p->tile_rows = 1;
         p->stage_bytes = (uint32_t)row_bytes;
         const size_t per_stage = (size_t)ntens * row_bytes;
-        const int64_t s3 = (int64_t)(SMEM_THREE_PER_SM / per_stage);
-        const int64_t s2 = (int64_t)(SMEM_TWO_PER_SM / per_stage);
-        const int64_t s1 = (int64_t)(SMEM_ONE_PER_SM / per_stage);
-        if (cps == 3 && s3 >= 2) {
-            p->stages = (int)std::min<int64_t>(std::min<int64_t>(max_stages, s3),
-                                               ring_stages(mode, per_stage, 3));
-        } else if (cps >= 2 && s2 >= 3) {
-            cps = 2;
-            p->stages = (int)std::min<int64_t>(std::min<int64_t>(max_stages, s2),
-                                               ring_stages(mode, per_stage, 2));
-        } else if (s1 >= 2) {
-            cps = 1;
-            p->stages = (int)std::min<int64_t>(std::min<int64_t>(max_stages, s1),
-                                               ring_stages(mode, per_stage, 1));
-        } else {
-            return false;
+        int chosen = 0;
+        for (int c = cps; c >= 1 && !chosen; --c) {
+            const int64_t sc = (int64_t)(smem_per_cta(c) / per_stage);
+            if (sc >= (c >= 3 ? 2 : c == 2 ? 3 : 2)) {
+                chosen = c;
+                p->stages = (int)std::min<int64_t>(std::min<int64_t>(max_stages, sc),
+                                                   ring_stages(mode, per_stage, c));
+            }
         }
+        if (!chosen) return false;
+        cps = chosen;
         p->smem = STAGED_HEADER_BYTES + (size_t)p->stages * per_stage;
     }
     p->num_tiles = ceil_div(rows, p->tile_rows);
