@@ -66,7 +66,7 @@ struct Plan {
 struct StagedCfg { int nt, g, v, max_nv; };
 struct DirectCfg { int nt, v, max_nv; };
 
-constexpr int N_STAGED_CFG = 11;
+constexpr int N_STAGED_CFG = 15;
 constexpr StagedCfg STAGED_CFGS[N_STAGED_CFG] = {
     // sub-warp / warp per row (shuffle-only reductions), 256 threads
     {256, 8, 1, 8}, {256, 16, 1, 16}, {256, 32, 1, 32},
@@ -76,6 +76,10 @@ constexpr StagedCfg STAGED_CFGS[N_STAGED_CFG] = {
     // CTA per row, four vectors per thread: two 256-thread CTAs per SM for
     // rows of up to 8192 (forward only: the VJP would need too many registers)
     {256, 256, 4, 1024},
+    // CTA per row for rows of 3 * 2^k vectors (D = 1536, 3072, 6144, 12288 in
+    // bf16), which the power-of-two CTAs above fit with a quarter of their
+    // threads idle
+    {96, 96, 2, 192}, {192, 192, 2, 384}, {384, 384, 2, 768}, {768, 768, 2, 1536},
 };
 constexpr int STAGED_CFG_WIDE = 10;
 
@@ -86,29 +90,39 @@ constexpr DirectCfg DIRECT_CFGS[N_DIRECT_CFG] = {
 
 // Most CTAs of a staged configuration that can share one SM, as the kernels'
 // __launch_bounds__ promise it (registers per thread capped to fit):
-// CTA-per-row forwards with two vectors per thread: 6 of 128 threads (85
-// registers) or 3 of 256 (85); CTA-per-row VJPs of 128 threads: 4 (128);
-// other CTAs of up to 256 threads 2 (128 registers), except the small-D VJP
-// with three or four vectors per lane, which needs the whole register file
-// like every larger CTA.
+// CTA-per-row forwards with two vectors per thread: 6 of up to 128 threads,
+// 3 of up to 256 (85 registers), 2 of 384 (85); CTA-per-row VJPs with two
+// vectors: 6 of 96 threads (113), 4 of 128 (128); other CTAs of up to 256
+// threads 2 (128 registers), except the small-D VJP with three or four
+// vectors per lane, which needs the whole register file like every larger CTA.
 constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
-    return (g == nt && mode < 2 && nt <= 128 && v <= 2)   ? 6
-           : (g == nt && mode < 2 && nt <= 256 && v <= 2) ? 3
+    return (g == nt && mode < 2 && nt <= 128 && v <= 2)    ? 6
+           : (g == nt && mode < 2 && nt <= 256 && v <= 2)  ? 3
+           : (g == nt && mode < 2 && nt <= 384 && v <= 2)  ? 2
+           : (g == nt && mode >= 2 && nt <= 96 && v <= 2)  ? 6
            : (g == nt && mode >= 2 && nt <= 128 && v <= 2) ? 4
-           : (nt <= 256 && !(mode >= 2 && v >= 3))        ? 2
-                                                           : 1;
+           : (nt <= 256 && !(mode >= 2 && v >= 3))         ? 2
+                                                            : 1;
 }
-// CTAs per SM the plan uses unless tuned otherwise (measured on GB300,
-// bf16, 8192-32768 rows): 128-thread CTA-per-row CTAs as many as fit (6 for
-// the forward, 4 for the VJP: at D = 2048 the forward went from 5697 to 6406
-// GB/s and the VJP from 3522 to 5802 against two); the forward without a
-// residual (mode 1) three 256-thread CTAs (D = 3072: 4486 -> 5614); everything
-// else two, or one where only one fits (the forward with a residual at
-// D = 4096: 6394 with two, 6221 with three).
+// CTAs per SM the plan uses unless tuned otherwise, from sweeps of 1-6 on
+// GB300 (bf16, rotating buffers, 8192-32768 rows).  CTA-per-row shapes:
+//   * up to 128 threads: as many as fit (D = 2048 forward 5697 -> 6442 GB/s,
+//     VJP 3522 -> 5814 against two);
+//   * the forward without a residual (mode 1): three of 192 or 256 threads
+//     (D = 3072: 4486 -> 5622), two of 384;
+//   * the forward with a residual (mode 0): three of 192 threads, two of 256
+//     (D = 4096: 6394 against 6221 with three), one of 384 or more, whose
+//     ring is then deep enough (D = 6144: 6575 against 6134 with two);
+//   * the VJP: two of up to 256 threads, one above.
+// Sub-warp shapes: two, or one where only one fits.
 constexpr int staged_ctas_per_sm(int mode, int nt, int g, int v) {
-    return (g == nt && nt <= 128) ? staged_max_ctas_per_sm(mode, nt, g, v)
-           : (g == nt && mode == 1 && staged_max_ctas_per_sm(mode, nt, g, v) >= 3) ? 3
-           : staged_max_ctas_per_sm(mode, nt, g, v) >= 2 ? 2 : 1;
+    const int most = staged_max_ctas_per_sm(mode, nt, g, v);
+    const int want = (g != nt)    ? 2
+                     : (nt <= 128) ? most
+                     : (mode == 1) ? (nt <= 256 ? 3 : nt <= 384 ? 2 : 1)
+                     : (mode == 0) ? (nt <= 192 ? 3 : nt <= 256 ? 2 : 1)
+                                   : (nt <= 256 ? 2 : 1);
+    return want < most ? want : most;
 }
 
 constexpr int GENERIC_NT = 256;

@@ -163,12 +163,14 @@ inline Plan make_plan(int mode, int64_t rows, int D, int esize, bool aligned, in
             !(is_vjp(mode) && forced == STAGED_CFG_WIDE) &&
             plan_staged(mode, rows, D, esize, sm_count, forced, &p))
             return p;
-        for (int ci = 0; ci < STAGED_CFG_WIDE; ++ci) {
-            if (nv <= STAGED_CFGS[ci].max_nv) {
-                if (plan_staged(mode, rows, D, esize, sm_count, ci, &p)) return p;
-                break;
-            }
-        }
+        // the configuration that fits the row most tightly (the wide one
+        // only when tuned)
+        int best = -1;
+        for (int ci = 0; ci < N_STAGED_CFG; ++ci)
+            if (ci != STAGED_CFG_WIDE && nv <= STAGED_CFGS[ci].max_nv &&
+                (best < 0 || STAGED_CFGS[ci].max_nv < STAGED_CFGS[best].max_nv))
+                best = ci;
+        if (best >= 0 && plan_staged(mode, rows, D, esize, sm_count, best, &p)) return p;
     }
     if (aligned) {
         for (int ci = 0; ci < N_DIRECT_CFG; ++ci) {
