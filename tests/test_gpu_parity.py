@@ -129,6 +129,9 @@ EDGE = [
     (4099, 520), (613, 1024), (2, 1032), (311, 1032), (305, 2048), (307, 4104),
     (153, 8192), (7, 16384), (155, 16384), (9, 16392), (3, 32768), (11, 40000),
     (2, 1 << 20),
+    # CTA-per-row configurations that fit rows of 3 * 2^k vectors exactly
+    # (96, 192, 384 and 768 threads), at and just past their widths
+    (301, 1536), (257, 3072), (263, 2056), (97, 6144), (131, 12288), (35, 8200),
 ]
 
 
