@@ -30,6 +30,7 @@ from .api import (  # noqa: F401
     rmsnorm_status_string,
     rmsnorm_vjp,
     rmsnorm_vjp_ex,
+    rmsnorm_vjp_noalloc,
     rmsnorm_vjp_workspace_size,
     rmsnorm_vjp_ws,
 )
@@ -47,6 +48,7 @@ __all__ = [
     "fused_add_rmsnorm",
     "rms_norm",
     "rmsnorm_vjp_ws",
+    "rmsnorm_vjp_noalloc",
     "rmsnorm_vjp_workspace_size",
     "rmsnorm_device_status",
     "rmsnorm_debug_inject",

@@ -383,6 +383,25 @@ def rmsnorm_vjp_ws(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float
     return gx, gw
 
 
+def rmsnorm_vjp_noalloc(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float,
+                        weight_bias: float = 0.0, *, gx: Optional[torch.Tensor] = None,
+                        gw: Optional[torch.Tensor] = None, stream=None):
+    """rmsnorm_vjp with its gw partial rows in the library's fixed device array
+    (nothing allocated by the library; gx and gw are allocated here through
+    torch when not given).  Problems whose partials do not fit the array raise
+    with RMSNORM_ERR_UNSUPPORTED."""
+    rows, D = _rows_d(x)
+    code = _dtype_code(x)
+    _check_w(w, x, D)
+    gx, gw = _vjp_outputs(x, g, gx, gw, D)
+    with _OnDevice(x.device):
+        st = _native.lib().rmsnorm_vjp_noalloc(_ptr(x), _ptr(w), _ptr(g), eps, weight_bias,
+                                               _ptr(gx), _ptr(gw), rows, D, code,
+                                               _stream(x.device, stream))
+    _native.check("rmsnorm_vjp_noalloc", st)
+    return gx, gw
+
+
 def rmsnorm_device_status(clear: bool = True) -> int:
     """Device status bits of the current device (synchronises).  The bits are
     returned, not raised: the status the C call derives from them (timeout,

@@ -93,15 +93,15 @@ constexpr DirectCfg DIRECT_CFGS[N_DIRECT_CFG] = {
 // CTA-per-row forwards with two vectors per thread: 6 of up to 128 threads,
 // 3 of up to 256 (85 registers), 2 of 384 (85); CTA-per-row VJPs with two
 // vectors: 6 of 96 threads (113), 4 of 128 (128); other CTAs of up to 256
-// threads 2 (128 registers), except the small-D VJP with three or four
-// vectors per lane, which needs the whole register file like every larger CTA.
+// threads 2 (128 registers; the sub-warp VJP with three or four vectors per
+// lane fits by re-reading rows from shared memory); larger CTAs 1.
 constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
     return (g == nt && mode < 2 && nt <= 128 && v <= 2)    ? 6
            : (g == nt && mode < 2 && nt <= 256 && v <= 2)  ? 3
            : (g == nt && mode < 2 && nt <= 384 && v <= 2)  ? 2
            : (g == nt && mode >= 2 && nt <= 96 && v <= 2)  ? 6
            : (g == nt && mode >= 2 && nt <= 128 && v <= 2) ? 4
-           : (nt <= 256 && !(mode >= 2 && v >= 3))         ? 2
+           : (nt <= 256)                                   ? 2
                                                             : 1;
 }
 // CTAs per SM the plan uses unless tuned otherwise, from sweeps of 1-6 on

@@ -37,9 +37,15 @@ constexpr size_t SMALL_TILE_BYTES = 16 * 1024;
 // (rows 16384, D 4096 and 8192): more read-ahead than this starves the
 // kernel's own writes and lowers the bandwidth, less leaves HBM idle.  The
 // forward writes as much as it reads and wants ~64 KB; the VJP (two bytes
-// read per byte written) ~96 KB.
+// read per byte written) ~96 KB.  Sub-warp tiles (sweeps at D = 128-1024,
+// 32768-262144 rows) want less: ~48 KB for the forward (D = 640: 6313 GB/s
+// against 5945 with 80 KB) and ~64 KB for the VJP with two or more vectors
+// per lane (D = 1024: 5431 against 5121 with 128 KB); the one-vector VJP
+// keeps ~96 KB (D = 256: 5417 against 4614 with 64 KB).
 constexpr size_t INFLIGHT_FWD = 64 * 1024;
 constexpr size_t INFLIGHT_VJP = 96 * 1024;
+constexpr size_t INFLIGHT_FWD_SUBWARP = 48 * 1024;
+constexpr size_t INFLIGHT_VJP_SUBWARP = 64 * 1024;
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -86,11 +92,10 @@ inline const Tuning &tuning() {
 }
 
 // Ring depth for a stage of `per_stage` bytes with `cps` CTAs per SM: one
-// stage being consumed plus enough in flight to reach the mode's target
+// stage being consumed plus enough in flight to reach `target` bytes per SM
 // (at least one).  An explicit RMSNORM_TUNE stages= wins.
-inline int ring_stages(int mode, size_t per_stage, int cps) {
+inline int ring_stages(size_t target, size_t per_stage, int cps) {
     if (tuning().stages) return tuning().stages;
-    const size_t target = is_vjp(mode) ? INFLIGHT_VJP : INFLIGHT_FWD;
     const size_t per_sm_stage = per_stage * (size_t)cps;
     const int ahead = (int)std::max<size_t>(1, (target + per_sm_stage / 2) / per_sm_stage);
     return std::min(MAX_STAGES, 1 + ahead);
@@ -123,7 +128,10 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
         cps = std::min(cps, 2);
         const size_t cap = cps == 2 ? SMEM_TWO_PER_SM : SMEM_ONE_PER_SM;
         p->stages = (int)std::min<size_t>(std::min<size_t>(max_stages, cap / per_stage),
-                                          ring_stages(mode, per_stage, cps));
+                                          ring_stages(!is_vjp(mode) ? INFLIGHT_FWD_SUBWARP
+                                                      : c.v >= 2 ? INFLIGHT_VJP_SUBWARP
+                                                                 : INFLIGHT_VJP,
+                                                      per_stage, cps));
         if (p->stages < 2) return false;
         p->smem = STAGED_HEADER_BYTES + (size_t)p->stages * per_stage;
         if (is_vjp(mode))  // the cross-group gw sum reuses the ring
@@ -142,7 +150,9 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
             if (sc >= (c >= 3 ? 2 : c == 2 ? 3 : 2)) {
                 chosen = c;
                 p->stages = (int)std::min<int64_t>(std::min<int64_t>(max_stages, sc),
-                                                   ring_stages(mode, per_stage, c));
+                                                   ring_stages(is_vjp(mode) ? INFLIGHT_VJP
+                                                                            : INFLIGHT_FWD,
+                                                               per_stage, c));
             }
         }
         if (!chosen) return false;

@@ -55,6 +55,11 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     // Tiles of several rows a stride apart take one copy per row, spread over
     // the CTA's threads; a CTA-per-row tile is always a single copy.
     constexpr bool SPREAD_COPIES = GEN && !CTA_ROW;
+    // The sub-warp VJP with three or four vectors per lane re-reads a row from
+    // the stage (still resident until the tile is done) for its outputs
+    // instead of holding it in registers across the reduction: 128 registers,
+    // two CTAs per SM instead of one.
+    constexpr bool RELOAD = is_vjp(MODE) && !CTA_ROW && V >= 3;
     constexpr int NTENS = input_tensors(MODE);
     constexpr bool VJP = is_vjp(MODE);
     constexpr bool ADD = (MODE == MODE_VJP_ADD);
@@ -289,8 +294,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
 
     // Outputs of one row from the registers load_row filled (the fused-op VJP
     // also reads its row of the new_residual gradient, r2, from the stage).
-    auto row_outputs = [&](const float2 (&xa)[V][VP], const float2 (&xb)[V][VP], const uint4 *r2,
-                           int64_t row, float r, float dot) {
+    auto row_outputs = [&](const float2 (&xa_in)[V][VP], const float2 (&xb_in)[V][VP],
+                           const uint4 *r0, const uint4 *r1, const uint4 *r2, int64_t row, float r,
+                           float dot) {
         const size_t base0 = (size_t)(row * lo0), base1 = (size_t)(row * lo1);
         const float2 rr = make_float2(r, r);
         const float c = (r * r) * (dot / Df);  // r^2 * dot / D
@@ -300,12 +306,21 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
             const int vi = gl + j * G;
             if (vi < NV) {
                 float2 o[VP];
+                const float2 *xa = xa_in[j], *xb = xb_in[j];
+                float2 ra[VP], rb[VP];
+                if constexpr (RELOAD) {
+                    const int si = SPREAD_COPIES ? col[SPREAD_COPIES ? j : 0] : vi;
+                    unpack_vec<T>(r0[si], ra);
+                    unpack_vec<T>(r1[si], rb);
+                    xa = ra;
+                    xb = rb;
+                }
                 if constexpr (VJP) {
 #pragma unroll
                     for (int q = 0; q < VP; ++q) {
-                        const float2 u = f2mul(xb[j][q], wp[j][q]);           // g w'
-                        o[q] = f2mul(f2fma(xa[j][q], nc2, u), rr);             // r (g w' - x c)
-                        acc[j][q] = f2fma(xb[j][q], f2mul(xa[j][q], rr), acc[j][q]);  // g x r
+                        const float2 u = f2mul(xb[q], wp[j][q]);           // g w'
+                        o[q] = f2mul(f2fma(xa[q], nc2, u), rr);             // r (g w' - x c)
+                        acc[j][q] = f2fma(xb[q], f2mul(xa[q], rr), acc[j][q]);  // g x r
                     }
                     if constexpr (ADD) {
                         float2 gr[VP];
@@ -315,8 +330,8 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                     }
                 } else {
 #pragma unroll
-                    for (int q = 0; q < VP; ++q) o[q] = f2mul(f2mul(xa[j][q], rr), wp[j][q]);
-                    if constexpr (MODE == MODE_FWD_RES) st_global(out1 + base1 + vi, pack_vec<T>(xa[j]));
+                    for (int q = 0; q < VP; ++q) o[q] = f2mul(f2mul(xa[q], rr), wp[j][q]);
+                    if constexpr (MODE == MODE_FWD_RES) st_global(out1 + base1 + vi, pack_vec<T>(xa_in[j]));
                 }
                 st_global(out0 + base0 + vi, pack_vec<T>(o));
             }
@@ -356,7 +371,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
             } else if constexpr (GEN) {
                 if (a.rstd && tid == 0) a.rstd[row] = r;
             }
-            row_outputs(xa, xb, reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS - 1)), row, r,
+            row_outputs(xa, xb, reinterpret_cast<const uint4 *>(stage_ptr(s, 0)),
+                        reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS >= 2 ? 1 : 0)),
+                        reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS - 1)), row, r,
                         tot.y);
             if (++s == S) {
                 s = 0;
@@ -395,7 +412,8 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                     } else if constexpr (GEN) {
                         if (a.rstd && gl == 0) a.rstd[row0 + q] = r;
                     }
-                    row_outputs(xa, xb, t2 + (size_t)q * row_step, row0 + q, r, sb);
+                    row_outputs(xa, xb, t0 + (size_t)q * row_step, t1 + (size_t)q * row_step,
+                                t2 + (size_t)q * row_step, row0 + q, r, sb);
                 }
             }
             // Thread 0 has seen the stage's phase complete (ok), so the next

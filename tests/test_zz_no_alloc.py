@@ -69,3 +69,19 @@ def test_noalloc_refuses_problems_beyond_its_array(lib):
     st, gx, gw = _call_noalloc(lib, x, w, x, 1e-6, 0.0)
     assert st == 2  # RMSNORM_ERR_UNSUPPORTED, nothing enqueued
     assert lib.rmsnorm_status_string(st) == b"unsupported problem size"
+
+
+def test_noalloc_python_binding_is_bit_identical_to_rmsnorm_vjp():
+    import rmsnorm_fwd_bwd_add_gb300 as rn
+    from rmsnorm_fwd_bwd_add_gb300 import workloads as W
+    case = W.random_case(2048, 2048, torch.bfloat16, seed=21, residual=False)
+    x, w, g = case.x.to(DEV), case.w.to(DEV), case.g.to(DEV)
+    gx_ref, gw_ref = rn.rmsnorm_vjp(x, w, g, case.eps)
+    gx, gw = rn.rmsnorm_vjp_noalloc(x, w, g, case.eps)
+    # the same plan and summation order: the same bits
+    assert torch.equal(gx, gx_ref)
+    assert torch.equal(gw.view(torch.int32), gw_ref.view(torch.int32))
+    with pytest.raises(rn.RmsnormError) as e:
+        xl = torch.randn(2000, 40000, device=DEV).to(torch.bfloat16)
+        rn.rmsnorm_vjp_noalloc(xl, torch.ones(40000, dtype=torch.bfloat16, device=DEV), xl, 1e-6)
+    assert e.value.status == 2
