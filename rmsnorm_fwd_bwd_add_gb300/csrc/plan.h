@@ -92,7 +92,7 @@ constexpr DirectCfg DIRECT_CFGS[N_DIRECT_CFG] = {
 // __launch_bounds__ promise it (registers per thread capped to fit):
 // CTA-per-row forwards with two vectors per thread: 6 of up to 128 threads,
 // 3 of up to 256 (85 registers), 2 of 384 (85); CTA-per-row VJPs with two
-// vectors: 6 of 96 threads (113), 4 of 128 (128); other CTAs of up to 256
+// vectors: 6 of 96 threads (113), 4 of 128 (128), 3 of 192 (113); other CTAs of up to 256
 // threads 2 (128 registers; the sub-warp VJP with three or four vectors per
 // lane fits by re-reading rows from shared memory); larger CTAs 1.
 constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
@@ -101,6 +101,7 @@ constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
            : (g == nt && mode < 2 && nt <= 384 && v <= 2)  ? 2
            : (g == nt && mode >= 2 && nt <= 96 && v <= 2)  ? 6
            : (g == nt && mode >= 2 && nt <= 128 && v <= 2) ? 4
+           : (g == nt && mode >= 2 && nt <= 192 && v <= 2) ? 3
            : (nt <= 256)                                   ? 2
                                                             : 1;
 }
@@ -113,7 +114,8 @@ constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
 //   * the forward with a residual (mode 0): three of 192 threads, two of 256
 //     (D = 4096: 6394 against 6221 with three), one of 384 or more, whose
 //     ring is then deep enough (D = 6144: 6575 against 6134 with two);
-//   * the VJP: two of up to 256 threads, one above.
+//   * the VJP: three of 192 threads (D = 3072: 5032 -> 5294 against two),
+//     two of 256, one above.
 // Sub-warp shapes: two, or one where only one fits.
 constexpr int staged_ctas_per_sm(int mode, int nt, int g, int v) {
     const int most = staged_max_ctas_per_sm(mode, nt, g, v);
@@ -121,7 +123,7 @@ constexpr int staged_ctas_per_sm(int mode, int nt, int g, int v) {
                      : (nt <= 128) ? most
                      : (mode == 1) ? (nt <= 256 ? 3 : nt <= 384 ? 2 : 1)
                      : (mode == 0) ? (nt <= 192 ? 3 : nt <= 256 ? 2 : 1)
-                                   : (nt <= 256 ? 2 : 1);
+                                   : (nt <= 192 ? most : nt <= 256 ? 2 : 1);
     return want < most ? want : most;
 }
 
