@@ -5,7 +5,7 @@
 // from a precomputed table or computed on the fly).
 //
 // Vectorised shapes (Dh % 16 == 0, 16-byte aligned, up to 32 rotation units
-// per head) of at least 128 tokens run warp-wide: a warp takes one token (or one of up to eight parts
+// per head) run warp-wide: a warp takes one token (or one of up to eight parts
 // of it, when there are fewer tokens than warps), each lane owns one rotation
 // unit -- 8 pairs, two 16-byte vectors, in the rotate-half layout; 4 pairs,
 // one vector, interleaved -- of 32 / units heads at a time, and computes (or
@@ -54,7 +54,6 @@ constexpr int ROPE_CTAS_PER_SM = 4;
 // in flight per lane.  Measured against three CTAs with two heads: +21 % at
 // 4096 tokens, +6 % at 8192, +3 % at 16384, -1 % at 65536.
 constexpr int ROPE_WARP_CTAS_PER_SM = 2;
-constexpr int64_t ROPE_WARP_MIN_TOKENS = 128;
 constexpr int ROPE_HEADS_PER_BATCH = 4;   // heads whose loads a lane keeps in flight
 constexpr int ROPE_MAX_DH = 1024;
 constexpr int ROPE_TOKENS_PER_ITER = 4;  // tokens a CTA handles between barriers
@@ -357,11 +356,9 @@ template <typename T, bool INTERLEAVED>
 cudaError_t launch_rope_t(const RopeArgs &a, bool vec, int sm, cudaStream_t s) {
     const int64_t resident = (int64_t)sm * ROPE_CTAS_PER_SM;
     const int units = INTERLEAVED ? a.Dh / 8 : a.Dh / 16;  // rotation units per head
-    // A warp computes its lanes' cos/sin one pair after another (a dependent
-    // chain of 4-8 sincosf): with a handful of tokens that latency shows
-    // (8 tokens: +1.7 us), so decode-sized calls keep the CTA-wide kernel,
-    // whose 256 threads compute a group's table side by side.
-    if (vec && units <= 32 && a.T >= ROPE_WARP_MIN_TOKENS) {
+    // At every token count: replayed from a CUDA graph, 8 tokens take 3.3 us
+    // here against 5.1 us with the CTA-wide kernel (1 token: 3.2 us either).
+    if (vec && units <= 32) {
         // warps per token: spread a few tokens over more warps (up to 8)
         const int64_t resident_w = (int64_t)sm * ROPE_WARP_CTAS_PER_SM;
         const int64_t warps = resident_w * (ROPE_NT / 32);

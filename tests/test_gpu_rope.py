@@ -78,14 +78,15 @@ def test_rope_decode_and_prefill(T, interleaved, dtype):
     _run_and_check(q, k, v, kc, vc, pos, slots, base=500000.0, interleaved=interleaved)
 
 
-# Shapes of the warp-wide kernel (128 tokens or more, Dh % 16 == 0, up to 32
-# rotation units per head): units per head that do not divide 32 (Dh = 80:
-# five), exactly 32 (rotate-half Dh = 512, interleaved Dh = 256), past it
-# (interleaved Dh = 512: the CTA-wide kernel), and token counts that spread a
-# token over several warps (300) or one warp (1000 with few heads).
+# Shapes of the warp-wide kernel (Dh % 16 == 0, up to 32 rotation units per
+# head): units per head that do not divide 32 (Dh = 80: five), exactly 32
+# (rotate-half Dh = 512, interleaved Dh = 256), past it (interleaved Dh = 512
+# and Dh = 1024: the CTA-wide kernel), and token counts that spread a token
+# over several warps (300, 40) or one warp (1000 with few heads).
 @pytest.mark.parametrize("T,Hq,Hkv,Dh", [(300, 8, 2, 64), (1000, 4, 1, 80), (300, 6, 3, 128),
-                                         (130, 2, 2, 256), (129, 3, 1, 512)],
-                         ids=["t300_d64", "t1000_d80", "t300_d128", "t130_d256", "t129_d512"])
+                                         (130, 2, 2, 256), (129, 3, 1, 512), (40, 2, 1, 1024)],
+                         ids=["t300_d64", "t1000_d80", "t300_d128", "t130_d256", "t129_d512",
+                              "t40_d1024"])
 @pytest.mark.parametrize("interleaved", [False, True], ids=["half", "interleaved"])
 @pytest.mark.parametrize("use_table", [False, True], ids=["computed", "table"])
 def test_rope_warp_kernel_shapes(T, Hq, Hkv, Dh, interleaved, use_table):
