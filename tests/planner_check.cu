@@ -1,0 +1,36 @@
+// planner_check.cu -- prints the dispatch plan for a grid of problems, one
+// line per problem, for tests/test_planner_cpu.py.  Host code only: it runs
+// without a GPU (make_plan is a pure function of its arguments).
+//
+// Output: the staged configuration table ("cfg index nt g v max_nv"), then
+// per problem: mode esize D rows tier cfg nt g v max_nv stages tile_rows
+// num_tiles grid smem stage_bytes max_ctas
+#include <cstdio>
+
+#include "planner.h"
+
+int main() {
+    using namespace rmsn;
+    const int sm = 152;
+    const int Ds[] = {8, 16, 64, 120, 128, 256, 264, 512, 520, 640, 768, 1000, 1024, 1032, 1536, 2048,
+                      2056, 3072, 4096, 4104, 6144, 8192, 8200, 12288, 16384, 16392, 32768, 65536};
+    const long long rows_list[] = {1, 8, 9, 64, 300, 4096, 16384, 131072, 3000000000LL};
+    for (int ci = 0; ci < N_STAGED_CFG; ++ci)
+        std::printf("cfg %d %d %d %d %d\n", ci, STAGED_CFGS[ci].nt, STAGED_CFGS[ci].g,
+                    STAGED_CFGS[ci].v, STAGED_CFGS[ci].max_nv);
+    for (int mode = 0; mode < 4; ++mode)
+        for (int esize : {2, 4})
+            for (int D : Ds)
+                for (long long rows : rows_list) {
+                    const Plan p = planner::make_plan(mode, rows, D, esize, true, sm);
+                    int max_nv = 0, max_ctas = 0;
+                    if (p.tier == TIER_STAGED) {
+                        max_nv = STAGED_CFGS[p.cfg].max_nv;
+                        max_ctas = staged_max_ctas_per_sm(mode, p.nt, p.g, p.v);
+                    }
+                    std::printf("%d %d %d %lld %d %d %d %d %d %d %d %d %lld %d %zu %u %d\n", mode, esize,
+                                D, rows, p.tier, p.cfg, p.nt, p.g, p.v, max_nv, p.stages, p.tile_rows,
+                                (long long)p.num_tiles, p.grid, p.smem, p.stage_bytes, max_ctas);
+                }
+    return 0;
+}
