@@ -112,3 +112,43 @@ def test_last_cuda_error_is_per_thread():
     t.start()
     t.join()
     assert seen == [0]
+
+
+def test_graph_capture_of_strided_calls_with_tensor_maps():
+    """Rows a stride apart through the tensor-map path (sub-warp tiles) and the
+    per-row scale, captured in a graph: the maps are encoded at capture time
+    and the replays give the eager results bit for bit."""
+    rows, D = 4000, 512
+    c = W.random_case(rows, D, torch.bfloat16, seed=5)
+    buf = torch.cat([c.x, c.residual], dim=1).to(DEV)
+    x, res, w, g = buf[:, :D], buf[:, D:], c.w.to(DEV), c.g.to(DEV)
+    obuf = torch.empty(rows, 2 * D, dtype=torch.bfloat16, device=DEV)
+
+    def step(o):
+        out, nr = o[0][:, :D], o[0][:, D:]
+        rn.rmsnorm_fwd_ex(x, w, c.eps, 1.0, res, out=out, new_residual=nr, rstd=o[1])
+        rn.rmsnorm_vjp_ex(nr, w, g, c.eps, 1.0, res, rstd=o[1], gx=o[2][:, :D], gw=o[3])
+
+    eager = [obuf.clone(), torch.empty(rows, device=DEV),
+             torch.empty(rows, 2 * D, dtype=torch.bfloat16, device=DEV),
+             torch.empty(D, device=DEV)]
+    step(eager)
+    torch.cuda.synchronize()
+    outs = [torch.empty_like(t) for t in eager]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(outs)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(outs)
+    for t in outs:
+        t.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], eager[0])
+    assert torch.equal(outs[1].view(torch.int32), eager[1].view(torch.int32))
+    assert torch.equal(outs[2][:, :D], eager[2][:, :D])
+    assert torch.equal(outs[3].view(torch.int32), eager[3].view(torch.int32))
