@@ -71,7 +71,7 @@ cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t s
 
 template <typename T, int MODE>
 cudaError_t launch_staged_mode(const Plan &p, const KernelArgs &a, cudaStream_t s) {
-    static_assert(N_STAGED_CFG == 15, "keep this switch in step with STAGED_CFGS");
+    static_assert(N_STAGED_CFG == 19, "keep this switch in step with STAGED_CFGS");
     switch (p.cfg) {
         case 0: return launch_staged_one<T, MODE, 256, 8, 1>(p, a, s);
         case 1: return launch_staged_one<T, MODE, 256, 16, 1>(p, a, s);
@@ -90,6 +90,10 @@ cudaError_t launch_staged_mode(const Plan &p, const KernelArgs &a, cudaStream_t 
         case 12: return launch_staged_one<T, MODE, 192, 192, 2>(p, a, s);
         case 13: return launch_staged_one<T, MODE, 384, 384, 2>(p, a, s);
         case 14: return launch_staged_one<T, MODE, 768, 768, 2>(p, a, s);
+        case 15: return launch_staged_one<T, MODE, 160, 160, 2>(p, a, s);
+        case 16: return launch_staged_one<T, MODE, 224, 224, 2>(p, a, s);
+        case 17: return launch_staged_one<T, MODE, 320, 320, 2>(p, a, s);
+        case 18: return launch_staged_one<T, MODE, 448, 448, 2>(p, a, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -66,7 +66,7 @@ struct Plan {
 struct StagedCfg { int nt, g, v, max_nv; };
 struct DirectCfg { int nt, v, max_nv; };
 
-constexpr int N_STAGED_CFG = 15;
+constexpr int N_STAGED_CFG = 19;
 constexpr StagedCfg STAGED_CFGS[N_STAGED_CFG] = {
     // sub-warp / warp per row (shuffle-only reductions), 256 threads
     {256, 8, 1, 8}, {256, 16, 1, 16}, {256, 32, 1, 32},
@@ -80,6 +80,8 @@ constexpr StagedCfg STAGED_CFGS[N_STAGED_CFG] = {
     // bf16), which the power-of-two CTAs above fit with a quarter of their
     // threads idle
     {96, 96, 2, 192}, {192, 192, 2, 384}, {384, 384, 2, 768}, {768, 768, 2, 1536},
+    // and for rows of 5 * 2^k and 7 * 2^k vectors (D = 2560, 5120; 3584, 7168)
+    {160, 160, 2, 320}, {224, 224, 2, 448}, {320, 320, 2, 640}, {448, 448, 2, 896},
 };
 constexpr int STAGED_CFG_WIDE = 10;
 
@@ -89,41 +91,44 @@ constexpr DirectCfg DIRECT_CFGS[N_DIRECT_CFG] = {
 };
 
 // Most CTAs of a staged configuration that can share one SM, as the kernels'
-// __launch_bounds__ promise it (registers per thread capped to fit):
-// CTA-per-row forwards with two vectors per thread: 6 of up to 128 threads,
-// 3 of up to 256 (85 registers), 2 of 384 (85); CTA-per-row VJPs with two
-// vectors: 6 of 96 threads (113), 4 of 128 (128), 3 of 192 (113); other CTAs of up to 256
-// threads 2 (128 registers; the sub-warp VJP with three or four vectors per
-// lane fits by re-reading rows from shared memory); larger CTAs 1.
+// __launch_bounds__ promise it (registers per thread capped to fit).
+// CTA-per-row forwards with two vectors per thread (about 80 registers):
+// 6 of up to 128 threads, 3 of up to 256, 2 of up to 448.  CTA-per-row VJPs
+// with two vectors (about 110 registers): 6 of 96 threads, 4 of 128, 3 of up
+// to 192, 2 of up to 320.  Other CTAs of up to 256 threads 2 (128 registers;
+// the sub-warp VJP with three or four vectors per lane fits by re-reading
+// rows from shared memory); larger CTAs 1.
 constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
     return (g == nt && mode < 2 && nt <= 128 && v <= 2)    ? 6
            : (g == nt && mode < 2 && nt <= 256 && v <= 2)  ? 3
-           : (g == nt && mode < 2 && nt <= 384 && v <= 2)  ? 2
+           : (g == nt && mode < 2 && nt <= 448 && v <= 2)  ? 2
            : (g == nt && mode >= 2 && nt <= 96 && v <= 2)  ? 6
            : (g == nt && mode >= 2 && nt <= 128 && v <= 2) ? 4
            : (g == nt && mode >= 2 && nt <= 192 && v <= 2) ? 3
            : (nt <= 256)                                   ? 2
+           : (g == nt && mode >= 2 && nt <= 320 && v <= 2) ? 2
                                                             : 1;
 }
 // CTAs per SM the plan uses unless tuned otherwise, from sweeps of 1-6 on
 // GB300 (bf16, rotating buffers, 8192-32768 rows).  CTA-per-row shapes:
 //   * up to 128 threads: as many as fit (D = 2048 forward 5697 -> 6442 GB/s,
 //     VJP 3522 -> 5814 against two);
-//   * the forward without a residual (mode 1): three of 192 or 256 threads
-//     (D = 3072: 4486 -> 5622), two of 384;
-//   * the forward with a residual (mode 0): three of 192 threads, two of 256
-//     (D = 4096: 6394 against 6221 with three), one of 384 or more, whose
-//     ring is then deep enough (D = 6144: 6575 against 6134 with two);
-//   * the VJP: three of 192 threads (D = 3072: 5032 -> 5294 against two),
-//     two of 256, one above.
+//   * the forward without a residual (mode 1): three of up to 256 threads
+//     (D = 3072: 4486 -> 5622), two of up to 448 (D = 7168: 4197 -> 5853);
+//   * the forward with a residual (mode 0): three of up to 192 threads, two
+//     of 224-320 (D = 4096: 6394 against 6221 with three) and of 448 (D =
+//     7168: 6259 against 6152), one of 384 (D = 6144: 6566 against 6144 with
+//     two, whose rings are then only two stages deep) and of 512 or more;
+//   * the VJP: as many as fit up to 192 threads (D = 3072: 5032 -> 5294
+//     against two), two of up to 320 (D = 5120: 3714 -> 5767), one above.
 // Sub-warp shapes: two, or one where only one fits.
 constexpr int staged_ctas_per_sm(int mode, int nt, int g, int v) {
     const int most = staged_max_ctas_per_sm(mode, nt, g, v);
     const int want = (g != nt)    ? 2
                      : (nt <= 128) ? most
-                     : (mode == 1) ? (nt <= 256 ? 3 : nt <= 384 ? 2 : 1)
-                     : (mode == 0) ? (nt <= 192 ? 3 : nt <= 256 ? 2 : 1)
-                                   : (nt <= 192 ? most : nt <= 256 ? 2 : 1);
+                     : (mode == 1) ? (nt <= 256 ? 3 : nt <= 448 ? 2 : 1)
+                     : (mode == 0) ? (nt <= 192 ? 3 : (nt <= 320 || nt == 448) ? 2 : 1)
+                                   : (nt <= 192 ? most : nt <= 320 ? 2 : 1);
     return want < most ? want : most;
 }
 

@@ -13,7 +13,8 @@ int main() {
     using namespace rmsn;
     const int sm = 152;
     const int Ds[] = {8, 16, 64, 120, 128, 256, 264, 512, 520, 640, 768, 1000, 1024, 1032, 1536, 2048,
-                      2056, 3072, 4096, 4104, 6144, 8192, 8200, 12288, 16384, 16392, 32768, 65536};
+                      2056, 2560, 3072, 3584, 4096, 4104, 5120, 6144, 7168, 8192, 8200, 10240,
+                      12288, 14336, 16384, 16392, 32768, 65536};
     const long long rows_list[] = {1, 8, 9, 64, 300, 4096, 16384, 131072, 3000000000LL};
     for (int ci = 0; ci < N_STAGED_CFG; ++ci)
         std::printf("cfg %d %d %d %d %d\n", ci, STAGED_CFGS[ci].nt, STAGED_CFGS[ci].g,

@@ -32,7 +32,8 @@ def _rstd_close(name, got, want):
 # (rows, D): staged sub-warp (64, 264), staged CTA per row (1024 .. 8192 in
 # fp32), direct (rows <= 8, and fp32 rows past the staged limit), generic (odd D)
 FP32_SHAPES = [(4096, 4096), (2048, 8192), (1000, 64), (777, 264), (300, 1024), (5, 4096),
-               (1, 512), (64, 1001), (40, 12288), (9, 40000)]
+               (1, 512), (64, 1001), (40, 12288), (9, 40000), (333, 1280), (129, 1792), (65, 2560),
+               (33, 3584)]
 
 
 @pytest.mark.parametrize("rows,D", FP32_SHAPES, ids=["r%d_d%d" % s for s in FP32_SHAPES])

@@ -47,7 +47,8 @@ def test_fused_vjp_prefill(D):
 
 
 EDGE = [(1, 64), (3, 4096), (8, 8192), (9, 264), (300, 520), (1000, 1024), (157, 2048),
-        (77, 33), (5, 1001), (11, 40000), (153, 16384), (263, 3072), (67, 12288), (99, 1536)]
+        (77, 33), (5, 1001), (11, 40000), (153, 16384), (263, 3072), (67, 12288), (99, 1536),
+        (201, 2560), (109, 3584), (87, 5120), (45, 7168)]
 
 
 @pytest.mark.parametrize("rows,D", EDGE, ids=["r%d_d%d" % e for e in EDGE])

@@ -132,6 +132,8 @@ EDGE = [
     # CTA-per-row configurations that fit rows of 3 * 2^k vectors exactly
     # (96, 192, 384 and 768 threads), at and just past their widths
     (301, 1536), (257, 3072), (263, 2056), (97, 6144), (131, 12288), (35, 8200),
+    # ... and of 5 * 2^k and 7 * 2^k vectors (160, 224, 320 and 448 threads)
+    (311, 2560), (229, 3584), (151, 5120), (93, 7168), (41, 10240), (39, 14336),
 ]
 
 
