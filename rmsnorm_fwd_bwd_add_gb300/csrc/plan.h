@@ -90,14 +90,33 @@ constexpr DirectCfg DIRECT_CFGS[N_DIRECT_CFG] = {
     {128, 1, 128}, {256, 1, 256}, {512, 1, 512}, {512, 2, 1024}, {1024, 2, 2048}, {1024, 4, 4096},
 };
 
+// Whether a VJP instance re-reads its rows from the stage for its outputs
+// instead of holding them in registers across the reduction (the stage stays
+// resident until the tile is done).  That is a second pass over shared memory
+// for fewer registers, and it pays where it buys CTAs or removes spills
+// (bf16 VJP, rotating buffers, GB300):
+//   * sub-warp tiles with three or four vectors per lane: 128 registers, two
+//     CTAs per SM instead of one (D = 640: 4370 -> 5484 GB/s);
+//   * CTAs of 384 and 448 threads: about 80 registers, two CTAs per SM
+//     instead of one (D = 6144: 5341 -> 5983, D = 7168: 5297 -> 5527);
+//   * CTAs of 768 and 1024 threads, whose register cap (80, 64) spilled
+//     (D = 12288: 4641 -> 5978, D = 16384: 3670 -> 6010).
+// Elsewhere it loses: 224-320 threads with three CTAs per SM instead of two
+// (D = 4096: 5746 against 5902), 512 threads with two instead of one (D =
+// 8192: 5882 against 6229).
+__host__ __device__ constexpr bool staged_reload(int mode, int nt, int g, int v) {
+    return mode >= 2 && (g != nt ? v >= 3 : (nt == 384 || nt == 448 || nt >= 768));
+}
+
 // Most CTAs of a staged configuration that can share one SM, as the kernels'
 // __launch_bounds__ promise it (registers per thread capped to fit).
 // CTA-per-row forwards with two vectors per thread (about 80 registers):
 // 6 of up to 128 threads, 3 of up to 256, 2 of up to 448.  CTA-per-row VJPs
 // with two vectors (about 110 registers): 6 of 96 threads, 4 of 128, 3 of up
-// to 192, 2 of up to 320.  Other CTAs of up to 256 threads 2 (128 registers;
-// the sub-warp VJP with three or four vectors per lane fits by re-reading
-// rows from shared memory); larger CTAs 1.
+// to 192, 2 of up to 320, and 2 of 384 or 448 threads, which re-read their
+// rows.  Other CTAs of up to 256 threads 2 (128 registers; the sub-warp VJP
+// with three or four vectors per lane fits by re-reading rows from shared
+// memory); larger CTAs 1.
 constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
     return (g == nt && mode < 2 && nt <= 128 && v <= 2)    ? 6
            : (g == nt && mode < 2 && nt <= 256 && v <= 2)  ? 3
@@ -107,6 +126,7 @@ constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
            : (g == nt && mode >= 2 && nt <= 192 && v <= 2) ? 3
            : (nt <= 256)                                   ? 2
            : (g == nt && mode >= 2 && nt <= 320 && v <= 2) ? 2
+           : (g == nt && staged_reload(mode, nt, g, v) && nt <= 448) ? 2
                                                             : 1;
 }
 // CTAs per SM the plan uses unless tuned otherwise, from sweeps of 1-6 on
@@ -120,7 +140,7 @@ constexpr int staged_max_ctas_per_sm(int mode, int nt, int g, int v) {
 //     7168: 6259 against 6152), one of 384 (D = 6144: 6566 against 6144 with
 //     two, whose rings are then only two stages deep) and of 512 or more;
 //   * the VJP: as many as fit up to 192 threads (D = 3072: 5032 -> 5294
-//     against two), two of up to 320 (D = 5120: 3714 -> 5767), one above.
+//     against two), two of up to 448 (D = 5120: 3714 -> 5767), one above.
 // Sub-warp shapes: two, or one where only one fits.
 constexpr int staged_ctas_per_sm(int mode, int nt, int g, int v) {
     const int most = staged_max_ctas_per_sm(mode, nt, g, v);
@@ -128,7 +148,7 @@ constexpr int staged_ctas_per_sm(int mode, int nt, int g, int v) {
                      : (nt <= 128) ? most
                      : (mode == 1) ? (nt <= 256 ? 3 : nt <= 448 ? 2 : 1)
                      : (mode == 0) ? (nt <= 192 ? 3 : (nt <= 320 || nt == 448) ? 2 : 1)
-                                   : (nt <= 192 ? most : nt <= 320 ? 2 : 1);
+                                   : (nt <= 192 ? most : nt <= 448 ? 2 : 1);
     return want < most ? want : most;
 }
 

@@ -55,13 +55,10 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     // Tiles of several rows a stride apart take one copy per row, spread over
     // the CTA's threads; a CTA-per-row tile is always a single copy.
     constexpr bool SPREAD_COPIES = GEN && !CTA_ROW;
-    // The sub-warp VJP with three or four vectors per lane re-reads a row from
-    // the stage (still resident until the tile is done) for its outputs
-    // instead of holding it in registers across the reduction: 128 registers,
-    // two CTAs per SM instead of one.  So do CTA-per-row VJPs of 768 or more
-    // threads, whose register cap (80, 64) would otherwise spill; a row's
-    // stage is released only at the next row's barrier.
-    constexpr bool RELOAD = is_vjp(MODE) && (CTA_ROW ? NT >= 768 : V >= 3);
+    // Some VJP instances re-read a row from the stage for their outputs
+    // instead of holding it in registers across the reduction (a CTA-per-row
+    // stage is released only at the next row's barrier).
+    constexpr bool RELOAD = staged_reload(MODE, NT, G, V);
     constexpr int NTENS = input_tensors(MODE);
     constexpr bool VJP = is_vjp(MODE);
     constexpr bool ADD = (MODE == MODE_VJP_ADD);
