@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
     const int NV = D / E;
     const float eps = a.eps;
     const float wb = a.weight_bias;
-    const float Df = (float)D;
+    const float inv_D = 1.0f / (float)D;  // per-row means by product
     const uint4 *in0 = static_cast<const uint4 *>(a.in0);
     const uint4 *in1 = static_cast<const uint4 *>(a.in1);
     const uint4 *in2 = static_cast<const uint4 *>(a.in2);
@@ -110,13 +110,13 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
             ss += red[it & 1][w][0];
             if constexpr (VJP) dot += red[it & 1][w][1];
         }
-        float r = rsqrtf(ss / Df + eps);
+        float r = rsqrtf(ss * inv_D + eps);
         if constexpr (VJP) {
             if (a.rstd) r = r_saved;
         } else {
             if (a.rstd && tid == 0) a.rstd[row] = r;
         }
-        const float c = (r * r) * (dot / Df);
+        const float c = (r * r) * (dot * inv_D);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = tid + j * NT;

@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a)
     const int D = a.D;
     const float eps = a.eps;
     const float wb = a.weight_bias;
-    const float Df = (float)D;
+    const float inv_D = 1.0f / (float)D;  // per-row means by product
     const T *in0 = static_cast<const T *>(a.in0);
     const T *in1 = static_cast<const T *>(a.in1);
     const T *in2 = static_cast<const T *>(a.in2);
@@ -90,13 +90,13 @@ __global__ void __launch_bounds__(GENERIC_NT) generic_kernel(const KernelArgs a)
             ss += red[it & 1][k][0];
             if constexpr (VJP) dot += red[it & 1][k][1];
         }
-        float r = rsqrtf(ss / Df + eps);
+        float r = rsqrtf(ss * inv_D + eps);
         if constexpr (VJP) {
             if (a.rstd) r = a.rstd[row];
         } else {
             if (a.rstd && tid == 0) a.rstd[row] = r;
         }
-        const float cc = (r * r) * (dot / Df);
+        const float cc = (r * r) * (dot * inv_D);
         T *o_row = out0 + row * lo0;
         for (int c = tid; c < D; c += NT) {
             const float x = Cvt<T>::load1(x_row + c);

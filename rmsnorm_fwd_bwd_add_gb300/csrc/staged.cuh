@@ -48,6 +48,7 @@ namespace rmsn {
 template <typename T, int MODE, int NT, int G, int V, int MINB, bool GEN>
 __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant__ KernelArgs a) {
     constexpr int NWARPS = NT / 32;
+    constexpr int WP = NWARPS <= 4 ? 4 : NWARPS <= 8 ? 8 : NWARPS <= 16 ? 16 : 32;
     constexpr int NG = NT / G;  // rows processed side by side
     constexpr int VP = vec_pairs<T>();   // float2 pairs per 16-byte vector
     constexpr int EPV = vec_elems<T>();  // elements per 16-byte vector
@@ -85,7 +86,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     const int64_t grid = gridDim.x;
     const int64_t nk = (a.num_tiles - (int64_t)blockIdx.x + grid - 1) / grid;  // >= 1
     const float eps = a.eps;
-    const float Df = (float)D;  // exact: D <= 2^24
+    // 1/D once per CTA: the per-row means are products, not divisions (exact
+    // for D a power of two; within an ulp of the quotient otherwise).
+    const float inv_D = 1.0f / (float)D;
 
     const T *in0 = static_cast<const T *>(a.in0);
     const T *in1 = static_cast<const T *>(a.in1);
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                            float dot) {
         const size_t base0 = (size_t)(row * lo0), base1 = (size_t)(row * lo1);
         const float2 rr = make_float2(r, r);
-        const float c = (r * r) * (dot / Df);  // r^2 * dot / D
+        const float c = (r * r) * (dot * inv_D);  // r^2 * dot / D
         const float2 nc2 = make_float2(-c, -c);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
@@ -361,10 +364,14 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                 return;
             }
             if (tid == 0 && k >= 1 && issued < nk) issue_next();
-            float2 tot = lane < NWARPS ? rb[lane] : make_float2(0.f, 0.f);
-            tot.x = group_sum<32>(tot.x);
-            if constexpr (VJP) tot.y = group_sum<32>(tot.y);
-            float r = rsqrtf(tot.x / Df + eps);
+            // Each group of WP lanes (the warp count rounded up to a power of
+            // two) sums all warp totals: the same sums a 32-lane tree with
+            // zeros past NWARPS gives, in log2(WP) shuffle levels.
+            const int wl = lane & (WP - 1);
+            float2 tot = wl < NWARPS ? rb[wl] : make_float2(0.f, 0.f);
+            tot.x = group_sum<WP>(tot.x);
+            if constexpr (VJP) tot.y = group_sum<WP>(tot.y);
+            float r = rsqrtf(tot.x * inv_D + eps);
             if constexpr (GEN && VJP) {
                 if (a.rstd) r = r_saved;
             } else if constexpr (GEN) {
@@ -405,7 +412,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                 sa = group_sum<G>(sa);
                 if constexpr (VJP) sb = group_sum<G>(sb);
                 if (valid && ok) {
-                    float r = rsqrtf(sa / Df + eps);
+                    float r = rsqrtf(sa * inv_D + eps);
                     if constexpr (GEN && VJP) {
                         if (a.rstd) r = r_saved;
                     } else if constexpr (GEN) {
