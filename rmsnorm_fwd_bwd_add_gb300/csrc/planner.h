@@ -140,7 +140,14 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
         // One row per tile, the whole CTA on it.  The requested CTAs per SM
         // when each CTA's share of shared memory holds its stages (two with
         // three or more CTAs, three with two), fewer otherwise, down to one
-        // CTA with at least two; the depth then follows the in-flight target.
+        // CTA with at least two; the depth then follows the in-flight target,
+        // but is at least three stages, where they fit, with one CTA per SM
+        // and for the VJP.  A stage is refilled only after the next row's
+        // barrier, so two stages leave nothing in flight while a row is read
+        // and reduced (bf16, rotating: forward D = 12288 5781 -> 6251 GB/s,
+        // 16384 5907 -> 6168; fused VJP D = 12288 5700 -> 6264, and with two
+        // CTAs per SM D = 6144 6045 -> 6231).  The forwards with two or more
+        // CTAs per SM keep two (D = 7168: 6230 against 6081 with three).
         p->tile_rows = 1;
         p->stage_bytes = (uint32_t)row_bytes;
         const size_t per_stage = (size_t)ntens * row_bytes;
@@ -149,10 +156,11 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
             const int64_t sc = (int64_t)(smem_per_cta(c) / per_stage);
             if (sc >= (c >= 3 ? 2 : c == 2 ? 3 : 2)) {
                 chosen = c;
-                p->stages = (int)std::min<int64_t>(std::min<int64_t>(max_stages, sc),
-                                                   ring_stages(is_vjp(mode) ? INFLIGHT_VJP
-                                                                            : INFLIGHT_FWD,
-                                                               per_stage, c));
+                const int floor = tu.stages ? 0 : (c == 1 || is_vjp(mode)) ? 3 : 2;
+                p->stages = (int)std::min<int64_t>(
+                    std::min<int64_t>(max_stages, sc),
+                    std::max(floor, ring_stages(is_vjp(mode) ? INFLIGHT_VJP : INFLIGHT_FWD,
+                                                per_stage, c)));
             }
         }
         if (!chosen) return false;
