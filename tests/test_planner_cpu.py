@@ -94,3 +94,44 @@ def test_plan_is_a_pure_function(plans, tmp_path):
     _, rows = plans
     again = {tuple(r[:4]): r[4:] for r in rows}
     assert len(again) == len(rows)  # one plan per (mode, esize, D, rows)
+
+
+def _smem_share(cps):
+    """Shared memory one CTA may take when `cps` CTAs share an SM (the planner's budget)."""
+    return {1: 225 * 1024, 2: 110 * 1024, 3: 72 * 1024}.get(cps, 224 * 1024 // max(cps, 1) - 2048)
+
+
+def test_ring_depth_floor(plans):
+    """CTA-per-row plans keep at least three stages where they fit when they run one CTA per
+    SM or are VJPs: a stage is refilled only after the next row's barrier, so two leave nothing
+    in flight while a row is read."""
+    _, rows = plans
+    n = 0
+    for (mode, es, D, R, tier, cfg, nt, g, v, max_nv, stages, tr, ntiles, grid, smem, sb,
+         max_ctas) in rows:
+        if tier != 0 or g != nt or R < 16384:
+            continue
+        cps = grid // SM
+        ntens = 1 if mode == 1 else 3 if mode == 3 else 2
+        if (cps == 1 or mode >= 2) and _smem_share(cps) // (ntens * sb) >= 3:
+            n += 1
+            assert stages >= 3, (mode, es, D, R, cps, stages)
+    assert n > 50
+
+
+def test_reread_vjp_ctas_per_sm(plans):
+    """The VJP instances that re-read their rows from the stage (384 and 448 threads) run two
+    CTAs per SM; the 512-thread VJP, which holds its rows, runs one."""
+    _, rows = plans
+    seen = set()
+    for (mode, es, D, R, tier, cfg, nt, g, v, max_nv, stages, tr, ntiles, grid, smem, sb,
+         max_ctas) in rows:
+        if tier != 0 or g != nt or mode < 2:
+            continue
+        if nt in (384, 448):
+            assert max_ctas == 2, (mode, es, D, nt)
+            seen.add(nt)
+        if nt == 512:
+            assert max_ctas == 1, (mode, es, D, nt)
+            seen.add(nt)
+    assert seen == {384, 448, 512}
