@@ -23,9 +23,11 @@
 // last base and Dh) and split into a hi + lo pair of floats passed with the
 // launch; per token p * (hi + lo) is formed as a double-float
 // (an exact product error from fmaf), reduced modulo 2 pi with 2 pi split in
-// two floats (Cody-Waite reduction), and sincosf takes the reduced angle:
-// about 1e-8 rad of error at p = 1e6, where a plain float product is off by
-// up to 0.06 rad.
+// two floats (Cody-Waite reduction): about 1e-8 rad of error at p = 1e6,
+// where a plain float product is off by up to 0.06 rad.  The reduced angle
+// lies in [-pi, pi], where the SFU's sine and cosine (__sincosf) are within
+// about 2^-21 absolute; they replace sincosf, whose instruction count sat on
+// every token's critical path (65536 tokens: 5869 -> 6142 GB/s).
 //
 // Device data is validated: a position outside the table (or negative) or a
 // slot past the cache sets RMSNORM_DEVSTATUS_BAD_INDEX and that token's
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(ROPE_NT, ROPE_WARP_CTAS_PER_SM) rope_warp_kern
 #pragma unroll
                 for (int m = 0; m < PPU; ++m) {
                     const float2 f = s_inv[i0 + m];
-                    sincosf(reduced_angle(p, f.x, f.y), &cs[m].y, &cs[m].x);
+                    __sincosf(reduced_angle(p, f.x, f.y), &cs[m].y, &cs[m].x);
                 }
             }
             const int step = wpt * hpi;
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(ROPE_NT, ROPE_CTAS_PER_SM) rope_kv_kernel(cons
                     c = a.cos_sin[p * Dh + i];
                     sn = a.cos_sin[p * Dh + half + i];
                 } else {
-                    sincosf(reduced_angle(p, a.inv[i].x, a.inv[i].y), &sn, &c);
+                    __sincosf(reduced_angle(p, a.inv[i].x, a.inv[i].y), &sn, &c);
                 }
                 cs[j][i] = make_float2(c, sn);
             }

@@ -78,6 +78,20 @@ def test_rope_decode_and_prefill(T, interleaved, dtype):
     _run_and_check(q, k, v, kc, vc, pos, slots, base=500000.0, interleaved=interleaved)
 
 
+@pytest.mark.parametrize("interleaved", [False, True], ids=["half", "interleaved"])
+def test_rope_far_positions(interleaved):
+    """Computed angles at positions 10^6 - 1.6 * 10^7: the product p * base^(-2i/Dh) is formed
+    as a double-float and reduced modulo 2 pi before the SFU sine and cosine, which are accurate
+    only near [-pi, pi]; a plain float product would be off by up to 0.06 rad here."""
+    T, Hq, Hkv, Dh = 64, 8, 2, 128
+    S = T
+    q, k, v, kc, vc = _inputs(T, Hq, Hkv, Dh, S, torch.float16, 77 + interleaved)
+    rng = np.random.default_rng(5)
+    pos = rng.integers(1_000_000, 16_000_000, size=T).tolist()
+    slots = rng.permutation(S)[:T].tolist()
+    _run_and_check(q, k, v, kc, vc, pos, slots, base=500000.0, interleaved=interleaved)
+
+
 # Shapes of the warp-wide kernel (Dh % 16 == 0, up to 32 rotation units per
 # head): units per head that do not divide 32 (Dh = 80: five), exactly 32
 # (rotate-half Dh = 512, interleaved Dh = 256), past it (interleaved Dh = 512
