@@ -130,7 +130,9 @@ int rmsnorm_fwd(const void *x, const void *residual, const void *w, float eps,
  * memory pool the library keeps per device (cudaMallocFromPoolAsync /
  * cudaFreeAsync; the pool holds on to freed memory for the next call);
  * allocation failure returns RMSNORM_ERR_NO_MEMORY.  No [rows, D] temporary
- * is ever allocated.
+ * is ever allocated.  A call that runs as a single CTA (one row) writes its one
+ * partial row straight into gw when gw is 16-byte aligned: no scratch, one
+ * kernel, the same bits.
  */
 int rmsnorm_vjp(const void *x, const void *w, const void *g, float eps,
                 float weight_bias, void *gx, float *gw, int64_t rows, int64_t D,

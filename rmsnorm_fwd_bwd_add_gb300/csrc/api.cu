@@ -269,8 +269,16 @@ int vjp_prepare(const VjpOperands &o, float eps, float weight_bias, int64_t rows
     return RMSNORM_OK;
 }
 
+// A VJP launched as a single CTA (decode: one row) has one partial row, which
+// is gw itself: the kernel writes it in place, with no scratch and no second
+// kernel (the fixed-order sum of one row is that row, so the bits are the
+// same).  The tiers store partial rows as 16-byte vectors, so gw must be
+// 16-byte aligned for this; otherwise the two-stage path runs.
+bool gw_in_place(const Plan &p, const float *gw) { return p.grid == 1 && aligned16(gw); }
+
 int vjp_run(const VjpOperands &o, float eps, float weight_bias, int64_t rows, int64_t D,
             int dtype, const DevInfo &dev, const Plan &p, float *partials, cudaStream_t s) {
+    const bool in_place = gw_in_place(p, o.gw);
     KernelArgs a = base_args(dev, p, eps, weight_bias, rows, D);
     a.in0 = o.x.p;
     a.ld_in0 = o.x.ld;
@@ -282,10 +290,11 @@ int vjp_run(const VjpOperands &o, float eps, float weight_bias, int64_t rows, in
     a.out0 = const_cast<void *>(o.gx.p);
     a.ld_out0 = o.gx.ld;
     a.out1 = nullptr;
-    a.partials = partials;
+    a.partials = in_place ? o.gw : partials;
     a.rstd = const_cast<float *>(o.rstd);  // read only in the VJP kernels
     cudaError_t e = launch_plan(dtype, o.g_res.p ? MODE_VJP_ADD : MODE_VJP, p, a, s);
     if (e != cudaSuccess) return cuda_fail(e);
+    if (in_place) return RMSNORM_OK;
     e = launch_gw_reduce(partials, o.gw, p.grid, (int)D, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return RMSNORM_OK;
@@ -304,6 +313,8 @@ int vjp_pooled(const VjpOperands &o, float eps, float weight_bias, int64_t rows,
         cudaError_t e = cudaMemsetAsync(gw, 0, (size_t)D * sizeof(float), s);
         return e == cudaSuccess ? RMSNORM_OK : cuda_fail(e);
     }
+    if (gw_in_place(p, gw))
+        return vjp_run(o, eps, weight_bias, rows, D, dtype, dev, p, nullptr, s);
     cudaMemPool_t pool = nullptr;
     st = scratch_pool(&pool);
     if (st != RMSNORM_OK) return st;

@@ -156,6 +156,21 @@ def test_empty_rows():
     assert torch.all(gw == 0), "empty VJP must write gw = 0"
 
 
+@pytest.mark.parametrize("D", [64, 2048, 8192, 1001])
+def test_single_row_vjp_gw(D):
+    """One row runs as one CTA: with gw 16-byte aligned its partial row is written into gw in
+    place (no second kernel); with gw 4 bytes off the two-stage path runs.  The in-place result
+    matches the oracle, and the two paths give gw bit for bit."""
+    case = W.random_case(1, D, torch.bfloat16, seed=D, weight_bias=1.0, eps=1e-5)
+    check_vjp(case, case.x, conditioned=True)  # gw freshly allocated: aligned, in place
+    x, w, g = _dev(case.x), _dev(case.w), _dev(case.g)
+    gws = []
+    for off in (0, 1):
+        buf = torch.full((D + 4,), float("nan"), dtype=torch.float32, device=DEV)
+        gws.append(rn.rmsnorm_vjp(x, w, g, case.eps, case.weight_bias, gw=buf[off:off + D])[1])
+    assert torch.equal(gws[0].view(torch.int32), gws[1].view(torch.int32))
+
+
 def _offset_view(t, offset_elems=1):
     """Same values as t, stored one element past a 16-byte boundary."""
     buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=DEV)
