@@ -60,3 +60,26 @@ def test_step_bytes():
     assert bench.fwd_bytes(16384, 8192) == 1073758208
     assert bench.vjp_bytes(16384, 8192) == 805355520
     assert bench.STEP_BYTES == 536879104 + 402677760 + 1073758208 + 805355520
+
+
+def test_reference_arm_json_line(monkeypatch, capsys):
+    """Rank 0 of the reference arm prints one JSON line with the contract's keys.  The timed
+    oracle pass is stubbed (the oracle itself is checked by the pin tests); the sample sizing,
+    timing and line assembly run as they are."""
+    import json
+    import bench
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.setattr(bench, "oracle_pass", lambda sample: 10 ** 6)
+    assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3
+    assert line["unit"] == bench.UNIT and line["metric"] == bench.METRIC
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["value"] > 0
