@@ -41,6 +41,7 @@ ROWS = 16384
 DS = (4096, 8192)
 ITEM = 2  # bf16
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s HBM3e figure the target is quoted against
 
 
 def fwd_bytes(rows, D, residual=True, s=ITEM):
@@ -71,6 +72,12 @@ OPS = [("fwd_d%d" % D, D) for D in DS] + [("vjp_d%d" % D, D) for D in DS]
 OP_BYTES = {"fwd_d%d" % D: fwd_bytes(ROWS, D) for D in DS}
 OP_BYTES.update({"vjp_d%d" % D: vjp_bytes(ROWS, D) for D in DS})
 KERNELS_PER_STEP = 6  # two forward kernels, two VJP main kernels, two gw reductions
+
+# The POC workload (fp16, rows 8192, D 4096, x, w, g ~ U(0,1), eps 1e-5): its
+# VJP and the forward without a residual, timed per op beside the step.
+C3_ROWS, C3_D, C3_ITEM = 8192, 4096, 2
+C3_OPS = {"c3_vjp_f16": vjp_bytes(C3_ROWS, C3_D, C3_ITEM),
+          "c3_fwd_nores_f16": fwd_bytes(C3_ROWS, C3_D, residual=False, s=C3_ITEM)}
 
 CONFIG = {
     "workload": "prefill fused add-RMSNorm fwd (with residual) + RMSNorm VJP on new_residual, "
@@ -329,6 +336,86 @@ def time_device(step: Step, steps: int, warmup: int, sampler: ClockSampler):
     return total_ms, per_op_us, sampler.summary(t0, t1)
 
 
+def time_sustained(call, sets, reps=20, min_ms=1.0, warmup=10):
+    """µs per call under the sustained protocol: calls back to back over the
+    rotating `sets` (together at least twice the L2, so no call finds its
+    operands in L2), N calls per repetition (a multiple of len(sets), at least
+    `min_ms` of work), CUDA events on the launching stream, median of `reps`
+    repetitions.  Consecutive calls overlap their launch and prologue with the
+    previous call's tail, as they do in a user's loop."""
+    K = len(sets)
+    for i in range(max(warmup, K)):
+        call(sets[i % K])
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(K):
+        call(sets[i])
+    b.record()
+    torch.cuda.synchronize()
+    est_us = max(1.0, 1e3 * a.elapsed_time(b) / K)
+    calls = K * max(1, -(-int(1e3 * min_ms / est_us) // K))
+    times = []
+    for _ in range(reps):
+        a.record()
+        for i in range(calls):
+            call(sets[i % K])
+        b.record()
+        torch.cuda.synchronize()
+        times.append(1e3 * a.elapsed_time(b) / calls)
+    return statistics.median(times)
+
+
+def sets_for_l2(set_bytes: int, device) -> int:
+    """Rotating sets needed for at least twice the device's L2 in total."""
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    return max(1, -(-2 * l2 // set_bytes))
+
+
+def sustained_ops(step: "Step", device):
+    """Per-op µs per call under the sustained protocol for the step's four ops
+    (their own buffers: each op's operands are 0.4-1.1 GB, one set is already
+    more than twice the L2) and for the POC workload's VJP and forward without
+    a residual (fp16 8192 x 4096, two rotating sets)."""
+    import rmsnorm_fwd_bwd_add_gb300 as rn
+    from rmsnorm_fwd_bwd_add_gb300 import workloads as W
+    us = {}
+    for name, D in OPS:
+        t = step.t[D]
+        n_sets = sets_for_l2(OP_BYTES[name], device)
+        sets = [t] + [{k: torch.empty_like(v) if v.dim() == 2 else v for k, v in t.items()}
+                      for _ in range(n_sets - 1)]
+        for s_ in sets[1:]:
+            for k in ("x", "res", "g", "nr"):
+                s_[k].copy_(t[k])
+        if name.startswith("fwd"):
+            def call(s_, D=D):
+                rn.rmsnorm_fwd(s_["x"], s_["w"], step.eps[D], 0.0, s_["res"], out=s_["out"],
+                               new_residual=s_["nr"])
+        else:
+            def call(s_, D=D):
+                rn.rmsnorm_vjp(s_["nr"], s_["w"], s_["g"], step.eps[D], 0.0, gx=s_["gx"],
+                               gw=s_["gw"])
+        us[name] = time_sustained(call, sets)
+        del sets
+    c = W.config3(C3_ROWS, C3_D)
+    x, w, g = c.x.to(device), c.w.to(device), c.g.to(device)
+    for name, nbytes in C3_OPS.items():
+        n_sets = sets_for_l2(nbytes, device)
+        sets = [dict(x=x.clone(), g=g.clone(), out=torch.empty_like(x),
+                     gw=torch.empty(C3_D, dtype=torch.float32, device=device))
+                for _ in range(n_sets)]
+        if name.startswith("c3_vjp"):
+            def call(s_):
+                rn.rmsnorm_vjp(s_["x"], w, s_["g"], c.eps, 0.0, gx=s_["out"], gw=s_["gw"])
+        else:
+            def call(s_):
+                rn.rmsnorm_fwd(s_["x"], w, c.eps, 0.0, out=s_["out"])
+        us[name] = time_sustained(call, sets)
+        del sets
+    return us
+
+
 def bind_to_gpu_numa_node(device_index: int) -> None:
     """Run this process on the CPUs next to the GPU (sysfs local_cpulist of
     its PCI function) so that pinned host buffers are allocated in the GPU's
@@ -434,72 +521,113 @@ def oracle_sample(cases, rows):
     return out
 
 
-def oracle_pass(sample):
-    """One forward (with residual) + VJP on new_residual per D; returns the
-    algorithmic bytes it stands for."""
+def host_cores() -> int:
+    """CPU cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_block(s, lo, hi):
     import oracle
+    _, h = oracle.fwd(s["x"][lo:hi], s["w"], s["eps"], 0.0, s["res"][lo:hi])
+    return oracle.vjp(h, s["w"], s["g"][lo:hi], s["eps"], 0.0)[1]
+
+
+def oracle_pass(sample, threads=1, pool=None):
+    """One forward (with residual) + VJP on new_residual per D.  With
+    threads > 1 the rows are split into that many contiguous blocks, each run
+    by the unchanged oracle functions on a thread of `pool` (the C oracle
+    releases the GIL while it runs), and the blocks' gw are added in block
+    order.  Returns the algorithmic bytes it stands for and each D's gw."""
     nbytes = 0
+    gws = {}
     for D, s in sample.items():
-        _, h = oracle.fwd(s["x"], s["w"], s["eps"], 0.0, s["res"])
-        oracle.vjp(h, s["w"], s["g"], s["eps"], 0.0)
         rows = s["x"].shape[0]
+        if threads <= 1 or pool is None:
+            gws[D] = _oracle_block(s, 0, rows)
+        else:
+            bounds = [rows * i // threads for i in range(threads + 1)]
+            parts = [pool.submit(_oracle_block, s, lo, hi)
+                     for lo, hi in zip(bounds, bounds[1:]) if hi > lo]
+            gw = None
+            for f in parts:  # block order
+                gw = f.result() if gw is None else gw + f.result()
+            gws[D] = gw
         nbytes += fwd_bytes(rows, D) + vjp_bytes(rows, D)
-    return nbytes
+    return nbytes, gws
 
 
-def cpu_baseline(cases, min_seconds=10.0, max_seconds=30.0, rows=256):
-    import oracle
-    oracle.build()
-    sample = oracle_sample(cases, rows)
-    oracle_pass(sample)  # load and warm
+def _timed_passes(sample, seconds, threads, pool):
+    oracle_pass(sample, threads, pool)  # load and warm
     t0 = time.perf_counter()
-    nbytes = 0
-    passes = 0
+    nbytes = passes = 0
     while True:
-        nbytes += oracle_pass(sample)
+        nbytes += oracle_pass(sample, threads, pool)[0]
         passes += 1
         el = time.perf_counter() - t0
-        if el >= min_seconds or el >= max_seconds:
-            break
-    return {"value": nbytes / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "first %d rows of each D (4096, 8192) of the prefill workload: fp64 C "
-                      "oracle forward with residual + VJP, %d passes in %.1f s, one thread"
-                      % (rows, passes, el)}
+        if el >= seconds:
+            return nbytes / el / 1e9, passes, el
+
+
+def cpu_baseline(cases, seconds_one=5.0, seconds_all=10.0, rows=None):
+    """The fp64 C oracle on the host: one thread, then one thread per host
+    core over contiguous row blocks.  `value` is the all-core figure."""
+    import concurrent.futures as cf
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    rows = rows or max(256, 32 * cores)
+    sample = oracle_sample(cases, rows)
+    one, passes1, el1 = _timed_passes(sample, seconds_one, 1, None)
+    with cf.ThreadPoolExecutor(max_workers=cores) as pool:
+        allc, passes, el = _timed_passes(sample, seconds_all, cores, pool)
+    return {"value": allc, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "host_cores": cores, "single_thread_value": one,
+            "sample": "first %d rows of each D (4096, 8192) of the prefill workload: fp64 C oracle "
+                      "forward with residual + VJP; %d threads over contiguous row blocks, %d "
+                      "passes in %.1f s (one thread: %d passes in %.1f s)"
+                      % (rows, cores, passes, el, passes1, el1)}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    import concurrent.futures as cf
     import oracle
     oracle.build()
     from rmsnorm_fwd_bwd_add_gb300 import workloads as W
-    cases = {D: W.config4(D, 512) for D in DS}  # rows of the same recipe; a sample is taken below
-    # size each step's sample so the whole run takes about a minute
-    cal = oracle_sample(cases, 32)
-    t0 = time.perf_counter()
-    cal_bytes = oracle_pass(cal)
-    rate = cal_bytes / max(time.perf_counter() - t0, 1e-6)
-    per_row = sum(fwd_bytes(1, D) + vjp_bytes(1, D) for D in DS)
-    rows = int(60.0 * rate / max(1, args.steps + args.warmup) / per_row)
-    rows = max(4, min(512, rows))
-    sample = oracle_sample(cases, rows)
-    for _ in range(args.warmup):
-        oracle_pass(sample)
-    t0 = time.perf_counter()
-    nbytes = 0
-    for _ in range(args.steps):
-        nbytes += oracle_pass(sample)
-    el = time.perf_counter() - t0
+    cores = host_cores()
+    cases = {D: W.config4(D, 1024) for D in DS}  # rows of the same recipe; a sample is taken below
+    with cf.ThreadPoolExecutor(max_workers=cores) as pool:
+        # size each step's sample so the whole run takes about a minute
+        cal = oracle_sample(cases, 4 * cores)
+        oracle_pass(cal, cores, pool)
+        t0 = time.perf_counter()
+        cal_bytes = oracle_pass(cal, cores, pool)[0]
+        rate = cal_bytes / max(time.perf_counter() - t0, 1e-6)
+        per_row = sum(fwd_bytes(1, D) + vjp_bytes(1, D) for D in DS)
+        rows = int(60.0 * rate / max(1, args.steps + args.warmup) / per_row)
+        rows = max(cores, min(1024, rows))
+        sample = oracle_sample(cases, rows)
+        for _ in range(args.warmup):
+            oracle_pass(sample, cores, pool)
+        t0 = time.perf_counter()
+        nbytes = 0
+        for _ in range(args.steps):
+            nbytes += oracle_pass(sample, cores, pool)[0]
+        el = time.perf_counter() - t0
     value = nbytes / el / 1e9
     desc = ("first %d rows of each D (4096, 8192) of the prefill workload per step: fp64 C oracle "
-            "forward with residual + VJP, one thread" % rows)
+            "forward with residual + VJP, %d threads over contiguous row blocks" % (rows, cores))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": CONFIG,
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "host_cores": cores, "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -800,17 +928,27 @@ def main(argv=None):
     value = world * STEP_BYTES * args.steps / (total_ms * 1e-3) / 1e9
 
     peak, peak_src = measured_peak()
+    sustained = sustained_ops(step, device)
+    all_bytes = dict(OP_BYTES, **C3_OPS)
     ops = {}
+    for name, us in sustained.items():
+        gbs = all_bytes[name] / (us * 1e-6) / 1e9
+        ops[name] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "frac_nominal": round(gbs / NOMINAL_HBM_GBS, 4), "bytes": all_bytes[name]}
     for name, _ in OPS:
         gbs = OP_BYTES[name] / (per_op_us[name] * 1e-6) / 1e9
-        ops[name] = {"us": round(per_op_us[name], 2), "gbs": round(gbs, 1),
-                     "frac": round(gbs / peak, 4), "bytes": OP_BYTES[name]}
+        ops[name].update({"us_step": round(per_op_us[name], 2), "gbs_step": round(gbs, 1),
+                          "frac_step": round(gbs / peak, 4)})
     dom = max(per_op_us, key=per_op_us.get)
-    roofline = {"bound": "hbm", "achieved": ops[dom]["gbs"], "peak": peak, "unit": UNIT,
-                "frac": ops[dom]["gbs"] / peak, "traffic": recorded_traffic(dom),
-                "kernel": dom, "peak_source": peak_src,
+    dom_gbs = OP_BYTES[dom] / (per_op_us[dom] * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak, "unit": UNIT,
+                "frac": dom_gbs / peak, "frac_nominal": dom_gbs / NOMINAL_HBM_GBS,
+                "traffic": recorded_traffic(dom), "kernel": dom, "peak_source": peak_src,
+                "achieved_sustained": ops[dom]["gbs"],
                 "note": "achieved = algorithmic bytes per launch / mean CUDA-event duration of "
-                        "the op (events on every %dth step of the timed region)" % PROBE_EVERY}
+                        "the op inside the timed steps (events around each op on every %dth "
+                        "step); achieved_sustained = the same op timed back to back over "
+                        "rotating buffers (ops[...].us)" % PROBE_EVERY}
 
     e2e = None
     if not args.no_e2e:

@@ -313,6 +313,18 @@ int rmsnorm_device_status(unsigned int *bits, int clear);
 int rmsnorm_debug_inject(int64_t drop_tile, int64_t budget_cycles);
 
 /*
+ * Test hook for the allocation-failure path.  The next `count` gw scratch
+ * allocations of rmsnorm_vjp, rmsnorm_fused_vjp and rmsnorm_vjp_ex in this
+ * process report failure without calling the allocator: each such call returns
+ * RMSNORM_ERR_NO_MEMORY after its argument checks and enqueues nothing (gx and
+ * gw are left untouched).  Calls that need no scratch (a VJP that runs as one
+ * CTA, rows == 0) and the caller-scratch entry points are not affected and do
+ * not use up the count.  count == 0 cancels what is pending; count < 0 returns
+ * RMSNORM_ERR_INVALID_ARG.  Host-side only: nothing faults on the device.
+ */
+int rmsnorm_debug_fail_allocs(int count);
+
+/*
  * Describes the kernel plan rmsnorm_fwd (op = 0) or rmsnorm_vjp (op = 1;
  * with has_residual, rmsnorm_fused_vjp with a g_residual) would use for this
  * problem and pointer alignment on the current device, as a

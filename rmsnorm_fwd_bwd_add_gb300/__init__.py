@@ -19,6 +19,7 @@ include/rmsnorm.h (librmsnorm_gb300.so), with these thin Python bindings:
 PyTorch supplies device memory and streams only.
 """
 from .api import (  # noqa: F401
+    rmsnorm_debug_fail_allocs,
     rmsnorm_debug_inject,
     rmsnorm_describe_dispatch,
     rmsnorm_device_status,
@@ -52,6 +53,7 @@ __all__ = [
     "rmsnorm_vjp_workspace_size",
     "rmsnorm_device_status",
     "rmsnorm_debug_inject",
+    "rmsnorm_debug_fail_allocs",
     "rmsnorm_describe_dispatch",
     "rmsnorm_status_string",
     "RmsnormError",

@@ -28,6 +28,7 @@ EXPORTS = (
     "rmsnorm_last_cuda_error",
     "rmsnorm_device_status",
     "rmsnorm_debug_inject",
+    "rmsnorm_debug_fail_allocs",
     "rmsnorm_describe_dispatch",
 )
 
@@ -98,6 +99,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.rmsnorm_device_status.restype = _i
     lib.rmsnorm_debug_inject.argtypes = [_i64, _i64]
     lib.rmsnorm_debug_inject.restype = _i
+    lib.rmsnorm_debug_fail_allocs.argtypes = [_i]
+    lib.rmsnorm_debug_fail_allocs.restype = _i
     lib.rmsnorm_describe_dispatch.argtypes = [_i, _i64, _i64, _i, _i, _i]
     lib.rmsnorm_describe_dispatch.restype = ctypes.c_char_p
     return lib

@@ -420,6 +420,12 @@ def rmsnorm_debug_inject(drop_tile: int = -1, budget_cycles: int = 0) -> None:
                   _native.lib().rmsnorm_debug_inject(drop_tile, budget_cycles))
 
 
+def rmsnorm_debug_fail_allocs(count: int) -> None:
+    """Test hook: the next `count` gw scratch allocations of the pooled VJP
+    entry points report RMSNORM_ERR_NO_MEMORY without allocating (0 cancels)."""
+    _native.check("rmsnorm_debug_fail_allocs", _native.lib().rmsnorm_debug_fail_allocs(count))
+
+
 def rmsnorm_describe_dispatch(op: str, rows: int, D: int, dtype: torch.dtype,
                               has_residual: bool = False, aligned: bool = True) -> str:
     """The kernel plan the library would choose ('fwd' or 'vjp')."""

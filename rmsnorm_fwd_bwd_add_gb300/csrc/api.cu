@@ -39,6 +39,15 @@ DevInfo g_dev[MAX_DEVICES];
 
 std::atomic<int64_t> g_drop_tile{-1};
 std::atomic<long long> g_wait_budget{DEFAULT_WAIT_BUDGET};
+std::atomic<int> g_fail_allocs{0};  // scratch allocations still to report as failed
+
+// Takes one injected allocation failure if any is pending.
+bool take_injected_alloc_failure() {
+    int n = g_fail_allocs.load();
+    while (n > 0 && !g_fail_allocs.compare_exchange_weak(n, n - 1)) {
+    }
+    return n > 0;
+}
 
 int cuda_fail(cudaError_t e) {
     t_last_cuda_error = (int)e;
@@ -315,6 +324,7 @@ int vjp_pooled(const VjpOperands &o, float eps, float weight_bias, int64_t rows,
     }
     if (gw_in_place(p, gw))
         return vjp_run(o, eps, weight_bias, rows, D, dtype, dev, p, nullptr, s);
+    if (take_injected_alloc_failure()) return RMSNORM_ERR_NO_MEMORY;  // test hook
     cudaMemPool_t pool = nullptr;
     st = scratch_pool(&pool);
     if (st != RMSNORM_OK) return st;
@@ -494,6 +504,12 @@ int rmsnorm_device_status(unsigned int *bits, int clear) {
 int rmsnorm_debug_inject(int64_t drop_tile, int64_t budget_cycles) {
     g_drop_tile.store(drop_tile < 0 ? -1 : drop_tile);
     g_wait_budget.store(budget_cycles > 0 ? (long long)budget_cycles : DEFAULT_WAIT_BUDGET);
+    return RMSNORM_OK;
+}
+
+int rmsnorm_debug_fail_allocs(int count) {
+    if (count < 0) return RMSNORM_ERR_INVALID_ARG;
+    g_fail_allocs.store(count);
     return RMSNORM_OK;
 }
 

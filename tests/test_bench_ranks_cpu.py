@@ -69,7 +69,7 @@ def test_reference_arm_json_line(monkeypatch, capsys):
     import json
     import bench
     monkeypatch.delenv("RANK", raising=False)
-    monkeypatch.setattr(bench, "oracle_pass", lambda sample: 10 ** 6)
+    monkeypatch.setattr(bench, "oracle_pass", lambda sample, threads=1, pool=None: (10 ** 6, {}))
     assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3"]) == 0
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
@@ -78,8 +78,33 @@ def test_reference_arm_json_line(monkeypatch, capsys):
         assert key in line, key
     assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3
     assert line["unit"] == bench.UNIT and line["metric"] == bench.METRIC
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["cores"] == bench.host_cores() == line["cpu_baseline"]["host_cores"]
     assert line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["value"] > 0
+
+
+def test_all_core_oracle_pass_matches_one_thread():
+    """The CPU baseline's all-core pass splits rows into contiguous blocks and
+    adds the blocks' gw in block order: the same gw as one thread up to fp64
+    reassociation, and the same bytes."""
+    import concurrent.futures as cf
+    import numpy as np
+    import oracle
+    import bench
+    from rmsnorm_fwd_bwd_add_gb300 import workloads as W
+    oracle.build()
+    cases = {D: W.config4(D, 37) for D in bench.DS}
+    sample = bench.oracle_sample(cases, 37)
+    b1, gw1 = bench.oracle_pass(sample)
+    with cf.ThreadPoolExecutor(max_workers=4) as pool:
+        b4, gw4 = bench.oracle_pass(sample, 4, pool)
+    assert b1 == b4 == sum(bench.fwd_bytes(37, D) + bench.vjp_bytes(37, D) for D in bench.DS)
+    for D in bench.DS:
+        np.testing.assert_allclose(gw4[D], gw1[D], rtol=1e-12, atol=1e-12)
+        # and gw is the oracle's own VJP of the whole sample
+        s = sample[D]
+        _, h = oracle.fwd(s["x"], s["w"], s["eps"], 0.0, s["res"])
+        np.testing.assert_array_equal(gw1[D], oracle.vjp(h, s["w"], s["g"], s["eps"], 0.0)[1])

@@ -332,3 +332,38 @@ def test_wait_timeout_is_reported_and_context_survives():
     # the context is still usable and the next call is correct
     check_fwd(case)
     assert rn.rmsnorm_device_status(clear=True) == 0
+
+
+def test_injected_scratch_allocation_failure():
+    """A failed gw scratch allocation (made on the host by the test hook, the
+    allocator is not called) returns RMSNORM_ERR_NO_MEMORY with nothing
+    enqueued; the next call allocates normally and is correct."""
+    case = W.random_case(3000, 2048, torch.bfloat16, seed=41, residual=False)
+    x, w, g = _dev(case.x), _dev(case.w), _dev(case.g)
+    assert rn.rmsnorm_describe_dispatch("vjp", case.rows, case.D, case.dtype).startswith("staged")
+    gx = torch.full_like(x, float("nan"))
+    gw = torch.full((case.D,), float("nan"), dtype=torch.float32, device=DEV)
+    rn.rmsnorm_debug_fail_allocs(1)
+    try:
+        with pytest.raises(rn.RmsnormError) as e:
+            rn.rmsnorm_vjp(x, w, g, case.eps, case.weight_bias, gx=gx, gw=gw)
+    finally:
+        rn.rmsnorm_debug_fail_allocs(0)
+    assert e.value.status == 4  # RMSNORM_ERR_NO_MEMORY
+    torch.cuda.synchronize()
+    assert torch.isnan(gx).all() and torch.isnan(gw).all(), "the failed call enqueued work"
+    # the hook is spent: the same call now runs and matches the oracle
+    rn.rmsnorm_vjp(x, w, g, case.eps, case.weight_bias, gx=gx, gw=gw)
+    want_gx, want_gw = oracle_vjp(case.x, case)
+    assert_close(case.name + " gx", gx, want_gx)
+    assert_close(case.name + " gw", gw, want_gw, torch.float32)
+    # a VJP that needs no scratch (one row: gw written in place) ignores the hook
+    one = W.random_case(1, 2048, torch.bfloat16, seed=42, residual=False)
+    rn.rmsnorm_debug_fail_allocs(1)
+    try:
+        gx1, gw1 = rn.rmsnorm_vjp(_dev(one.x), _dev(one.w), _dev(one.g), one.eps)
+    finally:
+        rn.rmsnorm_debug_fail_allocs(0)
+    want_gx1, want_gw1 = oracle_vjp(one.x, one)
+    assert_close("one row gx", gx1, want_gx1)
+    assert_close("one row gw", gw1, want_gw1, torch.float32)

@@ -149,3 +149,10 @@ def test_product_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b|rmsnorm_oracle", src, re.M), f
+
+
+def test_alloc_failure_hook_arguments(lib):
+    # the hook only sets a host-side counter: no GPU needed
+    assert lib.rmsnorm_debug_fail_allocs(-1) == 1
+    assert lib.rmsnorm_debug_fail_allocs(2) == 0
+    assert lib.rmsnorm_debug_fail_allocs(0) == 0
