@@ -271,10 +271,18 @@ int rmsnorm_rope_kv_append(const void *q, const void *k, const void *v,
  * library instead of allocated memory, and nothing is allocated.
  *   - Memory: the array occupies RMSNORM_VJP_NOALLOC_MAX_BYTES of device memory
  *     on every GPU where the library is loaded, until the process exits.
- *   - Limit: a problem whose scratch (rmsnorm_vjp_workspace_size for these
- *     pointers' alignment) exceeds RMSNORM_VJP_NOALLOC_MAX_BYTES returns
- *     RMSNORM_ERR_UNSUPPORTED and enqueues nothing.  On a 152-SM GB300 that
- *     admits 16-byte aligned rows with D up to about 13,000 at any row count.
+ *   - Limit: a problem whose scratch (one fp32 row of D per partial row of
+ *     the plan these pointers get) exceeds RMSNORM_VJP_NOALLOC_MAX_BYTES
+ *     returns RMSNORM_ERR_UNSUPPORTED and enqueues nothing.  On a 152-SM
+ *     GB300, at any row count: dense fp16/bf16 rows up to D = 65536 and fp32
+ *     rows up to D = 32768 whose tensors start on 16-byte boundaries (at most
+ *     912 partial rows of D <= 1536, 152 rows of D <= 16384, and one row per
+ *     cluster, at most 76, beyond), and dense rows whose tensors all start at
+ *     one shared offset from a boundary up to D = 16377 (fp16/bf16) or 8189
+ *     (fp32).  Anything else (tensors at different offsets, strided rows off
+ *     boundaries, longer rows) runs on the element-at-a-time tier with
+ *     min(2 x SMs, rows * 3 * size / 40) partial rows, which fit while
+ *     that count x D x 4 bytes <= 16 MiB (e.g. D <= 13,797 at 2,000+ rows).
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
  *   - Sharing: every call on a device uses the same array, and it keeps the
@@ -327,9 +335,12 @@ int rmsnorm_debug_fail_allocs(int count);
 /*
  * Describes the kernel plan rmsnorm_fwd (op = 0) or rmsnorm_vjp (op = 1;
  * with has_residual, rmsnorm_fused_vjp with a g_residual) would use for this
- * problem and pointer alignment on the current device, as a
- * static string such as "staged:cfg8:nt512:g512:v2:s6:tr1:grid152:smem..."; for
- * tests and benchmarks.
+ * problem on the current device, as a static string such as
+ * "staged:cfg8:nt512:g512:v2:s6:tr1:grid152:smem..." ("staged-shift:..." for
+ * the shifted-rows instances); for tests and benchmarks.  aligned: 1 = dense
+ * tensors at 16-byte aligned addresses (rows off 16-byte boundaries when
+ * D * size is not a multiple of 16), 2 = dense tensors that all start at the
+ * same unaligned offset, 0 = anything else (strided or mixed offsets).
  */
 const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype,
                                       int has_residual, int aligned);

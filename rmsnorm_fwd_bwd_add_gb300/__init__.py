@@ -5,6 +5,8 @@ include/rmsnorm.h (librmsnorm_gb300.so), with these thin Python bindings:
 
   rmsnorm_fwd  -- fused residual-add RMSNorm forward with two outputs
                   (out, new_residual), fp32 accumulation, weight_bias scalar.
+  rmsnorm_fwd_bind, rmsnorm_vjp_bind -- the same calls with their tensors
+                  checked once, for loops over fixed buffers (decode).
   rmsnorm_vjp  -- RMSNorm VJP: gx and an fp32 gw reduced across rows inside
                   the kernels (deterministic, no [rows, D] temporary).
   rmsnorm_fused_vjp -- VJP of the two-output fused op (adds the gradient that
@@ -19,17 +21,20 @@ include/rmsnorm.h (librmsnorm_gb300.so), with these thin Python bindings:
 PyTorch supplies device memory and streams only.
 """
 from .api import (  # noqa: F401
+    BoundCall,
     rmsnorm_debug_fail_allocs,
     rmsnorm_debug_inject,
     rmsnorm_describe_dispatch,
     rmsnorm_device_status,
     rmsnorm_fused_vjp,
     rmsnorm_fwd,
+    rmsnorm_fwd_bind,
     rmsnorm_fwd_ex,
     rmsnorm_gated_silu,
     rmsnorm_rope_kv_append,
     rmsnorm_status_string,
     rmsnorm_vjp,
+    rmsnorm_vjp_bind,
     rmsnorm_vjp_ex,
     rmsnorm_vjp_noalloc,
     rmsnorm_vjp_workspace_size,
@@ -41,6 +46,9 @@ from .autograd import fused_add_rmsnorm, rms_norm  # noqa: F401
 __all__ = [
     "rmsnorm_fwd",
     "rmsnorm_vjp",
+    "rmsnorm_fwd_bind",
+    "rmsnorm_vjp_bind",
+    "BoundCall",
     "rmsnorm_fused_vjp",
     "rmsnorm_fwd_ex",
     "rmsnorm_vjp_ex",

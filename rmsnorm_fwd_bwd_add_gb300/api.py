@@ -137,32 +137,221 @@ def _check_w(w: torch.Tensor, x: torch.Tensor, D: int) -> None:
         raise ValueError("w must be a contiguous [%d] %s tensor on %s" % (D, x.dtype, x.device))
 
 
+# ---- the per-token entry points: one cheap pass of checks per tensor -------
+# A decode step calls these once per layer and token, so their Python cost is
+# kept to a few attribute reads per tensor: dtype by identity, the device as an
+# index, the shape, contiguity.  The message of a failed check is built only
+# when it fails.
+
+_get_device = getattr(torch._C, "_cuda_getDevice", None)
+_fns = {}
+
+
+def _fn(name: str):
+    """The C entry point `name`, bound once."""
+    f = _fns.get(name)
+    if f is None:
+        f = _fns[name] = getattr(_native.lib(), name)
+    return f
+
+
+def _rows_dev(x: torch.Tensor):
+    """(rows, D, device index, dtype code) of a contiguous [..., D] CUDA tensor."""
+    dev = x.get_device()
+    if dev < 0:
+        raise ValueError("tensors must be CUDA tensors (there is no CPU path)")
+    shape = x.shape
+    if not shape:
+        raise ValueError("x must have at least one dimension")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    code = _DTYPES.get(x.dtype)
+    if code is None:
+        _dtype_code(x)  # raises with the message
+    D = shape[-1]
+    return (x.numel() // D if D else 0), D, dev, code
+
+
+def _like(name: str, t: torch.Tensor, x: torch.Tensor, dev: int) -> None:
+    if (t.dtype is not x.dtype or t.get_device() != dev or t.shape != x.shape
+            or not t.is_contiguous()):
+        _check_like(name, t, x)  # raises with the message
+        raise ValueError("%s must be a contiguous %s tensor on cuda:%d" % (name, x.dtype, dev))
+
+
+def _weight(w: torch.Tensor, x: torch.Tensor, D: int, dev: int) -> None:
+    if (w.dtype is not x.dtype or w.get_device() != dev or w.dim() != 1 or w.shape[0] != D
+            or not w.is_contiguous()):
+        _check_w(w, x, D)
+        raise ValueError("w must be a contiguous [%d] %s tensor on cuda:%d" % (D, x.dtype, dev))
+
+
+def _gw(gw: Optional[torch.Tensor], D: int, dev: int) -> torch.Tensor:
+    if gw is None:
+        return torch.empty(D, dtype=torch.float32, device=torch.device("cuda", dev))
+    if (gw.dtype is not torch.float32 or gw.get_device() != dev or gw.dim() != 1
+            or gw.shape[0] != D or not gw.is_contiguous()):
+        raise ValueError("gw must be a contiguous [%d] float32 tensor on cuda:%d" % (D, dev))
+    return gw
+
+
+def _call(dev: int, stream, fn, *args) -> int:
+    """fn(*args, stream) with device `dev` current (switched only if needed)."""
+    cur = _get_device() if _get_device is not None else torch.cuda.current_device()
+    h = stream.cuda_stream if stream is not None else (
+        _raw_stream(dev) if _raw_stream is not None else torch.cuda.current_stream(dev).cuda_stream)
+    if cur == dev:
+        return fn(*args, h)
+    torch.cuda.set_device(dev)
+    try:
+        return fn(*args, h)
+    finally:
+        torch.cuda.set_device(cur)
+
+
 def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float, weight_bias: float = 0.0,
                 residual: Optional[torch.Tensor] = None, *, out: Optional[torch.Tensor] = None,
                 new_residual: Optional[torch.Tensor] = None, stream=None):
     """Fused residual-add RMSNorm forward.  Returns (out, new_residual);
     new_residual is None when residual is None.  Pass out=x or
     new_residual=residual to update in place."""
-    rows, D = _rows_d(x)
-    code = _dtype_code(x)
-    _check_w(w, x, D)
-    if residual is not None:
-        _check_like("residual", residual, x)
+    rows, D, dev, code = _rows_dev(x)
+    _weight(w, x, D, dev)
     if out is None:
         out = torch.empty_like(x)
-    _check_like("out", out, x)
+    else:
+        _like("out", out, x, dev)
     if residual is not None:
+        _like("residual", residual, x, dev)
         if new_residual is None:
             new_residual = torch.empty_like(x)
-        _check_like("new_residual", new_residual, x)
+        else:
+            _like("new_residual", new_residual, x, dev)
+        st = _call(dev, stream, _fn("rmsnorm_fwd"), x.data_ptr() or None,
+                   residual.data_ptr() or None, w.data_ptr(), eps, weight_bias,
+                   out.data_ptr() or None, new_residual.data_ptr() or None, rows, D, code)
     elif new_residual is not None:
         raise ValueError("new_residual given without residual")
-    with _OnDevice(x.device):
-        st = _native.lib().rmsnorm_fwd(_ptr(x), _ptr(residual), _ptr(w), eps, weight_bias,
-                                       _ptr(out), _ptr(new_residual), rows, D, code,
-                                       _stream(x.device, stream))
-    _native.check("rmsnorm_fwd", st)
+    else:
+        st = _call(dev, stream, _fn("rmsnorm_fwd"), x.data_ptr() or None, None, w.data_ptr(),
+                   eps, weight_bias, out.data_ptr() or None, None, rows, D, code)
+    if st:
+        _native.check("rmsnorm_fwd", st)
     return out, new_residual
+
+
+def rmsnorm_vjp(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float,
+                weight_bias: float = 0.0, *, gx: Optional[torch.Tensor] = None,
+                gw: Optional[torch.Tensor] = None, stream=None):
+    """RMSNorm VJP.  Returns (gx, gw) with gw fp32, reduced across rows on the
+    GPU.  The library takes its gw scratch from its own stream-ordered pool."""
+    rows, D, dev, code = _rows_dev(x)
+    _weight(w, x, D, dev)
+    _like("g", g, x, dev)
+    if gx is None:
+        gx = torch.empty_like(x)
+    else:
+        _like("gx", gx, x, dev)
+    gw = _gw(gw, D, dev)
+    st = _call(dev, stream, _fn("rmsnorm_vjp"), x.data_ptr() or None, w.data_ptr(),
+               g.data_ptr() or None, eps, weight_bias, gx.data_ptr() or None, gw.data_ptr(), rows,
+               D, code)
+    if st:
+        _native.check("rmsnorm_vjp", st)
+    return gx, gw
+
+
+def rmsnorm_fused_vjp(h: torch.Tensor, w: torch.Tensor, g_out: torch.Tensor, eps: float,
+                      weight_bias: float = 0.0, g_residual: Optional[torch.Tensor] = None, *,
+                      g_h: Optional[torch.Tensor] = None, gw: Optional[torch.Tensor] = None,
+                      stream=None):
+    """VJP of the two-output fused op at h (its new_residual): returns
+    (g_h, gw), g_h = VJP(h, g_out) + g_residual the gradient with respect to
+    both x and residual."""
+    rows, D, dev, code = _rows_dev(h)
+    _weight(w, h, D, dev)
+    _like("g_out", g_out, h, dev)
+    if g_residual is not None:
+        _like("g_residual", g_residual, h, dev)
+    if g_h is None:
+        g_h = torch.empty_like(h)
+    else:
+        _like("g_h", g_h, h, dev)
+    gw = _gw(gw, D, dev)
+    st = _call(dev, stream, _fn("rmsnorm_fused_vjp"), h.data_ptr() or None, w.data_ptr(),
+               g_out.data_ptr() or None,
+               None if g_residual is None else (g_residual.data_ptr() or None), eps, weight_bias,
+               g_h.data_ptr() or None, gw.data_ptr(), rows, D, code)
+    if st:
+        _native.check("rmsnorm_fused_vjp", st)
+    return g_h, gw
+
+
+class BoundCall:
+    """One C call with its tensors checked once (rmsnorm_fwd_bind,
+    rmsnorm_vjp_bind): calling it launches the kernels on the device's
+    current stream (or the stream given at bind time).  For loops that run
+    the same op on the same buffers every step (a decode loop's per-token
+    norm): it keeps the tensors alive, and they must keep their storage,
+    shape and dtype for as long as the bound call is used."""
+
+    __slots__ = ("_fn", "_args", "_dev", "_stream", "_name", "_keep", "outputs")
+
+    def __init__(self, name, fn, args, dev, stream, keep, outputs):
+        self._name = name
+        self._fn = fn
+        self._args = args
+        self._dev = dev
+        self._stream = stream
+        self._keep = keep
+        self.outputs = outputs
+
+    def __call__(self):
+        st = _call(self._dev, self._stream, self._fn, *self._args)
+        if st:
+            _native.check(self._name, st)
+        return self.outputs
+
+
+def rmsnorm_fwd_bind(x: torch.Tensor, w: torch.Tensor, eps: float, weight_bias: float = 0.0,
+                     residual: Optional[torch.Tensor] = None, *, out: Optional[torch.Tensor] = None,
+                     new_residual: Optional[torch.Tensor] = None, stream=None) -> BoundCall:
+    """rmsnorm_fwd with its arguments checked now and the call issued by the
+    returned BoundCall (which returns (out, new_residual))."""
+    rows, D, dev, code = _rows_dev(x)
+    _weight(w, x, D, dev)
+    if out is None:
+        out = torch.empty_like(x)
+    _like("out", out, x, dev)
+    if residual is not None:
+        _like("residual", residual, x, dev)
+        if new_residual is None:
+            new_residual = torch.empty_like(x)
+        _like("new_residual", new_residual, x, dev)
+    elif new_residual is not None:
+        raise ValueError("new_residual given without residual")
+    args = (x.data_ptr() or None, None if residual is None else (residual.data_ptr() or None),
+            w.data_ptr(), eps, weight_bias, out.data_ptr() or None,
+            None if new_residual is None else (new_residual.data_ptr() or None), rows, D, code)
+    return BoundCall("rmsnorm_fwd", _fn("rmsnorm_fwd"), args, dev, stream,
+                     (x, w, residual), (out, new_residual))
+
+
+def rmsnorm_vjp_bind(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float,
+                     weight_bias: float = 0.0, *, gx: Optional[torch.Tensor] = None,
+                     gw: Optional[torch.Tensor] = None, stream=None) -> BoundCall:
+    """rmsnorm_vjp with its arguments checked now and the call issued by the
+    returned BoundCall (which returns (gx, gw))."""
+    rows, D, dev, code = _rows_dev(x)
+    _weight(w, x, D, dev)
+    _like("g", g, x, dev)
+    if gx is None:
+        gx = torch.empty_like(x)
+    _like("gx", gx, x, dev)
+    gw = _gw(gw, D, dev)
+    args = (x.data_ptr() or None, w.data_ptr(), g.data_ptr() or None, eps, weight_bias,
+            gx.data_ptr() or None, gw.data_ptr(), rows, D, code)
+    return BoundCall("rmsnorm_vjp", _fn("rmsnorm_vjp"), args, dev, stream, (x, w, g), (gx, gw))
 
 
 def _vjp_outputs(x, g, gx, gw, D):
@@ -176,43 +365,6 @@ def _vjp_outputs(x, g, gx, gw, D):
             or not gw.is_contiguous()):
         raise ValueError("gw must be a contiguous [%d] float32 tensor on %s" % (D, x.device))
     return gx, gw
-
-
-def rmsnorm_vjp(x: torch.Tensor, w: torch.Tensor, g: torch.Tensor, eps: float,
-                weight_bias: float = 0.0, *, gx: Optional[torch.Tensor] = None,
-                gw: Optional[torch.Tensor] = None, stream=None):
-    """RMSNorm VJP.  Returns (gx, gw) with gw fp32, reduced across rows on the
-    GPU.  The library takes its gw scratch from its own stream-ordered pool."""
-    rows, D = _rows_d(x)
-    code = _dtype_code(x)
-    _check_w(w, x, D)
-    gx, gw = _vjp_outputs(x, g, gx, gw, D)
-    with _OnDevice(x.device):
-        st = _native.lib().rmsnorm_vjp(_ptr(x), _ptr(w), _ptr(g), eps, weight_bias, _ptr(gx),
-                                       _ptr(gw), rows, D, code, _stream(x.device, stream))
-    _native.check("rmsnorm_vjp", st)
-    return gx, gw
-
-
-def rmsnorm_fused_vjp(h: torch.Tensor, w: torch.Tensor, g_out: torch.Tensor, eps: float,
-                      weight_bias: float = 0.0, g_residual: Optional[torch.Tensor] = None, *,
-                      g_h: Optional[torch.Tensor] = None, gw: Optional[torch.Tensor] = None,
-                      stream=None):
-    """VJP of the two-output fused op at h (its new_residual): returns
-    (g_h, gw), g_h = VJP(h, g_out) + g_residual the gradient with respect to
-    both x and residual."""
-    rows, D = _rows_d(h)
-    code = _dtype_code(h)
-    _check_w(w, h, D)
-    if g_residual is not None:
-        _check_like("g_residual", g_residual, h)
-    g_h, gw = _vjp_outputs(h, g_out, g_h, gw, D)
-    with _OnDevice(h.device):
-        st = _native.lib().rmsnorm_fused_vjp(_ptr(h), _ptr(w), _ptr(g_out), _ptr(g_residual), eps,
-                                             weight_bias, _ptr(g_h), _ptr(gw), rows, D, code,
-                                             _stream(h.device, stream))
-    _native.check("rmsnorm_fused_vjp", st)
-    return g_h, gw
 
 
 def rmsnorm_gated_silu(x: torch.Tensor, *, out: Optional[torch.Tensor] = None, stream=None):
@@ -428,9 +580,11 @@ def rmsnorm_debug_fail_allocs(count: int) -> None:
 
 def rmsnorm_describe_dispatch(op: str, rows: int, D: int, dtype: torch.dtype,
                               has_residual: bool = False, aligned: bool = True) -> str:
-    """The kernel plan the library would choose ('fwd' or 'vjp')."""
+    """The kernel plan the library would choose ('fwd' or 'vjp').  aligned:
+    True/1 dense 16-byte aligned tensors, 2 dense tensors at one shared
+    unaligned offset, False/0 anything else."""
     s = _native.lib().rmsnorm_describe_dispatch(1 if op == "vjp" else 0, rows, D, _DTYPES[dtype],
-                                                1 if has_residual else 0, 1 if aligned else 0)
+                                                1 if has_residual else 0, int(aligned))
     return s.decode()
 
 

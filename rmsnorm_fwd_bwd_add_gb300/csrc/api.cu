@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "common.cuh"
@@ -33,6 +34,7 @@ struct DevInfo {
     int sm_count = 0;
     unsigned int *status = nullptr;  // device address of g_devstatus
     cudaMemPool_t pool = nullptr;    // gw scratch of rmsnorm_vjp; keeps its memory
+    int cluster_cap[9] = {};         // clusters of 2, 4, 8 CTAs the device holds at once
 };
 std::mutex g_dev_mu;
 DevInfo g_dev[MAX_DEVICES];
@@ -68,6 +70,7 @@ int current_device(DevInfo *out) {
         e = cudaGetSymbolAddress(&p, g_devstatus);
         if (e != cudaSuccess) return cuda_fail(e);
         d.status = static_cast<unsigned int *>(p);
+        for (int cl : {2, 4, 8}) d.cluster_cap[cl] = cluster_capacity(cl);
         d.ready = true;
     }
     *out = d;
@@ -191,8 +194,40 @@ bool rows_aligned(const Mat &m, int es) {
     return !m.p || (aligned16(m.p) && (m.ld * es) % 16 == 0);
 }
 
+// Every element of every operand must sit at a multiple of its size.
+bool elem_aligned(const void *p, int es) { return ((uintptr_t)p % (uintptr_t)es) == 0; }
+
+// How the row tensors of one call (null entries ignored) and w sit relative
+// to 16-byte boundaries (planner Align): every row aligned -> ALIGN_VEC
+// (dense rows, no rstd) or ALIGN_VEC_GEN (rows a stride apart, or rstd);
+// dense rows (stride D) whose tensors all start at the same offset from a
+// boundary, with no rstd -> ALIGN_SHIFT; anything else -> ALIGN_NONE.
+int align_of(std::initializer_list<const Mat *> ms, const void *w, const void *rstd, int64_t D,
+             int es) {
+    bool vec = (D * es) % 16 == 0 && aligned16(w);
+    bool dense = rstd == nullptr;
+    for (const Mat *m : ms) {
+        vec = vec && rows_aligned(*m, es);
+        dense = dense && (!m->p || m->ld == D);
+    }
+    if (vec) return dense ? ALIGN_VEC : ALIGN_VEC_GEN;
+    if (rstd) return ALIGN_NONE;
+    int off = -1;
+    for (const Mat *m : ms) {
+        if (!m->p) continue;
+        if (m->ld != D) return ALIGN_NONE;
+        const int o = (int)((uintptr_t)m->p & 15u);
+        if (off >= 0 && o != off) return ALIGN_NONE;
+        off = o;
+    }
+    return ALIGN_SHIFT;
+}
+
+// gw partial rows of a VJP plan: one per CTA, or one per cluster.
+int partial_rows(const Plan &p) { return p.tier == TIER_CLUSTER ? p.grid / p.cl : p.grid; }
+
 size_t partials_bytes(const Plan &p, int64_t D) {
-    const size_t b = (size_t)p.grid * (size_t)D * sizeof(float);
+    const size_t b = (size_t)partial_rows(p) * (size_t)D * sizeof(float);
     return (b + 255) & ~(size_t)255;
 }
 
@@ -200,6 +235,7 @@ cudaError_t launch_plan(int dtype, int mode, const Plan &p, const KernelArgs &a,
     switch (p.tier) {
         case TIER_STAGED: return launch_staged(dtype, mode, p, a, s);
         case TIER_DIRECT: return launch_direct(dtype, mode, p, a, s);
+        case TIER_CLUSTER: return launch_cluster(dtype, mode, p, a, s);
         default: return launch_generic(dtype, mode, p, a, s);
     }
 }
@@ -217,6 +253,7 @@ KernelArgs base_args(const DevInfo &dev, const Plan &p, float eps, float wb, int
     a.num_tiles = p.num_tiles;
     a.stage_bytes = p.stage_bytes;
     a.wait_budget = g_wait_budget.load(std::memory_order_relaxed);
+    a.cl_cols = p.cl_cols;
     a.drop_tile = g_drop_tile.load(std::memory_order_relaxed);
     return a;
 }
@@ -245,6 +282,10 @@ int vjp_prepare(const VjpOperands &o, float eps, float weight_bias, int64_t rows
     if (st != RMSNORM_OK) return st;
     if (!o.w || !o.gw) return RMSNORM_ERR_INVALID_ARG;
     const int es = esize_of(dtype);
+    if (!elem_aligned(o.w, es) || !elem_aligned(o.gw, 4) || !elem_aligned(o.rstd, 4))
+        return RMSNORM_ERR_INVALID_ARG;
+    for (const Mat *m : {&o.x, &o.g, &o.g_res, &o.gx})
+        if (!elem_aligned(m->p, es)) return RMSNORM_ERR_INVALID_ARG;
     const size_t nw = (size_t)D * es, ngw = (size_t)D * 4, nr = (size_t)rows * 4;
     if (rows > 0) {
         if (!o.x.p || !o.g.p || !o.gx.p) return RMSNORM_ERR_INVALID_ARG;
@@ -269,11 +310,11 @@ int vjp_prepare(const VjpOperands &o, float eps, float weight_bias, int64_t rows
     st = current_device(dev);
     if (st != RMSNORM_OK) return st;
     if (rows > 0) {
-        const bool aligned = (D * es) % 16 == 0 && aligned16(o.w) && rows_aligned(o.x, es) &&
-                             rows_aligned(o.g, es) && rows_aligned(o.gx, es) &&
-                             rows_aligned(o.g_res, es);
-        *plan = make_plan(o.g_res.p ? MODE_VJP_ADD : MODE_VJP, rows, (int)D, es, aligned,
-                          dev->sm_count);
+        const Mat x = mat(o.x.p, o.x.ld, rows, D), g = mat(o.g.p, o.g.ld, rows, D);
+        const Mat gr = mat(o.g_res.p, o.g_res.ld, rows, D), gx = mat(o.gx.p, o.gx.ld, rows, D);
+        const int align = align_of({&x, &g, &gr, &gx}, o.w, o.rstd, D, es);
+        *plan = make_plan(o.g_res.p ? MODE_VJP_ADD : MODE_VJP, rows, (int)D, es, align,
+                          dev->sm_count, dev->cluster_cap);
     }
     return RMSNORM_OK;
 }
@@ -283,7 +324,7 @@ int vjp_prepare(const VjpOperands &o, float eps, float weight_bias, int64_t rows
 // kernel (the fixed-order sum of one row is that row, so the bits are the
 // same).  The tiers store partial rows as 16-byte vectors, so gw must be
 // 16-byte aligned for this; otherwise the two-stage path runs.
-bool gw_in_place(const Plan &p, const float *gw) { return p.grid == 1 && aligned16(gw); }
+bool gw_in_place(const Plan &p, const float *gw) { return partial_rows(p) == 1 && aligned16(gw); }
 
 int vjp_run(const VjpOperands &o, float eps, float weight_bias, int64_t rows, int64_t D,
             int dtype, const DevInfo &dev, const Plan &p, float *partials, cudaStream_t s) {
@@ -304,7 +345,7 @@ int vjp_run(const VjpOperands &o, float eps, float weight_bias, int64_t rows, in
     cudaError_t e = launch_plan(dtype, o.g_res.p ? MODE_VJP_ADD : MODE_VJP, p, a, s);
     if (e != cudaSuccess) return cuda_fail(e);
     if (in_place) return RMSNORM_OK;
-    e = launch_gw_reduce(partials, o.gw, p.grid, (int)D, s);
+    e = launch_gw_reduce(partials, o.gw, partial_rows(p), (int)D, s);
     if (e != cudaSuccess) return cuda_fail(e);
     return RMSNORM_OK;
 }
@@ -342,7 +383,8 @@ int vjp_pooled(const VjpOperands &o, float eps, float weight_bias, int64_t rows,
 }
 
 const char *tier_name(int t) {
-    return t == TIER_STAGED ? "staged" : t == TIER_DIRECT ? "direct" : "generic";
+    return t == TIER_STAGED ? "staged" : t == TIER_DIRECT ? "direct" : t == TIER_CLUSTER ? "cluster"
+                                                                                    : "generic";
 }
 
 }  // namespace
@@ -368,6 +410,9 @@ int rmsnorm_fwd_ex(const void *x, int64_t ld_x, const void *residual, int64_t ld
     const Mat mx = mat(x, ld_x, rows, D), mo = mat(out, ld_out, rows, D);
     const Mat mr = mat(residual, ld_residual, rows, D);
     const Mat mn = mat(new_residual, ld_new_residual, rows, D);
+    for (const void *q : {x, residual, w, (const void *)out, (const void *)new_residual})
+        if (!elem_aligned(q, es)) return RMSNORM_ERR_INVALID_ARG;
+    if (!elem_aligned(rstd, 4)) return RMSNORM_ERR_INVALID_ARG;
     const size_t nw = (size_t)D * es, nr = (size_t)rows * 4;
     if (mats_overlap(mo, mn, rows, D, es)) return RMSNORM_ERR_INVALID_ARG;
     for (const Mat *o : {&mo, &mn}) {
@@ -383,9 +428,8 @@ int rmsnorm_fwd_ex(const void *x, int64_t ld_x, const void *residual, int64_t ld
     st = current_device(&dev);
     if (st != RMSNORM_OK) return st;
     const int mode = residual ? MODE_FWD_RES : MODE_FWD_NORES;
-    const bool aligned = (D * es) % 16 == 0 && aligned16(w) && rows_aligned(mx, es) &&
-                         rows_aligned(mo, es) && rows_aligned(mr, es) && rows_aligned(mn, es);
-    const Plan p = make_plan(mode, rows, (int)D, es, aligned, dev.sm_count);
+    const int align = align_of({&mx, &mr, &mo, &mn}, w, rstd, D, es);
+    const Plan p = make_plan(mode, rows, (int)D, es, align, dev.sm_count, dev.cluster_cap);
     KernelArgs a = base_args(dev, p, eps, weight_bias, rows, D);
     a.in0 = x;
     a.ld_in0 = mx.ld;
@@ -413,11 +457,13 @@ size_t rmsnorm_vjp_workspace_size(int64_t rows, int64_t D, int dtype) {
     if (check_common(rows, D, dtype, 0.f, 0.f) != RMSNORM_OK || rows == 0) return 0;
     DevInfo dev;
     if (current_device(&dev) != RMSNORM_OK) return 0;
-    // The plan depends on pointer alignment; cover both outcomes.
+    // The plan depends on pointer alignment; cover every outcome.
     const int es = esize_of(dtype);
-    const Plan pa = make_plan(MODE_VJP, rows, (int)D, es, (D * es) % 16 == 0, dev.sm_count);
-    const Plan pu = make_plan(MODE_VJP, rows, (int)D, es, false, dev.sm_count);
-    return std::max(partials_bytes(pa, D), partials_bytes(pu, D));
+    size_t most = 0;
+    for (int align : {ALIGN_VEC, ALIGN_SHIFT, ALIGN_NONE})
+        most = std::max(most, partials_bytes(make_plan(MODE_VJP, rows, (int)D, es, align,
+                                                       dev.sm_count, dev.cluster_cap), D));
+    return most;
 }
 
 int rmsnorm_vjp_ws(const void *x, const void *w, const void *g, float eps, float weight_bias,
@@ -523,10 +569,14 @@ const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype
     const int mode = op == 1 ? (has_residual ? MODE_VJP_ADD : MODE_VJP)
                              : (has_residual ? MODE_FWD_RES : MODE_FWD_NORES);
     const int es = esize_of(dtype);
-    const Plan p = make_plan(mode, rows, (int)D, es, aligned && (D * es) % 16 == 0, dev.sm_count);
-    std::snprintf(buf, sizeof(buf), "%s:cfg%d:nt%d:g%d:v%d:s%d:tr%d:grid%d:smem%zu",
-                  tier_name(p.tier), p.cfg, p.nt, p.g, p.v, p.stages, p.tile_rows, p.grid,
-                  p.smem);
+    const int align = aligned == 2               ? ALIGN_SHIFT
+                      : !aligned                  ? ALIGN_NONE
+                      : (D * es) % 16 == 0        ? ALIGN_VEC
+                                                  : ALIGN_SHIFT;
+    const Plan p = make_plan(mode, rows, (int)D, es, align, dev.sm_count, dev.cluster_cap);
+    std::snprintf(buf, sizeof(buf), "%s%s:cfg%d:nt%d:g%d:v%d:s%d:tr%d:grid%d:smem%zu:cl%d",
+                  tier_name(p.tier), p.shift ? "-shift" : "", p.cfg, p.nt, p.g, p.v, p.stages,
+                  p.tile_rows, p.grid, p.smem, p.cl);
     return buf;
 }
 
@@ -543,9 +593,9 @@ size_t vjp_partials_bytes_for(const void *x, const void *w, const void *g, const
     DevInfo dev;
     if (current_device(&dev) != RMSNORM_OK) return 0;
     const int es = esize_of(dtype);
-    const bool aligned =
-        (D * es) % 16 == 0 && aligned16(x) && aligned16(g) && aligned16(gx) && aligned16(w);
-    return partials_bytes(make_plan(MODE_VJP, rows, (int)D, es, aligned, dev.sm_count), D);
+    const Mat mx{x, D}, mg{g, D}, mgx{gx, D};
+    const int align = align_of({&mx, &mg, &mgx}, w, nullptr, D, es);
+    return partials_bytes(make_plan(MODE_VJP, rows, (int)D, es, align, dev.sm_count, dev.cluster_cap), D);
 }
 
 // Records a failed CUDA call for rmsnorm_last_cuda_error().

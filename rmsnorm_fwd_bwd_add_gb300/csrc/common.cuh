@@ -273,3 +273,68 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, 
 }
 
 }  // namespace rmsn
+
+namespace rmsn {
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters (inline PTX): rank, the hardware cluster barrier, and
+// distributed shared memory (another CTA's shared memory in the cluster).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA in the cluster arrives and waits (release /
+// acquire: shared-memory writes before it are visible to the cluster after).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared::cluster address of this CTA's shared variable at `p` in the
+// cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void dsmem_store_f2(uint32_t addr, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
+                 : "memory");
+}
+
+// One arrival on an mbarrier in another CTA of the cluster, ordered after
+// this thread's earlier (shared::cluster) writes.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+                 : "memory");
+}
+
+// try_wait that acquires at cluster scope (sees the writes that other CTAs
+// ordered before their arrivals).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_t parity,
+                                                          long long budget) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (clock64() - t0 > budget) return false;
+    }
+}
+
+}  // namespace rmsn

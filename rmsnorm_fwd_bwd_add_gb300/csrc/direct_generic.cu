@@ -9,9 +9,20 @@ namespace rmsn {
 cudaError_t launch_staged_f16(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
 cudaError_t launch_staged_bf16(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
 cudaError_t launch_staged_f32(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
+cudaError_t launch_staged_f16_sh(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
+cudaError_t launch_staged_bf16_sh(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
+cudaError_t launch_staged_f32_sh(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
 
 cudaError_t launch_staged(int dtype, int mode, const Plan &p, const KernelArgs &a,
                           cudaStream_t s) {
+    if (p.shift) {
+        switch (dtype) {
+            case 0: return launch_staged_f16_sh(mode, p, a, s);
+            case 1: return launch_staged_bf16_sh(mode, p, a, s);
+            case 2: return launch_staged_f32_sh(mode, p, a, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (dtype) {
         case 0: return launch_staged_f16(mode, p, a, s);
         case 1: return launch_staged_bf16(mode, p, a, s);
@@ -88,6 +99,20 @@ cudaError_t launch_generic(int dtype, int mode, const Plan &p, const KernelArgs 
         case 0: return generic_t<__half>(mode, p, a, s);
         case 1: return generic_t<__nv_bfloat16>(mode, p, a, s);
         case 2: return generic_t<float>(mode, p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_cluster_f16(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
+cudaError_t launch_cluster_bf16(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
+cudaError_t launch_cluster_f32(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s);
+
+cudaError_t launch_cluster(int dtype, int mode, const Plan &p, const KernelArgs &a,
+                           cudaStream_t s) {
+    switch (dtype) {
+        case 0: return launch_cluster_f16(mode, p, a, s);
+        case 1: return launch_cluster_bf16(mode, p, a, s);
+        case 2: return launch_cluster_f32(mode, p, a, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -1,0 +1,51 @@
+// launch_cluster.cuh -- picks the cluster_kernel instance for a plan.
+#pragma once
+
+#include "cluster.cuh"
+#include "launch_util.h"
+
+namespace rmsn {
+
+template <typename T, int MODE, int NT, int CL>
+cudaError_t launch_cluster_inst(const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    static std::atomic<uint64_t> smem_mask{0};
+    auto kern = cluster_kernel<T, MODE, NT, CL>;
+    cudaError_t e = allow_max_dynamic_smem((const void *)kern, smem_mask);
+    if (e != cudaSuccess) return e;
+    return launch_pdl_cluster(kern, dim3(p.grid), dim3(NT), p.smem, s, CL, a);
+}
+
+template <typename T, int MODE, int NT>
+cudaError_t launch_cluster_cl(const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    switch (p.cl) {
+        case 2: return launch_cluster_inst<T, MODE, NT, 2>(p, a, s);
+        case 4: return launch_cluster_inst<T, MODE, NT, 4>(p, a, s);
+        case 8: return launch_cluster_inst<T, MODE, NT, 8>(p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T, int MODE>
+cudaError_t launch_cluster_mode(const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    switch (p.nt) {
+        case 512: return launch_cluster_cl<T, MODE, 512>(p, a, s);
+        case 1024:
+            // forward only: the VJP's 1024-thread CTA would spill at 64 registers
+            if constexpr (is_vjp(MODE)) return cudaErrorInvalidValue;
+            else return launch_cluster_cl<T, MODE, 1024>(p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t launch_cluster_t(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    switch (mode) {
+        case MODE_FWD_RES: return launch_cluster_mode<T, MODE_FWD_RES>(p, a, s);
+        case MODE_FWD_NORES: return launch_cluster_mode<T, MODE_FWD_NORES>(p, a, s);
+        case MODE_VJP: return launch_cluster_mode<T, MODE_VJP>(p, a, s);
+        case MODE_VJP_ADD: return launch_cluster_mode<T, MODE_VJP_ADD>(p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rmsn

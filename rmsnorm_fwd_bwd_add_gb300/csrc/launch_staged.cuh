@@ -9,11 +9,11 @@
 
 namespace rmsn {
 
-template <typename T, int MODE, int NT, int G, int V, bool GEN>
+template <typename T, int MODE, int NT, int G, int V, bool GEN, bool SH>
 cudaError_t launch_staged_inst(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
     constexpr int MINB = staged_max_ctas_per_sm(MODE, NT, G, V);
     static std::atomic<uint64_t> smem_mask{0};
-    auto kern = staged_kernel<T, MODE, NT, G, V, MINB, GEN>;
+    auto kern = staged_kernel<T, MODE, NT, G, V, MINB, GEN, SH>;
     cudaError_t e = allow_max_dynamic_smem((const void *)kern, smem_mask);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.grid), dim3(NT), p.smem, stream, a);
@@ -32,17 +32,18 @@ inline int tmap_boxes(int64_t D, int es) {
 // The dense instance unless a tensor the mode uses has rows a stride apart
 // or rstd is given.  General sub-warp tiles go through 2-D tensor maps when
 // D splits into boxes (one copy per box instead of one per row), else one
-// bulk copy per row.
+// bulk copy per row.  SH: the shifted-rows instances (dense rows whose
+// tensors share one offset from a 16-byte boundary; the plan says so).
 template <typename T, int MODE, int NT, int G, int V>
-cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
+cudaError_t launch_staged_general(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
     const int64_t D = a.D;
     bool gen = a.rstd != nullptr || a.ld_in0 != D || a.ld_out0 != D;
     if constexpr (input_tensors(MODE) >= 2) gen = gen || a.ld_in1 != D;
     if constexpr (input_tensors(MODE) == 3) gen = gen || a.ld_in2 != D;
     if constexpr (MODE == MODE_FWD_RES) gen = gen || a.ld_out1 != D;
-    if (!gen) return launch_staged_inst<T, MODE, NT, G, V, false>(p, a, stream);
+    if (!gen) return launch_staged_inst<T, MODE, NT, G, V, false, false>(p, a, stream);
     if constexpr (G == NT) {
-        return launch_staged_inst<T, MODE, NT, G, V, true>(p, a, stream);
+        return launch_staged_inst<T, MODE, NT, G, V, true, false>(p, a, stream);
     } else {
         constexpr int es = (int)sizeof(T);
         constexpr int dtype = es == 4 ? 2 : std::is_same<T, __half>::value ? 0 : 1;
@@ -65,46 +66,54 @@ cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t s
                 b.use_tmap = 1;
             }
         }
-        return launch_staged_inst<T, MODE, NT, G, V, true>(p, b, stream);
+        return launch_staged_inst<T, MODE, NT, G, V, true, false>(p, b, stream);
     }
 }
 
-template <typename T, int MODE>
+template <typename T, int MODE, int NT, int G, int V, bool SH>
+cudaError_t launch_staged_one(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
+    if constexpr (SH)
+        return launch_staged_inst<T, MODE, NT, G, V, false, true>(p, a, stream);
+    else
+        return launch_staged_general<T, MODE, NT, G, V>(p, a, stream);
+}
+
+template <typename T, int MODE, bool SH>
 cudaError_t launch_staged_mode(const Plan &p, const KernelArgs &a, cudaStream_t s) {
     static_assert(N_STAGED_CFG == 19, "keep this switch in step with STAGED_CFGS");
     switch (p.cfg) {
-        case 0: return launch_staged_one<T, MODE, 256, 8, 1>(p, a, s);
-        case 1: return launch_staged_one<T, MODE, 256, 16, 1>(p, a, s);
-        case 2: return launch_staged_one<T, MODE, 256, 32, 1>(p, a, s);
-        case 3: return launch_staged_one<T, MODE, 256, 32, 2>(p, a, s);
-        case 4: return launch_staged_one<T, MODE, 256, 32, 3>(p, a, s);
-        case 5: return launch_staged_one<T, MODE, 256, 32, 4>(p, a, s);
-        case 6: return launch_staged_one<T, MODE, 128, 128, 2>(p, a, s);
-        case 7: return launch_staged_one<T, MODE, 256, 256, 2>(p, a, s);
-        case 8: return launch_staged_one<T, MODE, 512, 512, 2>(p, a, s);
-        case 9: return launch_staged_one<T, MODE, 1024, 1024, 2>(p, a, s);
+        case 0: return launch_staged_one<T, MODE, 256, 8, 1, SH>(p, a, s);
+        case 1: return launch_staged_one<T, MODE, 256, 16, 1, SH>(p, a, s);
+        case 2: return launch_staged_one<T, MODE, 256, 32, 1, SH>(p, a, s);
+        case 3: return launch_staged_one<T, MODE, 256, 32, 2, SH>(p, a, s);
+        case 4: return launch_staged_one<T, MODE, 256, 32, 3, SH>(p, a, s);
+        case 5: return launch_staged_one<T, MODE, 256, 32, 4, SH>(p, a, s);
+        case 6: return launch_staged_one<T, MODE, 128, 128, 2, SH>(p, a, s);
+        case 7: return launch_staged_one<T, MODE, 256, 256, 2, SH>(p, a, s);
+        case 8: return launch_staged_one<T, MODE, 512, 512, 2, SH>(p, a, s);
+        case 9: return launch_staged_one<T, MODE, 1024, 1024, 2, SH>(p, a, s);
         case 10:
             if constexpr (is_vjp(MODE)) return cudaErrorInvalidValue;
-            else return launch_staged_one<T, MODE, 256, 256, 4>(p, a, s);
-        case 11: return launch_staged_one<T, MODE, 96, 96, 2>(p, a, s);
-        case 12: return launch_staged_one<T, MODE, 192, 192, 2>(p, a, s);
-        case 13: return launch_staged_one<T, MODE, 384, 384, 2>(p, a, s);
-        case 14: return launch_staged_one<T, MODE, 768, 768, 2>(p, a, s);
-        case 15: return launch_staged_one<T, MODE, 160, 160, 2>(p, a, s);
-        case 16: return launch_staged_one<T, MODE, 224, 224, 2>(p, a, s);
-        case 17: return launch_staged_one<T, MODE, 320, 320, 2>(p, a, s);
-        case 18: return launch_staged_one<T, MODE, 448, 448, 2>(p, a, s);
+            else return launch_staged_one<T, MODE, 256, 256, 4, SH>(p, a, s);
+        case 11: return launch_staged_one<T, MODE, 96, 96, 2, SH>(p, a, s);
+        case 12: return launch_staged_one<T, MODE, 192, 192, 2, SH>(p, a, s);
+        case 13: return launch_staged_one<T, MODE, 384, 384, 2, SH>(p, a, s);
+        case 14: return launch_staged_one<T, MODE, 768, 768, 2, SH>(p, a, s);
+        case 15: return launch_staged_one<T, MODE, 160, 160, 2, SH>(p, a, s);
+        case 16: return launch_staged_one<T, MODE, 224, 224, 2, SH>(p, a, s);
+        case 17: return launch_staged_one<T, MODE, 320, 320, 2, SH>(p, a, s);
+        case 18: return launch_staged_one<T, MODE, 448, 448, 2, SH>(p, a, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <typename T>
+template <typename T, bool SH>
 cudaError_t launch_staged_t(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s) {
     switch (mode) {
-        case MODE_FWD_RES: return launch_staged_mode<T, MODE_FWD_RES>(p, a, s);
-        case MODE_FWD_NORES: return launch_staged_mode<T, MODE_FWD_NORES>(p, a, s);
-        case MODE_VJP: return launch_staged_mode<T, MODE_VJP>(p, a, s);
-        case MODE_VJP_ADD: return launch_staged_mode<T, MODE_VJP_ADD>(p, a, s);
+        case MODE_FWD_RES: return launch_staged_mode<T, MODE_FWD_RES, SH>(p, a, s);
+        case MODE_FWD_NORES: return launch_staged_mode<T, MODE_FWD_NORES, SH>(p, a, s);
+        case MODE_VJP: return launch_staged_mode<T, MODE_VJP, SH>(p, a, s);
+        case MODE_VJP_ADD: return launch_staged_mode<T, MODE_VJP_ADD, SH>(p, a, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -9,7 +9,7 @@
 
 namespace rmsn {
 
-enum Tier : int { TIER_STAGED = 0, TIER_DIRECT = 1, TIER_GENERIC = 2 };
+enum Tier : int { TIER_STAGED = 0, TIER_DIRECT = 1, TIER_GENERIC = 2, TIER_CLUSTER = 3 };
 
 // Kernel arguments.  in0 = x; in1 = residual (forward) or g (VJP);
 // in2 = the gradient of new_residual (fused-op VJP); out0 = out (forward), gx
@@ -46,6 +46,9 @@ struct KernelArgs {
     int box_cols;
     int use_tmap;
     CUtensorMap tmap[3];
+    // Cluster tier: columns of each CTA's slice of a row (a whole number of
+    // 16-byte vectors).
+    int cl_cols;
 };
 
 struct Plan {
@@ -60,7 +63,20 @@ struct Plan {
     int grid;          // CTAs; for the VJP also the number of gw partial rows
     size_t smem;       // dynamic shared memory bytes
     uint32_t stage_bytes;
+    bool shift;        // staged tier: shifted-rows instance (rows off a 16-byte boundary)
+    int cl;            // cluster tier: CTAs per cluster (per row)
+    int cl_cols;       // cluster tier: columns of one CTA's slice
 };
+
+// How a problem's row tensors sit relative to 16-byte boundaries.
+//   ALIGN_VEC:   every row of every tensor (and w) starts on a boundary;
+//   ALIGN_SHIFT: dense rows whose tensors all start at the same offset from a
+//                boundary (an unaligned base, or D * size not a multiple of
+//                16), elements naturally aligned;
+//   ALIGN_VEC_GEN: every row aligned, but rows a stride apart or a per-row
+//                rstd given (the general instances; not the cluster tier);
+//   ALIGN_NONE:  anything else (the element-at-a-time tier).
+enum Align : int { ALIGN_NONE = 0, ALIGN_VEC = 1, ALIGN_SHIFT = 2, ALIGN_VEC_GEN = 3 };
 
 // Configuration tables (index = Plan::cfg).
 struct StagedCfg { int nt, g, v, max_nv; };
@@ -165,6 +181,11 @@ cudaError_t launch_direct(int dtype, int mode, const Plan &plan, const KernelArg
 cudaError_t launch_generic(int dtype, int mode, const Plan &plan, const KernelArgs &a,
                            cudaStream_t stream);
 cudaError_t launch_gw_reduce(const float *partials, float *gw, int P, int D, cudaStream_t stream);
+cudaError_t launch_cluster(int dtype, int mode, const Plan &plan, const KernelArgs &a,
+                           cudaStream_t stream);
+// Clusters of `cl` CTAs (2..8), one CTA per SM, that the current device can
+// hold at once (0 if clusters are unavailable).
+int cluster_capacity(int cl);
 
 // A 2-D tensor map of a [rows, D] tensor with row stride ld elements and
 // boxes of box_cols x box_rows elements, counted in 8-byte units (box rows of

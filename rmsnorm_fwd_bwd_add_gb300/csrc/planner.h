@@ -5,13 +5,18 @@
 // in 16-byte vectors, so the thresholds below are in vectors (nv = D * esize
 // / 16) and bytes; the D figures quoted are for 2-byte elements (fp32 rows
 // reach each threshold at half the D).
-//   * unaligned pointers or row strides, or D * esize not a multiple of 16
-//     -> generic tier;
+//   * rows off 16-byte boundaries: dense rows whose tensors share one offset
+//     take the staged tier's shifted-rows instances (more than DECODE_ROWS
+//     rows), anything else -> generic tier;
 //   * rows <= DECODE_ROWS (decode: one token per sequence)  -> direct tier;
 //   * D <= 16384 -> staged tier (TMA bulk ring): sub-warp/warp per row for
 //     D <= 1024, CTA per row above;
-//   * longer rows -> direct tier (forward up to 32768, VJP up to 16384), then
-//     generic.
+//   * longer aligned rows -> direct tier (forward up to 4096 vectors: one CTA
+//     per row, the row in registers), then the cluster tier (2-8 CTAs per
+//     row, each streaming a slice of it; the VJP from 2048 vectors, up to
+//     8 x 1024, the forward up to 8 x 2048), then generic;
+//   * rows <= DECODE_ROWS of up to 4096 (forward) / 2048 (VJP) vectors ->
+//     direct tier.
 #pragma once
 
 #include <algorithm>
@@ -101,11 +106,32 @@ inline int ring_stages(size_t target, size_t per_stage, int cps) {
     return std::min(MAX_STAGES, 1 + ahead);
 }
 
-inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, int ci, Plan *p) {
+// Vectors of 16 bytes a row spans: with shifted rows, its 16-byte aligned
+// superset at the worst offset (16 - esize bytes).
+inline int64_t row_vectors(int64_t D, int esize, bool shift) {
+    return shift ? ((int64_t)(16 - esize) + D * esize + 15) / 16 : D * esize / 16;
+}
+
+// Bytes of one tensor's stage for `tr` rows (shifted rows: their aligned
+// superset at the worst offset).
+inline size_t stage_bytes_for(int64_t tr, int64_t D, int esize, bool shift) {
+    return shift ? (size_t)(((int64_t)(16 - esize) + tr * D * esize + 15) / 16 * 16)
+                 : (size_t)(tr * D * esize);
+}
+
+// Rows after which a row's offset from a 16-byte boundary repeats.
+inline int shift_period(int64_t D, int esize) {
+    const int64_t rb = (D * esize) % 16;
+    return rb == 0 ? 1 : rb % 8 == 0 ? 2 : rb % 4 == 0 ? 4 : 8;
+}
+
+inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, int ci, bool shift,
+                        Plan *p) {
     const StagedCfg &c = STAGED_CFGS[ci];
     const Tuning &tu = tuning();
     const int ntens = input_tensors(mode);
     const size_t row_bytes = (size_t)D * esize;
+    p->shift = shift;
     const int max_stages = tu.stages ? tu.stages : MAX_STAGES;
     const int cps_max = staged_max_ctas_per_sm(mode, c.nt, c.g, c.v);
     int cps = tu.cps ? std::min(tu.cps, cps_max) : staged_ctas_per_sm(mode, c.nt, c.g, c.v);
@@ -122,8 +148,8 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
         const int64_t want_tiles = (int64_t)sm_count * cps * 2;
         const int64_t rpg =
             std::min(rpg_max, std::max<int64_t>(1, ceil_div(rows, ng * want_tiles)));
-        p->tile_rows = (int)(ng * rpg);
-        p->stage_bytes = (uint32_t)(p->tile_rows * row_bytes);
+        p->tile_rows = (int)(ng * rpg);  // a multiple of 8 rows (shifted rows rely on it)
+        p->stage_bytes = (uint32_t)stage_bytes_for(p->tile_rows, D, esize, shift);
         const size_t per_stage = (size_t)ntens * p->stage_bytes;
         cps = std::min(cps, 2);
         const size_t cap = cps == 2 ? SMEM_TWO_PER_SM : SMEM_ONE_PER_SM;
@@ -149,8 +175,8 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
         // CTAs per SM D = 6144 6045 -> 6231).  The forwards with two or more
         // CTAs per SM keep two (D = 7168: 6230 against 6081 with three).
         p->tile_rows = 1;
-        p->stage_bytes = (uint32_t)row_bytes;
-        const size_t per_stage = (size_t)ntens * row_bytes;
+        p->stage_bytes = (uint32_t)stage_bytes_for(1, D, esize, shift);
+        const size_t per_stage = (size_t)ntens * p->stage_bytes;
         int chosen = 0;
         for (int c = cps; c >= 1 && !chosen; --c) {
             const int64_t sc = (int64_t)(smem_per_cta(c) / per_stage);
@@ -169,17 +195,77 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
     }
     p->num_tiles = ceil_div(rows, p->tile_rows);
     p->grid = (int)std::min<int64_t>(p->num_tiles, (int64_t)sm_count * cps);
+    // Shifted rows, one per tile: a CTA that takes several rows sees the
+    // same offset on all of them when the grid is a multiple of its period.
+    const int period = shift && c.g == c.nt ? shift_period(D, esize) : 1;
+    if (p->grid < p->num_tiles && p->grid % period != 0)
+        p->grid = std::max(period, p->grid - p->grid % period);
     return true;
 }
 
-inline Plan make_plan(int mode, int64_t rows, int D, int esize, bool aligned, int sm_count) {
+// Cluster plan for aligned rows longer than the staged and direct tiers take
+// (VJP: more than 2048 vectors, forward: more than 4096): clusters of 2, 4 or
+// 8 CTAs, each CTA's slice at most 1024 vectors (512 threads) or, for the
+// forward, 2048 (1024 threads), with a ring of at least four slices (two
+// rows are held while the cluster exchanges a row's sums); of the fitting
+// choices, the one that keeps more SMs busy (clusters the device holds at
+// once, cap[cl], times CTAs per cluster); one CTA per SM.
+inline bool plan_cluster(int mode, int64_t rows, int D, int esize, const int *cap, int sm_count,
+                         Plan *p) {
+    const int64_t nv = (int64_t)D * esize / 16;
+    const int ntens = input_tensors(mode);
+    int best_nt = 0, best_cl = 0;
+    int64_t best_sms = 0;
+    for (int nt : {512, 1024}) {
+        if (nt == 1024 && is_vjp(mode)) continue;  // 64 registers: the VJP would spill
+        int cl = 2;  // clusters of 2, 4 or 8 CTAs
+        while (cl <= 8 && (int64_t)cl * 2 * nt < nv) cl *= 2;
+        if (cl > 8) continue;
+        const int64_t slice = (nv + cl - 1) / cl * 16;
+        if ((int64_t)SMEM_ONE_PER_SM / ((int64_t)ntens * slice) < 4) continue;
+        const int64_t clusters = cap ? cap[cl] : sm_count / cl;
+        const int64_t sms = std::min<int64_t>(clusters, rows) * cl;
+        if (clusters > 0 && sms > best_sms) {
+            best_sms = sms;
+            best_nt = nt;
+            best_cl = cl;
+        }
+    }
+    if (!best_cl) return false;
+    const int64_t per_cta_vec = (nv + best_cl - 1) / best_cl;
+    *p = Plan{};
+    p->tier = TIER_CLUSTER;
+    p->nt = best_nt;
+    p->g = best_nt;
+    p->v = 2;
+    p->cl = best_cl;
+    p->cl_cols = (int)(per_cta_vec * 16 / esize);
+    p->tile_rows = 1;
+    p->stage_bytes = (uint32_t)(per_cta_vec * 16);
+    const size_t per_stage = (size_t)ntens * p->stage_bytes;
+    const int64_t sc = (int64_t)(SMEM_ONE_PER_SM / per_stage);
+    const int floor = tuning().stages ? 0 : 4;
+    p->stages = (int)std::min<int64_t>(
+        std::min<int64_t>(tuning().stages ? tuning().stages : MAX_STAGES, sc),
+        std::max(floor, 2 + ring_stages(is_vjp(mode) ? INFLIGHT_VJP : INFLIGHT_FWD, per_stage, 1)));
+    p->smem = 1024 + (size_t)p->stages * per_stage;  // header of the cluster kernel
+    p->num_tiles = rows;
+    const int64_t clusters = cap ? cap[best_cl] : sm_count / best_cl;
+    p->grid = (int)(std::min<int64_t>(clusters, rows) * best_cl);
+    return true;
+}
+
+inline Plan make_plan(int mode, int64_t rows, int D, int esize, int align, int sm_count,
+                      const int *cluster_cap = nullptr) {
     Plan p{};
-    const int nv = (int)((int64_t)D * esize / 16);
-    if (aligned && rows > DECODE_ROWS) {
+    const bool aligned = align == ALIGN_VEC || align == ALIGN_VEC_GEN;
+    const bool shift = align == ALIGN_SHIFT;
+    const int64_t nv = row_vectors(D, esize, shift);
+    if ((aligned || shift) && rows > DECODE_ROWS) {
         const int forced = tuning().cfg;
         if (forced >= 0 && nv <= STAGED_CFGS[forced].max_nv &&
             !(is_vjp(mode) && forced == STAGED_CFG_WIDE) &&
-            plan_staged(mode, rows, D, esize, sm_count, forced, &p))
+            plan_staged(mode, rows, D, esize, sm_count, forced, shift, &p))
             return p;
         // the configuration that fits the row most tightly (the wide one
         // only when tuned)
@@ -188,8 +274,11 @@ inline Plan make_plan(int mode, int64_t rows, int D, int esize, bool aligned, in
             if (ci != STAGED_CFG_WIDE && nv <= STAGED_CFGS[ci].max_nv &&
                 (best < 0 || STAGED_CFGS[ci].max_nv < STAGED_CFGS[best].max_nv))
                 best = ci;
-        if (best >= 0 && plan_staged(mode, rows, D, esize, sm_count, best, &p)) return p;
+        if (best >= 0 && plan_staged(mode, rows, D, esize, sm_count, best, shift, &p)) return p;
     }
+    if (align == ALIGN_VEC && rows > DECODE_ROWS && nv > (is_vjp(mode) ? 2048 : 4096) &&
+        plan_cluster(mode, rows, D, esize, cluster_cap, sm_count, &p))
+        return p;
     if (aligned) {
         for (int ci = 0; ci < N_DIRECT_CFG; ++ci) {
             const DirectCfg &c = DIRECT_CFGS[ci];
@@ -214,7 +303,12 @@ inline Plan make_plan(int mode, int64_t rows, int D, int esize, bool aligned, in
     p.g = GENERIC_NT;
     p.tile_rows = 1;
     p.num_tiles = rows;
-    p.grid = (int)std::min<int64_t>(rows, (int64_t)sm_count * 8);
+    // The VJP's partial rows (one per CTA) stay within 10 % of its bytes
+    // (P * 4 <= 0.1 * 3 * esize * rows) and within two CTAs per SM.
+    p.grid = is_vjp(mode)
+                 ? (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)sm_count * 2,
+                                                               rows * 3 * esize / 40))
+                 : (int)std::min<int64_t>(rows, (int64_t)sm_count * 8);
     return p;
 }
 

@@ -45,7 +45,7 @@
 
 namespace rmsn {
 
-template <typename T, int MODE, int NT, int G, int V, int MINB, bool GEN>
+template <typename T, int MODE, int NT, int G, int V, int MINB, bool GEN, bool SH>
 __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant__ KernelArgs a) {
     constexpr int NWARPS = NT / 32;
     constexpr int WP = NWARPS <= 4 ? 4 : NWARPS <= 8 ? 8 : NWARPS <= 16 ? 16 : 32;
@@ -58,16 +58,20 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     constexpr bool SPREAD_COPIES = GEN && !CTA_ROW;
     // Some VJP instances re-read a row from the stage for their outputs
     // instead of holding it in registers across the reduction (a CTA-per-row
-    // stage is released only at the next row's barrier).
-    constexpr bool RELOAD = staged_reload(MODE, NT, G, V);
+    // stage is released only at the next row's barrier): those staged_reload
+    // names, and the CTA-per-row VJPs of shifted rows, whose edge handling
+    // costs registers (D = 4097 bf16, 320 threads: 8 bytes spilled when held,
+    // 86 registers re-read; 4024 -> 4252 GB/s, 16384 rows).
+    constexpr bool RELOAD = staged_reload(MODE, NT, G, V) || (SH && is_vjp(MODE) && G == NT);
     constexpr int NTENS = input_tensors(MODE);
     constexpr bool VJP = is_vjp(MODE);
     constexpr bool ADD = (MODE == MODE_VJP_ADD);
     static_assert(G <= 32 || G == NT, "a row belongs to at most one warp, or to the whole CTA");
     static_assert(NWARPS <= 32, "one warp total per lane");
+    static_assert(!(SH && GEN), "shifted rows are dense rows");
 
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [MAX_STAGES]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);   // [MAX_STAGES]
     float2 *red = reinterpret_cast<float2 *>(smem + 128);  // [2][NWARPS]
     unsigned char *ring = smem + STAGED_HEADER_BYTES;
 
@@ -79,6 +83,68 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     const int D = a.D;
     const int NV = D / EPV;
     const uint32_t row_bytes = (uint32_t)D * (uint32_t)sizeof(T);
+    // SH ("shifted rows"): every row tensor's rows start at the same offset
+    // from a 16-byte boundary, but not at 0 (an unaligned base, or D * size a
+    // not multiple of 16).  Each row is copied as its 16-byte aligned
+    // superset, so the thread owning 16-byte vector j of that frame reads and
+    // writes aligned vectors; only a row's first and last vectors hold
+    // elements of the neighbouring rows, which are masked.  The grid is a
+    // multiple of the offset's period in rows (and tiles of several rows are
+    // multiples of 8 rows), so all of this thread's rows have the same offset
+    // `shm`: its columns, its w' and its gw accumulators stay fixed.
+    const uint32_t shm =
+        SH ? (uint32_t)(((uintptr_t)a.in0 + (uint64_t)(CTA_ROW ? blockIdx.x : gid) * row_bytes) & 15u)
+           : 0u;
+    const int shm_e = (int)(shm / sizeof(T));                    // the offset in elements
+    const int nvr = SH ? (int)((shm + row_bytes + 15u) >> 4) : NV;  // vectors of one row in its frame
+    // SH: vector vi of a row's frame holds columns vi * EPV - shm_e + e; only
+    // the first and last vectors of a row hold bytes of the neighbouring
+    // rows (an "edge" vector), and which of this thread's vectors those are
+    // is the same on all of its rows.
+    auto is_edge = [&](int vi) {
+        const int c0 = vi * EPV - shm_e;
+        return SH && (c0 < 0 || c0 + EPV > D);
+    };
+    // Bytes [lo, hi) of edge vector vi that belong to the row.
+    auto edge_bytes = [&](int vi, int &lo, int &hi) {
+        const int c0 = vi * EPV - shm_e;
+        lo = max(0, -c0) * (int)sizeof(T);
+        hi = min(EPV, D - c0) * (int)sizeof(T);
+    };
+    // The edge vector with the neighbours' bytes cleared (one AND a word).
+    auto edge_mask = [&](int vi, uint4 v) -> uint4 {
+        int lo, hi;
+        edge_bytes(vi, lo, hi);
+        auto word = [&](int b) -> uint32_t {  // bytes b..b+3 of the vector
+            uint32_t m = 0;
+#pragma unroll
+            for (int k = 0; k < 4; k += (int)(sizeof(T) < 4 ? sizeof(T) : 4))
+                if (b + k >= lo && b + k < hi) m |= (sizeof(T) == 2 ? 0xffffu : 0xffffffffu) << (8 * k);
+            return m;
+        };
+        return make_uint4(v.x & word(0), v.y & word(4), v.z & word(8), v.w & word(12));
+    };
+    // Writes the row's bytes of edge vector v at `dst` (16-byte aligned):
+    // aligned stores of 8, 4 and 2 bytes, at most three.
+    auto store_edge = [&](unsigned char *dst, int vi, const uint4 &v) {
+        int lo, hi;
+        edge_bytes(vi, lo, hi);
+        auto w = [&](int b) { return b < 4 ? v.x : b < 8 ? v.y : b < 12 ? v.z : v.w; };
+        int b = lo;
+        while (b < hi) {
+            if ((b & 7) == 0 && b + 8 <= hi) {
+                *reinterpret_cast<uint2 *>(dst + b) = make_uint2(w(b), w(b + 4));
+                b += 8;
+            } else if ((b & 3) == 0 && b + 4 <= hi) {
+                *reinterpret_cast<uint32_t *>(dst + b) = w(b);
+                b += 4;
+            } else {  // 2-byte elements only
+                const uint32_t x = w(b) >> (8 * (b & 3));
+                *reinterpret_cast<unsigned short *>(dst + b) = (unsigned short)(x & 0xffffu);
+                b += 2;
+            }
+        }
+    };
     const int S = a.stages;
     const int TR = a.tile_rows;
     const int64_t rows = a.rows;
@@ -168,35 +234,53 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
         }
         advance();
     };
+    // The tile starting at row0 (nr rows) of a dense tensor at `base`: its
+    // first byte's offset from a 16-byte boundary (SH; 0 otherwise), and the
+    // bytes of its copy (SH: the aligned superset).
+    auto tile_off = [&](int64_t row0) -> uint32_t {
+        return SH ? (uint32_t)(((uintptr_t)in0 + (uint64_t)row0 * row_bytes) & 15u) : 0u;
+    };
+    auto tile_bytes = [&](int nr, uint32_t off) -> uint32_t {
+        return SH ? ((off + (uint32_t)nr * row_bytes + 15u) & ~15u) : (uint32_t)nr * row_bytes;
+    };
+    auto tile_src = [&](const T *base, int64_t row0, int64_t ld, uint32_t off) {
+        return reinterpret_cast<const unsigned char *>(base + row0 * ld) - off;
+    };
     auto issue_next = [&]() {  // thread 0, the whole tile
         int64_t row0;
         int nr;
         if (tile_of(issued, row0, nr)) {
             uint64_t *bar = &full[issue_stage];
-            const uint32_t bytes = (uint32_t)nr * row_bytes;
-            mbar_arrive_expect_tx(bar, bytes * NTENS);
             if constexpr (!SPREAD_COPIES) {
                 // dense tiles, or CTA per row (one row: one copy per tensor);
                 // straight-line code, as thread 0 is on every row's critical path
+                const uint32_t off = tile_off(row0);
+                const uint32_t bytes = tile_bytes(nr, off);
+                mbar_arrive_expect_tx(bar, bytes * NTENS);
                 const int64_t l0 = GEN ? a.ld_in0 : D, l1 = GEN ? a.ld_in1 : D;
                 const int64_t l2 = GEN ? a.ld_in2 : D;
-                bulk_g2s(stage_ptr(issue_stage, 0), in0 + row0 * l0, bytes, bar, policy);
+                bulk_g2s(stage_ptr(issue_stage, 0), tile_src(in0, row0, l0, off), bytes, bar, policy);
                 if constexpr (NTENS >= 2)
-                    bulk_g2s(stage_ptr(issue_stage, 1), in1 + row0 * l1, bytes, bar, policy);
+                    bulk_g2s(stage_ptr(issue_stage, 1), tile_src(in1, row0, l1, off), bytes, bar,
+                             policy);
                 if constexpr (NTENS == 3)
-                    bulk_g2s(stage_ptr(issue_stage, 2), in2 + row0 * l2, bytes, bar, policy);
+                    bulk_g2s(stage_ptr(issue_stage, 2), tile_src(in2, row0, l2, off), bytes, bar,
+                             policy);
             } else {
+                mbar_arrive_expect_tx(bar, (uint32_t)nr * row_bytes * NTENS);
                 issue_copies(issued, issue_stage, 0, 1);
             }
         }
         advance();
     };
     // Timeout exit: flag it, then wait (bounded) for this CTA's copies that
-    // may still be landing in shared memory before the CTA retires.
-    auto fail = [&](int64_t k) {
+    // may still be landing in shared memory before the CTA retires (at most
+    // the last S issued tiles: an earlier stage was consumed before it was
+    // issued again).
+    auto fail = [&]() {
         if (tid == 0) {
             atomicOr(a.status, DEVSTATUS_WAIT_TIMEOUT);
-            for (int64_t kk = k; kk < issued; ++kk) {
+            for (int64_t kk = max((int64_t)0, issued - S); kk < issued; ++kk) {
                 if ((int64_t)blockIdx.x + kk * grid == a.drop_tile) continue;
                 mbar_wait_bounded(&full[kk % S], (uint32_t)((kk / S) & 1), DEFAULT_WAIT_BUDGET);
             }
@@ -238,9 +322,23 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = gl + j * G;
-            const uint4 wv = vi < NV ? reinterpret_cast<const uint4 *>(a.w)[vi] : make_uint4(0, 0, 0, 0);
             float2 wf[VP];
-            unpack_vec<T>(wv, wf);
+            if constexpr (SH) {
+                // this thread's columns: vi * EPV - shm_e + e (w has its own
+                // alignment; read once per CTA, element by element)
+                const T *wt = static_cast<const T *>(a.w);
+                const int c0 = vi * EPV - shm_e;
+#pragma unroll
+                for (int q = 0; q < VP; ++q) {
+                    const int c = c0 + 2 * q;
+                    wf[q].x = (vi < nvr && c >= 0 && c < D) ? Cvt<T>::load1(wt + c) : 0.f;
+                    wf[q].y = (vi < nvr && c + 1 >= 0 && c + 1 < D) ? Cvt<T>::load1(wt + c + 1) : 0.f;
+                }
+            } else {
+                const uint4 wv =
+                    vi < NV ? reinterpret_cast<const uint4 *>(a.w)[vi] : make_uint4(0, 0, 0, 0);
+                unpack_vec<T>(wv, wf);
+            }
 #pragma unroll
             for (int q = 0; q < VP; ++q) wp[j][q] = f2add(wb2, wf[q]);
         }
@@ -274,10 +372,15 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = gl + j * G;
-            if (vi < NV) {
+            if (vi < nvr) {
                 const int si = SPREAD_COPIES ? col[SPREAD_COPIES ? j : 0] : vi;
-                unpack_vec<T>(r0[si], xa[j]);
-                if constexpr (NTENS >= 2) unpack_vec<T>(r1[si], xb[j]);
+                uint4 u0 = r0[si], u1 = NTENS >= 2 ? r1[si] : u0;
+                if (is_edge(vi)) {  // elements of the neighbouring rows count as zeros
+                    u0 = edge_mask(vi, u0);
+                    u1 = edge_mask(vi, u1);
+                }
+                unpack_vec<T>(u0, xa[j]);
+                if constexpr (NTENS >= 2) unpack_vec<T>(u1, xb[j]);
                 if constexpr (MODE == MODE_FWD_RES) {
 #pragma unroll
                     for (int q = 0; q < VP; ++q) xa[j][q] = f2add(xa[j][q], xb[j][q]);  // h
@@ -300,13 +403,30 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                            const uint4 *r0, const uint4 *r1, const uint4 *r2, int64_t row, float r,
                            float dot) {
         const size_t base0 = (size_t)(row * lo0), base1 = (size_t)(row * lo1);
+        // SH: the rows' aligned frames in the outputs (same offset as the inputs)
+        uint4 *o0 = out0 + base0, *o1 = out1 + base1;
+        if constexpr (SH) {
+            o0 = reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.out0) + row * row_bytes - shm);
+            if constexpr (MODE == MODE_FWD_RES)
+                o1 = reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.out1) + row * row_bytes -
+                                               shm);
+        }
+        // Stores vector vi of a row: whole when it lies inside the row, else
+        // (SH: a row's first and last vectors) only the row's bytes of it.
+        auto store_vec = [&](uint4 *orow, int vi, const float2 (&f)[VP]) {
+            const uint4 v = pack_vec<T>(f);
+            if (is_edge(vi))
+                store_edge(reinterpret_cast<unsigned char *>(orow + vi), vi, v);
+            else
+                st_global(orow + vi, v);
+        };
         const float2 rr = make_float2(r, r);
         const float c = (r * r) * (dot * inv_D);  // r^2 * dot / D
         const float2 nc2 = make_float2(-c, -c);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = gl + j * G;
-            if (vi < NV) {
+            if (vi < nvr) {
                 float2 o[VP];
                 const float2 *xa = xa_in[j], *xb = xb_in[j];
                 float2 ra[VP], rb[VP];
@@ -333,9 +453,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                 } else {
 #pragma unroll
                     for (int q = 0; q < VP; ++q) o[q] = f2mul(f2mul(xa[q], rr), wp[j][q]);
-                    if constexpr (MODE == MODE_FWD_RES) st_global(out1 + base1 + vi, pack_vec<T>(xa_in[j]));
+                    if constexpr (MODE == MODE_FWD_RES) store_vec(o1, vi, xa_in[j]);
                 }
-                st_global(out0 + base0 + vi, pack_vec<T>(o));
+                store_vec(o0, vi, o);
             }
         }
     };
@@ -360,7 +480,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
             // Everyone has finished row k-1 (its stage is free again) and has
             // published row k's warp totals.
             if (__syncthreads_or(!ok)) {
-                fail(k);
+                fail();
                 return;
             }
             if (tid == 0 && k >= 1 && issued < nk) issue_next();
@@ -399,6 +519,13 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
             const uint4 *t0 = reinterpret_cast<const uint4 *>(stage_ptr(s, 0));
             const uint4 *t1 = reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS >= 2 ? 1 : 0));
             const uint4 *t2 = reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS - 1));
+            // Row q of the tile in the stage: q * row_step vectors in (SH: the
+            // aligned vector holding its first byte; the tile's copy starts at
+            // the aligned boundary below its first row)
+            const uint32_t toff = tile_off(row0);
+            auto rstep = [&](int q) -> size_t {
+                return SH ? (size_t)((toff + (uint32_t)q * row_bytes) >> 4) : (size_t)q * row_step;
+            };
             for (int qb = 0; qb < TR; qb += NG) {  // same trip count in every lane
                 const int q = qb + gid;
                 const bool valid = q < nr;
@@ -407,8 +534,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                     if (a.rstd && q + NG < nr) r_next = __ldg(a.rstd + row0 + q + NG);
                 float2 xa[V][VP], xb[V][VP];
                 float sa = 0.f, sb = 0.f;
-                if (valid)
-                    load_row(t0 + (size_t)q * row_step, t1 + (size_t)q * row_step, xa, xb, sa, sb);
+                if (valid) load_row(t0 + rstep(q), t1 + rstep(q), xa, xb, sa, sb);
                 sa = group_sum<G>(sa);
                 if constexpr (VJP) sb = group_sum<G>(sb);
                 if (valid && ok) {
@@ -418,8 +544,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                     } else if constexpr (GEN) {
                         if (a.rstd && gl == 0) a.rstd[row0 + q] = r;
                     }
-                    row_outputs(xa, xb, t0 + (size_t)q * row_step, t1 + (size_t)q * row_step,
-                                t2 + (size_t)q * row_step, row0 + q, r, sb);
+                    row_outputs(xa, xb, t0 + rstep(q), t1 + rstep(q), t2 + rstep(q), row0 + q, r, sb);
                 }
             }
             // Thread 0 has seen the stage's phase complete (ok), so the next
@@ -427,7 +552,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
             if constexpr (SPREAD_COPIES)
                 if (!tmap_mode && tid == 0 && ok && issued < nk) post_expect(issued, issue_stage);
             if (__syncthreads_or(!ok)) {  // the whole tile is consumed
-                fail(k);
+                fail();
                 return;
             }
             if constexpr (SPREAD_COPIES) {
@@ -459,12 +584,27 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                 reinterpret_cast<float4 *>(dst)[u] =
                     make_float4(acc[j][2 * u].x, acc[j][2 * u].y, acc[j][2 * u + 1].x, acc[j][2 * u + 1].y);
         };
+        // SH: this thread's columns of vector j start at vi * EPV - shm_e;
+        // those inside [0, D) are stored one by one.
+        auto store_acc_sh = [&](float *dst_row, int j, int vi) {
+            const int c0 = vi * EPV - shm_e;
+#pragma unroll
+            for (int q = 0; q < VP; ++q) {
+                const int c = c0 + 2 * q;
+                if (c >= 0 && c < D) dst_row[c] = acc[j][q].x;
+                if (c + 1 >= 0 && c + 1 < D) dst_row[c + 1] = acc[j][q].y;
+            }
+        };
         if constexpr (CTA_ROW) {
             // Each column is owned by exactly one thread of the CTA.
 #pragma unroll
             for (int j = 0; j < V; ++j) {
                 const int vi = gl + j * G;
-                if (vi < NV) store_acc(prow + (size_t)vi * EPV, j);
+                if constexpr (SH) {
+                    if (vi < nvr) store_acc_sh(prow, j, vi);
+                } else {
+                    if (vi < NV) store_acc(prow + (size_t)vi * EPV, j);
+                }
             }
         } else {
             // NG groups own the same columns: add their registers in group
@@ -474,7 +614,11 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
 #pragma unroll
             for (int j = 0; j < V; ++j) {
                 const int vi = gl + j * G;
-                if (vi < NV) store_acc(buf + (size_t)gid * D + (size_t)vi * EPV, j);
+                if constexpr (SH) {
+                    if (vi < nvr) store_acc_sh(buf + (size_t)gid * D, j, vi);
+                } else {
+                    if (vi < NV) store_acc(buf + (size_t)gid * D + (size_t)vi * EPV, j);
+                }
             }
             __syncthreads();
             for (int col = tid; col < D; col += NT) {

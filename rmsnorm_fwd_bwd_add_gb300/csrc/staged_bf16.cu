@@ -3,6 +3,6 @@
 
 namespace rmsn {
 cudaError_t launch_staged_bf16(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s) {
-    return launch_staged_t<__nv_bfloat16>(mode, p, a, s);
+    return launch_staged_t<__nv_bfloat16, false>(mode, p, a, s);
 }
 }  // namespace rmsn

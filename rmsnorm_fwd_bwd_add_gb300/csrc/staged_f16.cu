@@ -3,6 +3,6 @@
 
 namespace rmsn {
 cudaError_t launch_staged_f16(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s) {
-    return launch_staged_t<__half>(mode, p, a, s);
+    return launch_staged_t<__half, false>(mode, p, a, s);
 }
 }  // namespace rmsn

@@ -3,6 +3,6 @@
 
 namespace rmsn {
 cudaError_t launch_staged_f32(int mode, const Plan &p, const KernelArgs &a, cudaStream_t s) {
-    return launch_staged_t<float>(mode, p, a, s);
+    return launch_staged_t<float, false>(mode, p, a, s);
 }
 }  // namespace rmsn

@@ -121,9 +121,11 @@ def test_config5_sweep(D, dtype):
 # ---- edge shapes: every tier, ragged tails, maximum sizes ---------------------
 
 EDGE = [
-    # (rows, D): generic (D % 8 != 0), direct (rows <= 8 or long rows),
-    # staged small-D (D <= 1024) and CTA-per-row (1024 < D <= 16384) with
-    # row counts that leave ragged last tiles and uneven CTA loads.
+    # (rows, D): direct (rows <= 8), generic (a few rows off 16-byte
+    # boundaries, rows too long for any vectorised tier), shifted rows (D % 8
+    # != 0 with more than 8 rows), staged small-D (D <= 1024) and CTA-per-row
+    # (1024 < D <= 16384), clusters (aligned rows of more than 2048 vectors),
+    # with row counts that leave ragged last tiles and uneven CTA loads.
     (1, 1), (3, 7), (2, 9), (5, 255), (9, 257), (17, 263), (33, 1000),
     (1, 8), (8, 64), (9, 64), (1000, 64), (301, 128), (157, 256), (999, 264),
     (4099, 520), (613, 1024), (2, 1032), (311, 1032), (305, 2048), (307, 4104),
@@ -334,6 +336,27 @@ def test_wait_timeout_is_reported_and_context_survives():
     assert rn.rmsnorm_device_status(clear=True) == 0
 
 
+def test_vjp_wait_timeout_is_reported_and_context_survives():
+    """The CTA-per-row VJP's row loop has no CTA barrier: a tile whose copy
+    never arrives (dropped by the host-side hook) times out in every warp of
+    that CTA, the timeout bit is set, and the next call is correct."""
+    case = W.random_case(2000, 4096, torch.bfloat16, seed=5, residual=False)
+    x, w, g = _dev(case.x), _dev(case.w), _dev(case.g)
+    plan = rn.rmsnorm_describe_dispatch("vjp", 2000, 4096, case.dtype)
+    assert plan.startswith("staged") and ":g256:" in plan, plan
+    grid = int(plan.split(":grid")[1].split(":")[0])
+    rn.rmsnorm_device_status(clear=True)
+    rn.rmsnorm_debug_inject(drop_tile=grid + 3, budget_cycles=2_000_000)  # CTA 3's second row
+    try:
+        rn.rmsnorm_vjp(x, w, g, case.eps, case.weight_bias)
+        bits = rn.rmsnorm_device_status(clear=True)
+    finally:
+        rn.rmsnorm_debug_inject(-1, 0)
+    assert bits & rn.DEVSTATUS_WAIT_TIMEOUT
+    check_vjp(case, case.x)
+    assert rn.rmsnorm_device_status(clear=True) == 0
+
+
 def test_injected_scratch_allocation_failure():
     """A failed gw scratch allocation (made on the host by the test hook, the
     allocator is not called) returns RMSNORM_ERR_NO_MEMORY with nothing
@@ -367,3 +390,29 @@ def test_injected_scratch_allocation_failure():
     want_gx1, want_gw1 = oracle_vjp(one.x, one)
     assert_close("one row gx", gx1, want_gx1)
     assert_close("one row gw", gw1, want_gw1, torch.float32)
+
+
+def test_bound_calls_match_the_oracle():
+    """rmsnorm_fwd_bind / rmsnorm_vjp_bind (tensors checked once, the call
+    issued on every invocation) on a decode step: the same bits as the plain
+    calls, checked against the oracle, after several invocations."""
+    case = W.config2(8, 4096, True)
+    x, res, w, g = _dev(case.x), _dev(case.residual), _dev(case.w), _dev(case.g)
+    fwd = rn.rmsnorm_fwd_bind(x, w, case.eps, case.weight_bias, res)
+    for _ in range(3):
+        out, nr = fwd()
+    ref_out, ref_nr = rn.rmsnorm_fwd(x, w, case.eps, case.weight_bias, res)
+    assert torch.equal(out, ref_out) and torch.equal(nr, ref_nr)
+    want_out, want_h = oracle_fwd(case)
+    assert_close("bound out", out, want_out)
+    xr = _dev(rounded_h(want_h, case.dtype))
+    vjp = rn.rmsnorm_vjp_bind(xr, w, g, case.eps, case.weight_bias)
+    for _ in range(3):
+        gx, gw = vjp()
+    ref_gx, ref_gw = rn.rmsnorm_vjp(xr, w, g, case.eps, case.weight_bias)
+    assert torch.equal(gx, ref_gx) and torch.equal(gw.view(torch.int32), ref_gw.view(torch.int32))
+    want_gx, want_gw = oracle_vjp(xr.cpu(), case)
+    assert_close("bound gx", gx, want_gx)
+    assert_close("bound gw", gw, want_gw, torch.float32)
+    with pytest.raises(ValueError):
+        rn.rmsnorm_fwd_bind(x.cpu(), w, case.eps)

@@ -43,11 +43,27 @@ def plans(tmp_path_factory):
     return cfgs, rows
 
 
+def _cluster_fits(mode, nv):
+    """Whether a cluster of at most 8 CTAs (slices of up to 1024 vectors, or
+    2048 for the forward) covers a row of nv vectors with four stages of its
+    slices in one SM's shared memory."""
+    ntens = 1 if mode == 1 else 3 if mode == 3 else 2
+    for nt in ((512,) if mode >= 2 else (512, 1024)):
+        cl = 2
+        while cl <= 8 and cl * 2 * nt < nv:
+            cl *= 2
+        if cl <= 8 and (225 * 1024) // (ntens * (-(-nv // cl) * 16)) >= 4:
+            return True
+    return False
+
+
 def test_tiers_and_configurations(plans):
     cfgs, rows = plans
     assert len(rows) > 1000
     for (mode, es, D, R, tier, cfg, nt, g, v, max_nv, stages, tr, ntiles, grid, smem, sb,
-         max_ctas) in rows:
+         max_ctas, align, shift, cl, cl_cols) in rows:
+        if align == 2:
+            continue  # shifted rows: test_shifted_plans
         nv = D * es // 16
         vjp = mode >= 2
         if R > 8 and nv <= 2048:
@@ -56,9 +72,13 @@ def test_tiers_and_configurations(plans):
             fits = [c for c, (_, _, _, mx) in cfgs.items() if c != WIDE and nv <= mx]
             assert cfg == min(fits, key=lambda c: cfgs[c][3]), (D, es, cfg)
             assert (nt, g, v, max_nv) == cfgs[cfg]
+        elif R > 8 and not vjp and nv <= 4096:
+            assert tier == 1, (mode, es, D, R)  # the row in one CTA's registers
+        elif R > 8 and _cluster_fits(mode, nv):
+            assert tier == 3, (mode, es, D, R)  # a cluster of CTAs per row
         elif R <= 8 and nv <= (2048 if vjp else 4096):
             assert tier == 1, (mode, es, D, R)
-        elif nv > (2048 if vjp else 4096):
+        else:
             assert tier == 2, (mode, es, D, R)
 
 
@@ -66,7 +86,7 @@ def test_staged_plans_fit_the_hardware(plans):
     _, rows = plans
     n = 0
     for (mode, es, D, R, tier, cfg, nt, g, v, max_nv, stages, tr, ntiles, grid, smem, sb,
-         max_ctas) in rows:
+         max_ctas, align, shift, cl, cl_cols) in rows:
         if tier != 0:
             continue
         n += 1
@@ -74,7 +94,10 @@ def test_staged_plans_fit_the_hardware(plans):
         where = (mode, es, D, R)
         assert 2 <= stages <= 8, where
         assert tr >= 1 and (g == nt and tr == 1 or tr % (nt // g) == 0), where
-        assert sb == tr * D * es and sb % 16 == 0, where
+        if align == 1:
+            assert not shift and sb == tr * D * es and sb % 16 == 0, where
+        else:  # the aligned superset of the tile at the worst offset
+            assert shift and sb % 16 == 0 and sb >= 16 - es + tr * D * es, where
         assert ntens * sb <= TX_LIMIT, where             # one tile's bytes on one mbarrier
         assert smem >= HEADER + stages * ntens * sb, where
         if mode >= 2 and g < nt:                          # the cross-group gw sum reuses the ring
@@ -92,7 +115,7 @@ def test_staged_plans_fit_the_hardware(plans):
 
 def test_plan_is_a_pure_function(plans, tmp_path):
     _, rows = plans
-    again = {tuple(r[:4]): r[4:] for r in rows}
+    again = {tuple(r[:4]) + (r[17],): r[4:] for r in rows}
     assert len(again) == len(rows)  # one plan per (mode, esize, D, rows)
 
 
@@ -108,7 +131,7 @@ def test_ring_depth_floor(plans):
     _, rows = plans
     n = 0
     for (mode, es, D, R, tier, cfg, nt, g, v, max_nv, stages, tr, ntiles, grid, smem, sb,
-         max_ctas) in rows:
+         max_ctas, align, shift, cl, cl_cols) in rows:
         if tier != 0 or g != nt or R < 16384:
             continue
         cps = grid // SM
@@ -125,7 +148,7 @@ def test_reread_vjp_ctas_per_sm(plans):
     _, rows = plans
     seen = set()
     for (mode, es, D, R, tier, cfg, nt, g, v, max_nv, stages, tr, ntiles, grid, smem, sb,
-         max_ctas) in rows:
+         max_ctas, align, shift, cl, cl_cols) in rows:
         if tier != 0 or g != nt or mode < 2:
             continue
         if nt in (384, 448):
@@ -135,3 +158,68 @@ def test_reread_vjp_ctas_per_sm(plans):
             assert max_ctas == 1, (mode, es, D, nt)
             seen.add(nt)
     assert seen == {384, 448, 512}
+
+
+def _period(D, es):
+    """Rows after which a dense row's offset from a 16-byte boundary repeats."""
+    rb = D * es % 16
+    return 1 if rb == 0 else 2 if rb % 8 == 0 else 4 if rb % 4 == 0 else 8
+
+
+def test_shifted_plans(plans):
+    """Rows off 16-byte boundaries: the staged tier when the superset of a row
+    (worst offset) fits a configuration, the configuration that fits it most
+    tightly, sub-warp tiles of a multiple of 8 rows, and CTAs that take
+    several rows on a grid that is a multiple of the offset's period (so a
+    CTA sees one offset on all of its rows)."""
+    cfgs, rows = plans
+    n = 0
+    for (mode, es, D, R, tier, cfg, nt, g, v, max_nv, stages, tr, ntiles, grid, smem, sb,
+         max_ctas, align, shift, cl, cl_cols) in rows:
+        if align != 2:
+            continue
+        where = (mode, es, D, R)
+        nvs = -(-(16 - es + D * es) // 16)
+        if R > 8 and nvs <= 2048:
+            n += 1
+            assert tier == 0 and shift, where
+            fits = [c for c, (_, _, _, mx) in cfgs.items() if c != WIDE and nvs <= mx]
+            assert cfg == min(fits, key=lambda c: cfgs[c][3]), where
+            assert g * v >= nvs, where
+            if g < nt:
+                assert tr % 8 == 0, where
+            elif grid < ntiles:
+                assert grid % _period(D, es) == 0, where
+        else:
+            assert tier != 0 and not shift, where
+    assert n > 300
+
+
+def test_cluster_plans(plans):
+    """Rows of more than 2048 (VJP) or 4096 (forward) vectors: clusters of 2, 4
+    or 8 CTAs whose slices (whole 16-byte vectors, at most 1024 a CTA for the
+    VJP and 2048 for the forward) cover the row with no CTA left empty, one
+    CTA per SM, rings of at least four stages that fit one SM's shared
+    memory, and a grid of whole clusters (without a device query: SMs // cl
+    clusters at most)."""
+    _, rows = plans
+    n = 0
+    for (mode, es, D, R, tier, cfg, nt, g, v, max_nv, stages, tr, ntiles, grid, smem, sb,
+         max_ctas, align, shift, cl, cl_cols) in rows:
+        if tier != 3:
+            continue
+        n += 1
+        where = (mode, es, D, R)
+        nv = D * es // 16
+        ntens = 1 if mode == 1 else 3 if mode == 3 else 2
+        assert align == 1 and R > 8 and nv > (2048 if mode >= 2 else 4096), where
+        assert cl in (2, 4, 8) and nt in (512, 1024) and not (mode >= 2 and nt == 1024), where
+        assert cl_cols * es % 16 == 0, where
+        slice_v = cl_cols * es // 16
+        assert slice_v <= 2 * nt and cl * slice_v >= nv and (cl - 1) * slice_v < nv, where
+        assert sb == cl_cols * es, where
+        assert 4 <= stages <= 8 and smem == 1024 + stages * ntens * sb, where
+        assert smem + RESERVED_PER_CTA <= SMEM_PER_SM and smem <= SMEM_PER_CTA, where
+        assert ntiles == R and grid % cl == 0 and grid // cl == min(R, SM // cl), where
+        assert ntens * sb <= TX_LIMIT, where
+    assert n > 30
