@@ -278,11 +278,12 @@ int rmsnorm_rope_kv_append(const void *q, const void *k, const void *v,
  *     rows up to D = 32768 whose tensors start on 16-byte boundaries (at most
  *     912 partial rows of D <= 1536, 152 rows of D <= 16384, and one row per
  *     cluster, at most 76, beyond), and dense rows whose tensors all start at
- *     one shared offset from a boundary up to D = 16377 (fp16/bf16) or 8189
+ *     one shared offset from a boundary up to D = 16383 (fp16/bf16) or 8191
  *     (fp32).  Anything else (tensors at different offsets, strided rows off
  *     boundaries, longer rows) runs on the element-at-a-time tier with
- *     min(2 x SMs, rows * 3 * size / 40) partial rows, which fit while
- *     that count x D x 4 bytes <= 16 MiB (e.g. D <= 13,797 at 2,000+ rows).
+ *     max(min(rows, 8), min(2 x SMs, rows * 3 * size / 40)) partial rows,
+ *     which fit while that count x D x 4 bytes <= 16 MiB (e.g. D <= 13,797
+ *     at 2,000 or more rows).
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
  *   - Sharing: every call on a device uses the same array, and it keeps the

@@ -35,11 +35,13 @@ namespace rmsn {
 
 constexpr int CLUSTER_HEADER_BYTES = 1024;
 constexpr int CLUSTER_MAX = 8;  // portable cluster size
+constexpr int CLUSTER_NT = 512; // threads of a cluster CTA (one CTA per SM)
 
-// NT threads (512, or 1024 for the forward), two vectors each.
-template <typename T, int MODE, int NT, int CL>
+// NT threads, up to V 16-byte vectors of the slice each (the slice is at
+// most NT * V vectors); PIPE: the exchange of a row's sums overlaps the next
+// row (four or more stages), else one row at a time (three).
+template <typename T, int MODE, int NT, int V, int CL, bool PIPE>
 __global__ void __launch_bounds__(NT, 1) cluster_kernel(const __grid_constant__ KernelArgs a) {
-    constexpr int V = 2;  // 16-byte vectors of the slice per thread
     constexpr int NWARPS = NT / 32;
     constexpr int WP = NWARPS <= 4 ? 4 : NWARPS <= 8 ? 8 : NWARPS <= 16 ? 16 : 32;
     constexpr int VP = vec_pairs<T>();
@@ -145,6 +147,7 @@ __global__ void __launch_bounds__(NT, 1) cluster_kernel(const __grid_constant__ 
 #pragma unroll
         for (int q = 0; q < VP; ++q) acc[j][q] = make_float2(0.f, 0.f);
 
+    constexpr int RD = 4;  // slots of slice sums (and their barriers)
     // Iteration k: A(k) = row k's slice sums, reduced in the CTA and sent to
     // the cluster; B(k-1) = row k-1's outputs, once every CTA's sums of that
     // row have arrived, with the slice re-read from its stage.  The cluster
@@ -155,8 +158,8 @@ __global__ void __launch_bounds__(NT, 1) cluster_kernel(const __grid_constant__ 
     // every CTA's sums of row k + 2, which this CTA sends after its B(k):
     // RD = 4 slots never overwrite sums still to be read, and no slot
     // barrier runs two phases ahead of a waiter.
-    constexpr int RD = 4;
     bool ok = true;
+    if constexpr (PIPE) {
     for (int64_t k = 0; k <= nk; ++k) {
         if (k < nk) {
             const int sk = (int)(k % S);
@@ -262,6 +265,107 @@ __global__ void __launch_bounds__(NT, 1) cluster_kernel(const __grid_constant__ 
                 }
             }
         }
+    }
+    } else {
+    // PIPE = false: row k's sums, the exchange and its outputs in one
+    // iteration; the stage of row k-1 is refilled after iteration k's
+    // barrier, so three stages suffice (and slices of four vectors a thread
+    // fit where four stages of them would not).  The row is held in
+    // registers across the exchange, or re-read from its stage when four
+    // vectors of x and g would not fit them (the VJP).
+    for (int64_t k = 0; k < nk; ++k) {
+        const int sk = (int)(k % S);
+        const int64_t row = cid + k * ncl;
+        ok = ok && mbar_wait_bounded(&full[sk], (uint32_t)((k / S) & 1), a.wait_budget);
+        const uint4 *r0 = reinterpret_cast<const uint4 *>(stage_ptr(sk, 0));
+        const uint4 *r1 = reinterpret_cast<const uint4 *>(stage_ptr(sk, NTENS >= 2 ? 1 : 0));
+        const uint4 *r2 = reinterpret_cast<const uint4 *>(stage_ptr(sk, NTENS - 1));
+        float2 xa[V][VP], xb[V][VP];
+        float2 s2 = make_float2(0.f, 0.f), d2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int vi = tid + j * NT;
+            if (vi < NVS) {
+                unpack_vec<T>(r0[vi], xa[j]);
+                if constexpr (NTENS >= 2) unpack_vec<T>(r1[vi], xb[j]);
+                if constexpr (MODE == MODE_FWD_RES) {
+#pragma unroll
+                    for (int q = 0; q < VP; ++q) xa[j][q] = f2add(xa[j][q], xb[j][q]);
+                }
+#pragma unroll
+                for (int q = 0; q < VP; ++q) s2 = f2fma(xa[j][q], xa[j][q], s2);
+                if constexpr (VJP) {
+#pragma unroll
+                    for (int q = 0; q < VP; ++q) d2 = f2fma(f2mul(xb[j][q], wp[j][q]), xa[j][q], d2);
+                }
+            }
+        }
+        const float sa = group_sum<32>(s2.x + s2.y);
+        const float sb = VJP ? group_sum<32>(d2.x + d2.y) : 0.f;
+        if (lane == 0) red[(k & 1) * NWARPS + warp] = make_float2(sa, sb);
+        if (__syncthreads_or(!ok)) break;
+        if (tid == 0 && k >= 1 && issued < nk) issue_next();  // into row k-1's stage
+        const float2 *rb = red + (k & 1) * NWARPS;
+        const int wl = lane & (WP - 1);
+        float2 tot = wl < NWARPS ? rb[wl] : make_float2(0.f, 0.f);
+        tot.x = group_sum<WP>(tot.x);
+        if constexpr (VJP) tot.y = group_sum<WP>(tot.y);
+        const int p = (int)(k % RD);
+        if (tid < CL) {
+            dsmem_store_f2(dsmem_addr(&cred[p * CL + rank], (uint32_t)tid), tot);
+            mbar_arrive_remote(dsmem_addr(&clbar[p], (uint32_t)tid));
+        }
+        ok = ok && mbar_wait_cluster_bounded(&clbar[p], (uint32_t)((k / RD) & 1), a.wait_budget);
+        if (ok) {
+            float ss = 0.f, dot = 0.f;
+#pragma unroll
+            for (int q = 0; q < CL; ++q) {
+                const float2 c = cred[p * CL + q];
+                ss += c.x;
+                dot += c.y;
+            }
+            const float r = rsqrtf(ss * inv_D + eps);
+            const float2 rr = make_float2(r, r);
+            const float cc = (r * r) * (dot * inv_D);
+            const float2 nc2 = make_float2(-cc, -cc);
+            const size_t base = (size_t)row * (size_t)NVR + (size_t)vc0;
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                const int vi = tid + j * NT;
+                if (vi < NVS) {
+                    float2 o[VP];
+                    constexpr bool RELOAD = VJP && V > 2;
+                    float2 ra[VP], rbv[VP];
+                    const float2 *xj = xa[j], *gj = xb[j];
+                    if constexpr (RELOAD) {
+                        unpack_vec<T>(r0[vi], ra);
+                        unpack_vec<T>(r1[vi], rbv);
+                        xj = ra;
+                        gj = rbv;
+                    }
+                    if constexpr (VJP) {
+#pragma unroll
+                        for (int q = 0; q < VP; ++q) {
+                            const float2 u = f2mul(gj[q], wp[j][q]);
+                            o[q] = f2mul(f2fma(xj[q], nc2, u), rr);
+                            acc[j][q] = f2fma(gj[q], f2mul(xj[q], rr), acc[j][q]);
+                        }
+                        if constexpr (ADD) {
+                            float2 gr[VP];
+                            unpack_vec<T>(r2[vi], gr);
+#pragma unroll
+                            for (int q = 0; q < VP; ++q) o[q] = f2add(o[q], gr[q]);
+                        }
+                    } else {
+                        if constexpr (MODE == MODE_FWD_RES) st_global(out1 + base + vi, pack_vec<T>(xa[j]));
+#pragma unroll
+                        for (int q = 0; q < VP; ++q) o[q] = f2mul(f2mul(xa[j][q], rr), wp[j][q]);
+                    }
+                    st_global(out0 + base + vi, pack_vec<T>(o));
+                }
+            }
+        }
+    }
     }
     const bool failed = __syncthreads_or(!ok);
     if (failed) {

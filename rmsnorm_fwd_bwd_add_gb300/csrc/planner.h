@@ -13,8 +13,8 @@
 //     D <= 1024, CTA per row above;
 //   * longer aligned rows -> direct tier (forward up to 4096 vectors: one CTA
 //     per row, the row in registers), then the cluster tier (2-8 CTAs per
-//     row, each streaming a slice of it; the VJP from 2048 vectors, up to
-//     8 x 1024, the forward up to 8 x 2048), then generic;
+//     row, each streaming a slice of up to 2048 vectors, four stages of which
+//     fit one SM), then generic;
 //   * rows <= DECODE_ROWS of up to 4096 (forward) / 2048 (VJP) vectors ->
 //     direct tier.
 #pragma once
@@ -106,11 +106,9 @@ inline int ring_stages(size_t target, size_t per_stage, int cps) {
     return std::min(MAX_STAGES, 1 + ahead);
 }
 
-// Vectors of 16 bytes a row spans: with shifted rows, its 16-byte aligned
-// superset at the worst offset (16 - esize bytes).
-inline int64_t row_vectors(int64_t D, int esize, bool shift) {
-    return shift ? ((int64_t)(16 - esize) + D * esize + 15) / 16 : D * esize / 16;
-}
+// Whole 16-byte vectors a row holds at most (shifted rows: a row off a
+// boundary holds one fewer or as many, its edge elements handled apart).
+inline int64_t row_vectors(int64_t D, int esize) { return D * esize / 16; }
 
 // Bytes of one tensor's stage for `tr` rows (shifted rows: their aligned
 // superset at the worst offset).
@@ -205,29 +203,36 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
 
 // Cluster plan for aligned rows longer than the staged and direct tiers take
 // (VJP: more than 2048 vectors, forward: more than 4096): clusters of 2, 4 or
-// 8 CTAs, each CTA's slice at most 1024 vectors (512 threads) or, for the
-// forward, 2048 (1024 threads), with a ring of at least four slices (two
-// rows are held while the cluster exchanges a row's sums); of the fitting
-// choices, the one that keeps more SMs busy (clusters the device holds at
-// once, cap[cl], times CTAs per cluster); one CTA per SM.
+// 8 CTAs of 512 threads, one per SM, each CTA's slice a whole number of
+// vectors, at most 1024 (two a thread) or 2048 (four), with a ring of at
+// least three slices (four or more: the row loop overlaps a row's exchange
+// with the next row, which measured faster wherever they fit: 2000 x 40000
+// bf16 VJP 2815 -> 3276 GB/s, D = 24576 3431 -> 4051; three: one row at a
+// time, which lets four-vector slices fit: D = 32768 3210 -> 4063, 65536
+// 2198 -> 2741).  Of the fitting sizes, the one with the most SMs busy (clusters the
+// device holds at once, cap[cl], times CTAs per cluster), counting a CTA
+// whose threads get fewer than two vectors a row as that fraction of an SM:
+// the per-row work of reducing and exchanging is not amortised over less
+// (2000 x 40000 bf16 VJP, 8 CTAs of 625 vectors: 1.2 a thread, 30 % of the
+// copy bandwidth).
 inline bool plan_cluster(int mode, int64_t rows, int D, int esize, const int *cap, int sm_count,
                          Plan *p) {
     const int64_t nv = (int64_t)D * esize / 16;
     const int ntens = input_tensors(mode);
-    int best_nt = 0, best_cl = 0;
-    int64_t best_sms = 0;
-    for (int nt : {512, 1024}) {
-        if (nt == 1024 && is_vjp(mode)) continue;  // 64 registers: the VJP would spill
-        int cl = 2;  // clusters of 2, 4 or 8 CTAs
-        while (cl <= 8 && (int64_t)cl * 2 * nt < nv) cl *= 2;
-        if (cl > 8) continue;
-        const int64_t slice = (nv + cl - 1) / cl * 16;
-        if ((int64_t)SMEM_ONE_PER_SM / ((int64_t)ntens * slice) < 4) continue;
+    constexpr int NT = 512;
+    int best_cl = 0;
+    double best = 0.0;
+    for (int cl : {2, 4, 8}) {
+        const int64_t slice = (nv + cl - 1) / cl;  // vectors of one CTA's slice
+        if (slice > 4 * NT) continue;
+        if ((int64_t)SMEM_ONE_PER_SM / ((int64_t)ntens * slice * 16) < 3) continue;
         const int64_t clusters = cap ? cap[cl] : sm_count / cl;
-        const int64_t sms = std::min<int64_t>(clusters, rows) * cl;
-        if (clusters > 0 && sms > best_sms) {
-            best_sms = sms;
-            best_nt = nt;
+        if (clusters <= 0) continue;
+        const double per_thread = (double)slice / NT;
+        const double score = (double)(std::min<int64_t>(clusters, rows) * cl) *
+                             std::min(1.0, per_thread / 2.0);
+        if (score > best) {
+            best = score;
             best_cl = cl;
         }
     }
@@ -235,19 +240,22 @@ inline bool plan_cluster(int mode, int64_t rows, int D, int esize, const int *ca
     const int64_t per_cta_vec = (nv + best_cl - 1) / best_cl;
     *p = Plan{};
     p->tier = TIER_CLUSTER;
-    p->nt = best_nt;
-    p->g = best_nt;
-    p->v = 2;
+    p->nt = NT;
+    p->g = NT;
+    p->v = per_cta_vec <= 2 * NT ? 2 : 4;
     p->cl = best_cl;
     p->cl_cols = (int)(per_cta_vec * 16 / esize);
     p->tile_rows = 1;
     p->stage_bytes = (uint32_t)(per_cta_vec * 16);
     const size_t per_stage = (size_t)ntens * p->stage_bytes;
+    // Four stages or more: the kernel overlaps a row's exchange with the next
+    // row (two rows held, the rest in flight); three: one row at a time.
     const int64_t sc = (int64_t)(SMEM_ONE_PER_SM / per_stage);
-    const int floor = tuning().stages ? 0 : 4;
-    p->stages = (int)std::min<int64_t>(
-        std::min<int64_t>(tuning().stages ? tuning().stages : MAX_STAGES, sc),
-        std::max(floor, 2 + ring_stages(is_vjp(mode) ? INFLIGHT_VJP : INFLIGHT_FWD, per_stage, 1)));
+    p->stages = sc >= 4 ? (int)std::min<int64_t>(
+                              std::min<int64_t>(MAX_STAGES, sc),
+                              std::max(4, 2 + ring_stages(is_vjp(mode) ? INFLIGHT_VJP : INFLIGHT_FWD,
+                                                          per_stage, 1)))
+                        : 3;
     p->smem = 1024 + (size_t)p->stages * per_stage;  // header of the cluster kernel
     p->num_tiles = rows;
     const int64_t clusters = cap ? cap[best_cl] : sm_count / best_cl;
@@ -260,7 +268,7 @@ inline Plan make_plan(int mode, int64_t rows, int D, int esize, int align, int s
     Plan p{};
     const bool aligned = align == ALIGN_VEC || align == ALIGN_VEC_GEN;
     const bool shift = align == ALIGN_SHIFT;
-    const int64_t nv = row_vectors(D, esize, shift);
+    const int64_t nv = row_vectors(D, esize);
     if ((aligned || shift) && rows > DECODE_ROWS) {
         const int forced = tuning().cfg;
         if (forced >= 0 && nv <= STAGED_CFGS[forced].max_nv &&
@@ -304,10 +312,12 @@ inline Plan make_plan(int mode, int64_t rows, int D, int esize, int align, int s
     p.tile_rows = 1;
     p.num_tiles = rows;
     // The VJP's partial rows (one per CTA) stay within 10 % of its bytes
-    // (P * 4 <= 0.1 * 3 * esize * rows) and within two CTAs per SM.
+    // (P * 4 <= 0.1 * 3 * esize * rows) and within two CTAs per SM, but a
+    // decode-sized VJP keeps a CTA per row (at most 8 partial rows).
     p.grid = is_vjp(mode)
-                 ? (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)sm_count * 2,
-                                                               rows * 3 * esize / 40))
+                 ? (int)std::max<int64_t>(std::min<int64_t>(rows, DECODE_ROWS),
+                                          std::min<int64_t>((int64_t)sm_count * 2,
+                                                            rows * 3 * esize / 40))
                  : (int)std::min<int64_t>(rows, (int64_t)sm_count * 8);
     return p;
 }

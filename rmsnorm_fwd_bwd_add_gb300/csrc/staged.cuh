@@ -86,64 +86,27 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     // SH ("shifted rows"): every row tensor's rows start at the same offset
     // from a 16-byte boundary, but not at 0 (an unaligned base, or D * size a
     // not multiple of 16).  Each row is copied as its 16-byte aligned
-    // superset, so the thread owning 16-byte vector j of that frame reads and
-    // writes aligned vectors; only a row's first and last vectors hold
-    // elements of the neighbouring rows, which are masked.  The grid is a
-    // multiple of the offset's period in rows (and tiles of several rows are
-    // multiples of 8 rows), so all of this thread's rows have the same offset
-    // `shm`: its columns, its w' and its gw accumulators stay fixed.
+    // superset.  Its first `hd` elements (before the first boundary) and its
+    // last ones (after the last whole vector) are the row's edge elements,
+    // at most 14; between them lie NB whole, aligned vectors, which the
+    // threads own exactly as they own an aligned row's vectors (the same
+    // configuration; one vector on from the copy's start when the row is
+    // offset).  Edge element i belongs to lane G - 1 - i of the row's group
+    // (the CTA's last lanes), read and written one element at a time.  The
+    // grid is a multiple of the offset's period in rows (and tiles of several
+    // rows are multiples of 8 rows), so all of a thread's rows have the same
+    // offset `shm`: its columns, its w' and its gw accumulators stay fixed.
     const uint32_t shm =
         SH ? (uint32_t)(((uintptr_t)a.in0 + (uint64_t)(CTA_ROW ? blockIdx.x : gid) * row_bytes) & 15u)
            : 0u;
-    const int shm_e = (int)(shm / sizeof(T));                    // the offset in elements
-    const int nvr = SH ? (int)((shm + row_bytes + 15u) >> 4) : NV;  // vectors of one row in its frame
-    // SH: vector vi of a row's frame holds columns vi * EPV - shm_e + e; only
-    // the first and last vectors of a row hold bytes of the neighbouring
-    // rows (an "edge" vector), and which of this thread's vectors those are
-    // is the same on all of its rows.
-    auto is_edge = [&](int vi) {
-        const int c0 = vi * EPV - shm_e;
-        return SH && (c0 < 0 || c0 + EPV > D);
-    };
-    // Bytes [lo, hi) of edge vector vi that belong to the row.
-    auto edge_bytes = [&](int vi, int &lo, int &hi) {
-        const int c0 = vi * EPV - shm_e;
-        lo = max(0, -c0) * (int)sizeof(T);
-        hi = min(EPV, D - c0) * (int)sizeof(T);
-    };
-    // The edge vector with the neighbours' bytes cleared (one AND a word).
-    auto edge_mask = [&](int vi, uint4 v) -> uint4 {
-        int lo, hi;
-        edge_bytes(vi, lo, hi);
-        auto word = [&](int b) -> uint32_t {  // bytes b..b+3 of the vector
-            uint32_t m = 0;
-#pragma unroll
-            for (int k = 0; k < 4; k += (int)(sizeof(T) < 4 ? sizeof(T) : 4))
-                if (b + k >= lo && b + k < hi) m |= (sizeof(T) == 2 ? 0xffffu : 0xffffffffu) << (8 * k);
-            return m;
-        };
-        return make_uint4(v.x & word(0), v.y & word(4), v.z & word(8), v.w & word(12));
-    };
-    // Writes the row's bytes of edge vector v at `dst` (16-byte aligned):
-    // aligned stores of 8, 4 and 2 bytes, at most three.
-    auto store_edge = [&](unsigned char *dst, int vi, const uint4 &v) {
-        int lo, hi;
-        edge_bytes(vi, lo, hi);
-        auto w = [&](int b) { return b < 4 ? v.x : b < 8 ? v.y : b < 12 ? v.z : v.w; };
-        int b = lo;
-        while (b < hi) {
-            if ((b & 7) == 0 && b + 8 <= hi) {
-                *reinterpret_cast<uint2 *>(dst + b) = make_uint2(w(b), w(b + 4));
-                b += 8;
-            } else if ((b & 3) == 0 && b + 4 <= hi) {
-                *reinterpret_cast<uint32_t *>(dst + b) = w(b);
-                b += 4;
-            } else {  // 2-byte elements only
-                const uint32_t x = w(b) >> (8 * (b & 3));
-                *reinterpret_cast<unsigned short *>(dst + b) = (unsigned short)(x & 0xffffu);
-                b += 2;
-            }
-        }
+    const int hd = SH && shm ? (int)((16u - shm) / sizeof(T)) : 0;  // head elements
+    const int NB = SH ? (D - hd) / EPV : NV;                         // whole vectors
+    const int bo = SH && shm ? 1 : 0;  // the copy's vector that holds whole vector 0
+    constexpr int ES = !SH ? 1 : (G >= 16 ? 1 : 2);                 // edge elements a lane
+    // Column of this lane's edge slot e, or -1.
+    auto edge_col = [&](int e) -> int {
+        const int i = (G - 1 - gl) + e * G;
+        return (!SH || i >= D - NB * EPV) ? -1 : i < hd ? i : NB * EPV + i;
     };
     const int S = a.stages;
     const int TR = a.tile_rows;
@@ -324,15 +287,14 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
             const int vi = gl + j * G;
             float2 wf[VP];
             if constexpr (SH) {
-                // this thread's columns: vi * EPV - shm_e + e (w has its own
+                // this thread's columns: hd + vi * EPV + e (w has its own
                 // alignment; read once per CTA, element by element)
                 const T *wt = static_cast<const T *>(a.w);
-                const int c0 = vi * EPV - shm_e;
+                const int c0 = hd + vi * EPV;
 #pragma unroll
                 for (int q = 0; q < VP; ++q) {
-                    const int c = c0 + 2 * q;
-                    wf[q].x = (vi < nvr && c >= 0 && c < D) ? Cvt<T>::load1(wt + c) : 0.f;
-                    wf[q].y = (vi < nvr && c + 1 >= 0 && c + 1 < D) ? Cvt<T>::load1(wt + c + 1) : 0.f;
+                    wf[q].x = vi < NB ? Cvt<T>::load1(wt + c0 + 2 * q) : 0.f;
+                    wf[q].y = vi < NB ? Cvt<T>::load1(wt + c0 + 2 * q + 1) : 0.f;
                 }
             } else {
                 const uint4 wv =
@@ -343,6 +305,20 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
             for (int q = 0; q < VP; ++q) wp[j][q] = f2add(wb2, wf[q]);
         }
     }
+    // SH: this lane's edge columns, their w' and (VJP) gw accumulators.
+    int ecol[ES];
+    float ewp[ES], eacc[ES];
+#pragma unroll
+    for (int e = 0; e < ES; ++e) {
+        ecol[e] = edge_col(e);
+        ewp[e] = ecol[e] >= 0 ? a.weight_bias + Cvt<T>::load1(static_cast<const T *>(a.w) + ecol[e])
+                              : 0.f;
+        eacc[e] = 0.f;
+    }
+    // Element c of a row whose copy's frame starts at vector pointer r.
+    auto row_elem = [&](const uint4 *r, int c) -> float {
+        return Cvt<T>::load1(reinterpret_cast<const T *>(reinterpret_cast<const unsigned char *>(r) + shm) + c);
+    };
     float2 acc[VJP ? V : 1][VP];
 #pragma unroll
     for (int j = 0; j < (VJP ? V : 1); ++j)
@@ -369,18 +345,25 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     auto load_row = [&](const uint4 *r0, const uint4 *r1, float2 (&xa)[V][VP],
                         float2 (&xb)[V][VP], float &sa, float &sb) {
         float2 s2 = make_float2(0.f, 0.f), d2 = make_float2(0.f, 0.f);
+        if constexpr (SH) {  // this lane's edge elements
+#pragma unroll
+            for (int e = 0; e < ES; ++e) {
+                if (ecol[e] >= 0) {
+                    float x = row_elem(r0, ecol[e]);
+                    const float y = NTENS >= 2 ? row_elem(r1, ecol[e]) : 0.f;
+                    if constexpr (MODE == MODE_FWD_RES) x = x + y;  // h
+                    s2.x = fmaf(x, x, s2.x);
+                    if constexpr (VJP) d2.x = fmaf(y * ewp[e], x, d2.x);
+                }
+            }
+        }
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = gl + j * G;
-            if (vi < nvr) {
-                const int si = SPREAD_COPIES ? col[SPREAD_COPIES ? j : 0] : vi;
-                uint4 u0 = r0[si], u1 = NTENS >= 2 ? r1[si] : u0;
-                if (is_edge(vi)) {  // elements of the neighbouring rows count as zeros
-                    u0 = edge_mask(vi, u0);
-                    u1 = edge_mask(vi, u1);
-                }
-                unpack_vec<T>(u0, xa[j]);
-                if constexpr (NTENS >= 2) unpack_vec<T>(u1, xb[j]);
+            if (vi < NB) {
+                const int si = SPREAD_COPIES ? col[SPREAD_COPIES ? j : 0] : vi + bo;
+                unpack_vec<T>(r0[si], xa[j]);
+                if constexpr (NTENS >= 2) unpack_vec<T>(r1[si], xb[j]);
                 if constexpr (MODE == MODE_FWD_RES) {
 #pragma unroll
                     for (int q = 0; q < VP; ++q) xa[j][q] = f2add(xa[j][q], xb[j][q]);  // h
@@ -403,35 +386,52 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                            const uint4 *r0, const uint4 *r1, const uint4 *r2, int64_t row, float r,
                            float dot) {
         const size_t base0 = (size_t)(row * lo0), base1 = (size_t)(row * lo1);
-        // SH: the rows' aligned frames in the outputs (same offset as the inputs)
+        // SH: whole vector vi of a row is vector vi + bo of its output row's
+        // aligned frame (the outputs have the inputs' offset)
         uint4 *o0 = out0 + base0, *o1 = out1 + base1;
         if constexpr (SH) {
-            o0 = reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.out0) + row * row_bytes - shm);
+            o0 = reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.out0) + row * row_bytes - shm) + bo;
             if constexpr (MODE == MODE_FWD_RES)
                 o1 = reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.out1) + row * row_bytes -
-                                               shm);
+                                               shm) + bo;
         }
-        // Stores vector vi of a row: whole when it lies inside the row, else
-        // (SH: a row's first and last vectors) only the row's bytes of it.
         auto store_vec = [&](uint4 *orow, int vi, const float2 (&f)[VP]) {
-            const uint4 v = pack_vec<T>(f);
-            if (is_edge(vi))
-                store_edge(reinterpret_cast<unsigned char *>(orow + vi), vi, v);
-            else
-                st_global(orow + vi, v);
+            st_global(orow + vi, pack_vec<T>(f));
         };
         const float2 rr = make_float2(r, r);
         const float c = (r * r) * (dot * inv_D);  // r^2 * dot / D
         const float2 nc2 = make_float2(-c, -c);
+        if constexpr (SH) {  // this lane's edge elements, one at a time
+            T *orow0 = static_cast<T *>(a.out0) + row * (int64_t)D;
+#pragma unroll
+            for (int e = 0; e < ES; ++e) {
+                if (ecol[e] >= 0) {
+                    float x = row_elem(r0, ecol[e]);
+                    const float y = NTENS >= 2 ? row_elem(r1, ecol[e]) : 0.f;
+                    if constexpr (VJP) {
+                        float o = r * (y * ewp[e] - x * c);
+                        eacc[e] = fmaf(y, x * r, eacc[e]);
+                        if constexpr (ADD) o = o + row_elem(r2, ecol[e]);
+                        Cvt<T>::store1(orow0 + ecol[e], o);
+                    } else {
+                        if constexpr (MODE == MODE_FWD_RES) {
+                            x = x + y;
+                            Cvt<T>::store1(static_cast<T *>(a.out1) + row * (int64_t)D + ecol[e], x);
+                        }
+                        Cvt<T>::store1(orow0 + ecol[e], (x * r) * ewp[e]);
+                    }
+                }
+            }
+        }
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int vi = gl + j * G;
-            if (vi < nvr) {
+            if (vi < NB) {
                 float2 o[VP];
                 const float2 *xa = xa_in[j], *xb = xb_in[j];
                 float2 ra[VP], rb[VP];
                 if constexpr (RELOAD) {
-                    const int si = SPREAD_COPIES ? col[SPREAD_COPIES ? j : 0] : vi;
+                    const int si = SPREAD_COPIES ? col[SPREAD_COPIES ? j : 0] : vi + bo;
                     unpack_vec<T>(r0[si], ra);
                     unpack_vec<T>(r1[si], rb);
                     xa = ra;
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                     }
                     if constexpr (ADD) {
                         float2 gr[VP];
-                        unpack_vec<T>(r2[SPREAD_COPIES ? col[SPREAD_COPIES ? j : 0] : vi], gr);
+                        unpack_vec<T>(r2[SPREAD_COPIES ? col[SPREAD_COPIES ? j : 0] : vi + bo], gr);
 #pragma unroll
                         for (int q = 0; q < VP; ++q) o[q] = f2add(o[q], gr[q]);  // + g_new_residual
                     }
@@ -584,16 +584,20 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                 reinterpret_cast<float4 *>(dst)[u] =
                     make_float4(acc[j][2 * u].x, acc[j][2 * u].y, acc[j][2 * u + 1].x, acc[j][2 * u + 1].y);
         };
-        // SH: this thread's columns of vector j start at vi * EPV - shm_e;
-        // those inside [0, D) are stored one by one.
+        // SH: this thread's columns of vector j start at hd + vi * EPV (stored
+        // one by one), its edge columns at ecol[].
         auto store_acc_sh = [&](float *dst_row, int j, int vi) {
-            const int c0 = vi * EPV - shm_e;
+            const int c0 = hd + vi * EPV;
 #pragma unroll
             for (int q = 0; q < VP; ++q) {
-                const int c = c0 + 2 * q;
-                if (c >= 0 && c < D) dst_row[c] = acc[j][q].x;
-                if (c + 1 >= 0 && c + 1 < D) dst_row[c + 1] = acc[j][q].y;
+                dst_row[c0 + 2 * q] = acc[j][q].x;
+                dst_row[c0 + 2 * q + 1] = acc[j][q].y;
             }
+        };
+        auto store_edge_acc = [&](float *dst_row) {
+#pragma unroll
+            for (int e = 0; e < ES; ++e)
+                if (ecol[e] >= 0) dst_row[ecol[e]] = eacc[e];
         };
         if constexpr (CTA_ROW) {
             // Each column is owned by exactly one thread of the CTA.
@@ -601,11 +605,12 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
             for (int j = 0; j < V; ++j) {
                 const int vi = gl + j * G;
                 if constexpr (SH) {
-                    if (vi < nvr) store_acc_sh(prow, j, vi);
+                    if (vi < NB) store_acc_sh(prow, j, vi);
                 } else {
                     if (vi < NV) store_acc(prow + (size_t)vi * EPV, j);
                 }
             }
+            if constexpr (SH) store_edge_acc(prow);
         } else {
             // NG groups own the same columns: add their registers in group
             // order through shared memory (the ring is idle now).
@@ -615,11 +620,12 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
             for (int j = 0; j < V; ++j) {
                 const int vi = gl + j * G;
                 if constexpr (SH) {
-                    if (vi < nvr) store_acc_sh(buf + (size_t)gid * D, j, vi);
+                    if (vi < NB) store_acc_sh(buf + (size_t)gid * D, j, vi);
                 } else {
                     if (vi < NV) store_acc(buf + (size_t)gid * D + (size_t)vi * EPV, j);
                 }
             }
+            if constexpr (SH) store_edge_acc(buf + (size_t)gid * D);
             __syncthreads();
             for (int col = tid; col < D; col += NT) {
                 float sum = 0.f;

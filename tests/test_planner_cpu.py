@@ -44,15 +44,13 @@ def plans(tmp_path_factory):
 
 
 def _cluster_fits(mode, nv):
-    """Whether a cluster of at most 8 CTAs (slices of up to 1024 vectors, or
-    2048 for the forward) covers a row of nv vectors with four stages of its
-    slices in one SM's shared memory."""
+    """Whether a cluster of 2, 4 or 8 CTAs (slices of up to 2048 vectors)
+    covers a row of nv vectors with three stages of its slices in one SM's
+    shared memory."""
     ntens = 1 if mode == 1 else 3 if mode == 3 else 2
-    for nt in ((512,) if mode >= 2 else (512, 1024)):
-        cl = 2
-        while cl <= 8 and cl * 2 * nt < nv:
-            cl *= 2
-        if cl <= 8 and (225 * 1024) // (ntens * (-(-nv // cl) * 16)) >= 4:
+    for cl in (2, 4, 8):
+        sl = -(-nv // cl)
+        if sl <= 2048 and (225 * 1024) // (ntens * sl * 16) >= 3:
             return True
     return False
 
@@ -167,9 +165,10 @@ def _period(D, es):
 
 
 def test_shifted_plans(plans):
-    """Rows off 16-byte boundaries: the staged tier when the superset of a row
-    (worst offset) fits a configuration, the configuration that fits it most
-    tightly, sub-warp tiles of a multiple of 8 rows, and CTAs that take
+    """Rows off 16-byte boundaries: the staged tier with the configuration an
+    aligned row of the same D gets (its whole vectors; the edge elements are
+    handled apart), stages that hold the superset of a tile at the worst
+    offset, sub-warp tiles of a multiple of 8 rows, and CTAs that take
     several rows on a grid that is a multiple of the offset's period (so a
     CTA sees one offset on all of its rows)."""
     cfgs, rows = plans
@@ -179,13 +178,13 @@ def test_shifted_plans(plans):
         if align != 2:
             continue
         where = (mode, es, D, R)
-        nvs = -(-(16 - es + D * es) // 16)
-        if R > 8 and nvs <= 2048:
+        nv = D * es // 16  # whole vectors; the edge elements are handled apart
+        if R > 8 and nv <= 2048:
             n += 1
             assert tier == 0 and shift, where
-            fits = [c for c, (_, _, _, mx) in cfgs.items() if c != WIDE and nvs <= mx]
+            fits = [c for c, (_, _, _, mx) in cfgs.items() if c != WIDE and nv <= mx]
             assert cfg == min(fits, key=lambda c: cfgs[c][3]), where
-            assert g * v >= nvs, where
+            assert g * v >= nv and g * 2 >= 14, where  # the edges: up to 14, 1-2 a lane
             if g < nt:
                 assert tr % 8 == 0, where
             elif grid < ntiles:
@@ -197,11 +196,11 @@ def test_shifted_plans(plans):
 
 def test_cluster_plans(plans):
     """Rows of more than 2048 (VJP) or 4096 (forward) vectors: clusters of 2, 4
-    or 8 CTAs whose slices (whole 16-byte vectors, at most 1024 a CTA for the
-    VJP and 2048 for the forward) cover the row with no CTA left empty, one
-    CTA per SM, rings of at least four stages that fit one SM's shared
-    memory, and a grid of whole clusters (without a device query: SMs // cl
-    clusters at most)."""
+    or 8 CTAs of 512 threads whose slices (whole 16-byte vectors, two or four
+    a thread) cover the row with no CTA left empty, one CTA per SM, rings of
+    at least three stages (four or more, for the pipelined loop, wherever
+    they fit) in one SM's shared memory, and a grid of whole clusters
+    (without a device query: SMs // cl clusters at most)."""
     _, rows = plans
     n = 0
     for (mode, es, D, R, tier, cfg, nt, g, v, max_nv, stages, tr, ntiles, grid, smem, sb,
@@ -213,12 +212,15 @@ def test_cluster_plans(plans):
         nv = D * es // 16
         ntens = 1 if mode == 1 else 3 if mode == 3 else 2
         assert align == 1 and R > 8 and nv > (2048 if mode >= 2 else 4096), where
-        assert cl in (2, 4, 8) and nt in (512, 1024) and not (mode >= 2 and nt == 1024), where
+        assert cl in (2, 4, 8) and nt == 512 and v in (2, 4), where
         assert cl_cols * es % 16 == 0, where
         slice_v = cl_cols * es // 16
-        assert slice_v <= 2 * nt and cl * slice_v >= nv and (cl - 1) * slice_v < nv, where
+        assert slice_v <= v * nt and (v == 2 or slice_v > 2 * nt), where
+        assert cl * slice_v >= nv and (cl - 1) * slice_v < nv, where
         assert sb == cl_cols * es, where
-        assert 4 <= stages <= 8 and smem == 1024 + stages * ntens * sb, where
+        assert 3 <= stages <= 8 and smem == 1024 + stages * ntens * sb, where
+        fits4 = (225 * 1024) // (ntens * sb) >= 4
+        assert (stages >= 4) == fits4, where  # the pipelined loop wherever four fit
         assert smem + RESERVED_PER_CTA <= SMEM_PER_SM and smem <= SMEM_PER_CTA, where
         assert ntiles == R and grid % cl == 0 and grid // cl == min(R, SM // cl), where
         assert ntens * sb <= TX_LIMIT, where
