@@ -686,6 +686,17 @@ def run_single_op(args):
         ob = torch.empty_like(xr)
         out, nr = ob[:, :args.D], ob[:, args.D:]
         gx = torch.empty_like(xr)[:, :args.D]
+    elif args.layout == "offset":
+        # every tensor one element past a 16-byte boundary (a slice of a
+        # bigger buffer): rows at one shared offset
+        def offset(t):
+            buf = torch.empty(t.numel() + 16, dtype=dtype, device=dev)
+            v = buf[1:1 + t.numel()].view(t.shape)
+            v.copy_(t)
+            return v
+        x, res, g = offset(x), offset(res), offset(g)
+        g_res = res
+        out, nr, gx = offset(x), offset(x), offset(x)
     elif args.layout == "padded":
         # every tensor in its own buffer with rows of D + 64 elements
         def padded(t):
@@ -702,7 +713,7 @@ def run_single_op(args):
     rstd = torch.empty(args.rows, dtype=torch.float32, device=dev) if args.rstd else None
     if args.rstd and args.op == "vjp":
         rn.rmsnorm_fwd_ex(x, w, c.eps, 0.0, rstd=rstd)  # a valid saved scale to read
-    general = args.rstd or args.layout != "dense" or args.dtype == "f32"
+    general = args.rstd or args.layout in ("strided", "padded") or args.dtype == "f32"
 
     if args.op == "gate":  # x = [a | b] of width 2D from the same draws
         xg = torch.cat([x, res], dim=1)
@@ -739,7 +750,9 @@ def run_single_op(args):
         nbytes += 4 * args.rows  # written by the forward, read by the VJP
     plan = ("gate" if args.op == "gate" else
             rn.rmsnorm_describe_dispatch("fwd" if args.op == "fwd" else "vjp", args.rows, args.D,
-                                         dtype, args.op != "vjp"))
+                                         dtype, args.op != "vjp",
+                                         2 if args.layout == "offset" else
+                                         1 if args.layout == "dense" else 0))
     print("op=%s dtype=%s layout=%s rstd=%d rows=%d D=%d plan=%s us=%.2f GB/s=%.1f" % (
         args.op, args.dtype, args.layout, int(args.rstd), args.rows, args.D, plan, us,
         nbytes / us / 1e3), flush=True)
@@ -887,9 +900,10 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--dtype", choices=("bf16", "f16", "f32"), default="bf16",
                     help="profiling mode: element type")
-    ap.add_argument("--layout", choices=("dense", "strided", "padded"), default="dense",
+    ap.add_argument("--layout", choices=("dense", "strided", "padded", "offset"), default="dense",
                     help="profiling mode: strided = the tensors are halves of [rows, 2D] "
-                         "buffers; padded = rows of D + 64 elements")
+                         "buffers; padded = rows of D + 64 elements; offset = every tensor one "
+                         "element past a 16-byte boundary")
     ap.add_argument("--rstd", action="store_true",
                     help="profiling mode: the forward writes rstd / the VJP reads it")
     ap.add_argument("--all-configs", action="store_true",
