@@ -60,6 +60,18 @@
  * wait for its own asynchronous copies runs out (about a second) stops, leaves
  * its outputs undefined and sets RMSNORM_DEVSTATUS_WAIT_TIMEOUT in the
  * library's device status word, read by rmsnorm_device_status().
+ *
+ * Row scheduling of the forward: the CTAs of the staged forward kernels take
+ * most of their rows from counters at run time, so a CTA the memory system
+ * slows down takes fewer; the results do not depend on which CTA takes a row.
+ * The counters are sets in the library's device memory that every launch
+ * leaves at zero.  Launches outside a graph capture take them in turn from
+ * 16384 sets; a launch recorded into a graph keeps a set of its own, which
+ * every replay of that graph instance uses (a graph instance never runs
+ * alongside itself).  Two instances made from one captured graph must
+ * therefore not run at the same time; the environment setting
+ * RMSNORM_TUNE=claim=0, read once per process, turns the counters off (the
+ * CTAs then take fixed rows).
  */
 #ifndef RMSNORM_GB300_H
 #define RMSNORM_GB300_H
@@ -334,11 +346,24 @@ int rmsnorm_debug_inject(int64_t drop_tile, int64_t budget_cycles);
 int rmsnorm_debug_fail_allocs(int count);
 
 /*
+ * Test hook for the staged forwards that take their tiles from counters at
+ * run time.  Launches made outside a graph capture normally cycle through
+ * 16384 counter sets; after this call they cycle through the first `count`
+ * (1 <= count <= 16384), so with count = 1 consecutive forwards reuse one
+ * set, which shows that every launch -- one that timed out included --
+ * leaves its set at zero.  Forwards that may run at the same time (other
+ * streams) must not be launched while count is small.  count == 0 restores
+ * the default; other values return RMSNORM_ERR_INVALID_ARG.
+ */
+int rmsnorm_debug_claim_counters(int count);
+
+/*
  * Describes the kernel plan rmsnorm_fwd (op = 0) or rmsnorm_vjp (op = 1;
  * with has_residual, rmsnorm_fused_vjp with a g_residual) would use for this
  * problem on the current device, as a static string such as
- * "staged:cfg8:nt512:g512:v2:s6:tr1:grid152:smem..." ("staged-shift:..." for
- * the shifted-rows instances); for tests and benchmarks.  aligned: 1 = dense
+ * "staged:cfg8:nt512:g512:v2:s6:tr1:grid152:smem...:cl0" ("staged-shift:..."
+ * for the shifted-rows instances; ":claim" at the end when the CTAs take their
+ * rows from counters at run time); for tests and benchmarks.  aligned: 1 = dense
  * tensors at 16-byte aligned addresses (rows off 16-byte boundaries when
  * D * size is not a multiple of 16), 2 = dense tensors that all start at the
  * same unaligned offset, 0 = anything else (strided or mixed offsets).

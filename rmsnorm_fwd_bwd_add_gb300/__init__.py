@@ -22,6 +22,7 @@ PyTorch supplies device memory and streams only.
 """
 from .api import (  # noqa: F401
     BoundCall,
+    rmsnorm_debug_claim_counters,
     rmsnorm_debug_fail_allocs,
     rmsnorm_debug_inject,
     rmsnorm_describe_dispatch,
@@ -62,6 +63,7 @@ __all__ = [
     "rmsnorm_device_status",
     "rmsnorm_debug_inject",
     "rmsnorm_debug_fail_allocs",
+    "rmsnorm_debug_claim_counters",
     "rmsnorm_describe_dispatch",
     "rmsnorm_status_string",
     "RmsnormError",

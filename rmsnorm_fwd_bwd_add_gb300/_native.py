@@ -29,6 +29,7 @@ EXPORTS = (
     "rmsnorm_device_status",
     "rmsnorm_debug_inject",
     "rmsnorm_debug_fail_allocs",
+    "rmsnorm_debug_claim_counters",
     "rmsnorm_describe_dispatch",
 )
 
@@ -101,6 +102,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.rmsnorm_debug_inject.restype = _i
     lib.rmsnorm_debug_fail_allocs.argtypes = [_i]
     lib.rmsnorm_debug_fail_allocs.restype = _i
+    lib.rmsnorm_debug_claim_counters.argtypes = [_i]
+    lib.rmsnorm_debug_claim_counters.restype = _i
     lib.rmsnorm_describe_dispatch.argtypes = [_i, _i64, _i64, _i, _i, _i]
     lib.rmsnorm_describe_dispatch.restype = ctypes.c_char_p
     return lib

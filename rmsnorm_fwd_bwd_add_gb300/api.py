@@ -572,6 +572,14 @@ def rmsnorm_debug_inject(drop_tile: int = -1, budget_cycles: int = 0) -> None:
                   _native.lib().rmsnorm_debug_inject(drop_tile, budget_cycles))
 
 
+def rmsnorm_debug_claim_counters(count: int) -> None:
+    """Test hook: staged forwards launched outside a capture cycle through the
+    first `count` claim-counter sets (1 makes consecutive forwards share one;
+    0 restores the default)."""
+    _native.check("rmsnorm_debug_claim_counters",
+                  _native.lib().rmsnorm_debug_claim_counters(count))
+
+
 def rmsnorm_debug_fail_allocs(count: int) -> None:
     """Test hook: the next `count` gw scratch allocations of the pooled VJP
     entry points report RMSNORM_ERR_NO_MEMORY without allocating (0 cancels)."""

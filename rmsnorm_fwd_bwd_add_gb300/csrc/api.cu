@@ -27,6 +27,18 @@ constexpr int MAX_DEVICES = 64;
 
 __device__ unsigned int g_devstatus;  // RMSNORM_DEVSTATUS_* bits, per device
 
+// Claim counters of the staged forwards that take their tiles at run time:
+// sets of CLAIM_WORDS words (group counters and a finished-CTA count), zero
+// from module load on and put back to zero by each launch's last CTA.
+// Launches outside a graph capture take the sets in turn (CTR_DIRECT of
+// them, so two launches share one only with CTR_DIRECT launches between
+// them, both still running); each launch recorded into a graph keeps one of
+// its own (CTR_CAPTURE per device, then the static round robin).
+constexpr uint32_t CTR_DIRECT = 16384;
+constexpr size_t CLAIM_MIN_ROW_TRAFFIC = 96 * 1024;
+constexpr uint32_t CTR_CAPTURE = 2048;
+__device__ unsigned long long g_tile_ctrs[(size_t)CLAIM_WORDS * (CTR_DIRECT + CTR_CAPTURE)];
+
 thread_local int t_last_cuda_error = 0;
 
 struct DevInfo {
@@ -35,6 +47,8 @@ struct DevInfo {
     unsigned int *status = nullptr;  // device address of g_devstatus
     cudaMemPool_t pool = nullptr;    // gw scratch of rmsnorm_vjp; keeps its memory
     int cluster_cap[9] = {};         // clusters of 2, 4, 8 CTAs the device holds at once
+    int index = 0;                   // device ordinal
+    unsigned long long *tile_ctrs = nullptr;  // device address of g_tile_ctrs
 };
 std::mutex g_dev_mu;
 DevInfo g_dev[MAX_DEVICES];
@@ -42,6 +56,9 @@ DevInfo g_dev[MAX_DEVICES];
 std::atomic<int64_t> g_drop_tile{-1};
 std::atomic<long long> g_wait_budget{DEFAULT_WAIT_BUDGET};
 std::atomic<int> g_fail_allocs{0};  // scratch allocations still to report as failed
+std::atomic<uint64_t> g_ctr_next[MAX_DEVICES];  // next direct-launch counter pair
+std::atomic<uint32_t> g_ctr_captured[MAX_DEVICES];  // counter pairs kept by captured launches
+std::atomic<uint32_t> g_ctr_cycle{CTR_DIRECT};        // direct-launch pairs in use (test hook)
 
 // Takes one injected allocation failure if any is pending.
 bool take_injected_alloc_failure() {
@@ -70,6 +87,10 @@ int current_device(DevInfo *out) {
         e = cudaGetSymbolAddress(&p, g_devstatus);
         if (e != cudaSuccess) return cuda_fail(e);
         d.status = static_cast<unsigned int *>(p);
+        e = cudaGetSymbolAddress(&p, g_tile_ctrs);
+        if (e != cudaSuccess) return cuda_fail(e);
+        d.tile_ctrs = static_cast<unsigned long long *>(p);
+        d.index = dev;
         for (int cl : {2, 4, 8}) d.cluster_cap[cl] = cluster_capacity(cl);
         d.ready = true;
     }
@@ -221,6 +242,39 @@ int align_of(std::initializer_list<const Mat *> ms, const void *w, const void *r
         off = o;
     }
     return ALIGN_SHIFT;
+}
+
+// Whether a forward plan takes its tiles from counters: the CTA-per-row
+// staged forwards (aligned rows, not shifted ones) whose rows take long
+// enough.  A claim is an L2 atomic whose round trip, with HBM saturated,
+// outlasts a short row: claims lost time wherever a CTA's row moved less than
+// ~96 KB per SM (GB300, bf16 with residual, rows 16384: D = 4096 (two CTAs an
+// SM) -3 %, 8192 +-0; 8192 x 4096 fp16 without residual -20 %) and won it
+// above (D = 16384 with residual, 128 KB: 6310 -> 6677 GB/s).
+bool claims_tiles(const Plan &p, int mode, int64_t D, int es, int sm_count) {
+    if (p.tier != TIER_STAGED || p.shift || p.g != p.nt || is_vjp(mode)) return false;
+    const size_t row_traffic = (size_t)D * es * (mode == MODE_FWD_RES ? 4 : 2);
+    const size_t per_sm = row_traffic * (size_t)std::max(1, p.grid / std::max(1, sm_count));
+    return per_sm >= CLAIM_MIN_ROW_TRAFFIC;
+}
+
+// The counter set a staged forward on stream s claims its tiles from, or
+// null for the static round robin (tuned off, capture state unknown, or
+// every capture set taken).
+unsigned long long *tile_counter(const DevInfo &d, cudaStream_t s) {
+    if (!d.tile_ctrs || !planner::tuning().claim) return nullptr;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (cs != cudaStreamCaptureStatusNone) {
+        const uint32_t i = g_ctr_captured[d.index].fetch_add(1);
+        return i < CTR_CAPTURE ? d.tile_ctrs + (size_t)CLAIM_WORDS * ((size_t)CTR_DIRECT + i)
+                               : nullptr;
+    }
+    return d.tile_ctrs +
+           (size_t)CLAIM_WORDS * (size_t)(g_ctr_next[d.index].fetch_add(1) % g_ctr_cycle.load());
 }
 
 // gw partial rows of a VJP plan: one per CTA, or one per cluster.
@@ -442,6 +496,13 @@ int rmsnorm_fwd_ex(const void *x, int64_t ld_x, const void *residual, int64_t ld
     a.ld_out1 = new_residual ? mn.ld : 0;
     a.partials = nullptr;
     a.rstd = rstd;
+    if (claims_tiles(p, mode, D, es, dev.sm_count)) {
+        a.tile_ctr = tile_counter(dev, static_cast<cudaStream_t>(stream));
+        // as many groups as divide the grid, up to the tuned or default number
+        int k = planner::tuning().claim_k;
+        while (p.grid % k) k /= 2;
+        a.claim_k = k;
+    }
     cudaError_t e = launch_plan(dtype, mode, p, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return RMSNORM_OK;
@@ -559,6 +620,12 @@ int rmsnorm_debug_fail_allocs(int count) {
     return RMSNORM_OK;
 }
 
+int rmsnorm_debug_claim_counters(int count) {
+    if (count < 0 || count > (int)CTR_DIRECT) return RMSNORM_ERR_INVALID_ARG;
+    g_ctr_cycle.store(count == 0 ? CTR_DIRECT : (uint32_t)count);
+    return RMSNORM_OK;
+}
+
 const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype,
                                       int has_residual, int aligned) {
     thread_local char buf[160];
@@ -574,9 +641,11 @@ const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype
                       : (D * es) % 16 == 0        ? ALIGN_VEC
                                                   : ALIGN_SHIFT;
     const Plan p = make_plan(mode, rows, (int)D, es, align, dev.sm_count, dev.cluster_cap);
-    std::snprintf(buf, sizeof(buf), "%s%s:cfg%d:nt%d:g%d:v%d:s%d:tr%d:grid%d:smem%zu:cl%d",
+    std::snprintf(buf, sizeof(buf), "%s%s:cfg%d:nt%d:g%d:v%d:s%d:tr%d:grid%d:smem%zu:cl%d%s",
                   tier_name(p.tier), p.shift ? "-shift" : "", p.cfg, p.nt, p.g, p.v, p.stages,
-                  p.tile_rows, p.grid, p.smem, p.cl);
+                  p.tile_rows, p.grid, p.smem, p.cl,
+                  claims_tiles(p, mode, D, es, dev.sm_count) && planner::tuning().claim ? ":claim"
+                                                                                        : "");
     return buf;
 }
 

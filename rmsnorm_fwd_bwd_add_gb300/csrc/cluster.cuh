@@ -35,15 +35,15 @@ namespace rmsn {
 
 constexpr int CLUSTER_HEADER_BYTES = 1024;
 constexpr int CLUSTER_MAX = 8;  // portable cluster size
-constexpr int CLUSTER_NT = 512; // threads of a cluster CTA (one CTA per SM)
-
-// NT threads, up to V 16-byte vectors of the slice each (the slice is at
-// most NT * V vectors); PIPE: the exchange of a row's sums overlaps the next
-// row (four or more stages), else one row at a time (three).
-template <typename T, int MODE, int NT, int V, int CL, bool PIPE>
-__global__ void __launch_bounds__(NT, 1) cluster_kernel(const __grid_constant__ KernelArgs a) {
-    constexpr int NWARPS = NT / 32;
-    constexpr int WP = NWARPS <= 4 ? 4 : NWARPS <= 8 ? 8 : NWARPS <= 16 ? 16 : 32;
+// blockDim.x = NT threads (a multiple of 32, at most NTMAX), up to V
+// 16-byte vectors of the slice each (the slice is at most NT * V vectors;
+// the plan sizes the CTA to its slice, so every warp has about the same share
+// of a row); PIPE: the exchange of a row's sums overlaps the next row (four
+// or more stages), else one row at a time (three).
+template <typename T, int MODE, int NTMAX, int V, int CL, bool PIPE>
+__global__ void __launch_bounds__(NTMAX, 1) cluster_kernel(const __grid_constant__ KernelArgs a) {
+    const int NT = blockDim.x;
+    const int NWARPS = NT >> 5;
     constexpr int VP = vec_pairs<T>();
     constexpr int EPV = vec_elems<T>();
     constexpr int NTENS = input_tensors(MODE);
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(NT, 1) cluster_kernel(const __grid_constant__ 
     uint64_t *clbar = reinterpret_cast<uint64_t *>(smem + 64);  // [4]: every CTA's sums arrived
     uint64_t *xbar = reinterpret_cast<uint64_t *>(smem + 96);   // exit handshake
     float2 *cred = reinterpret_cast<float2 *>(smem + 128);      // [4][CL] the CTAs' slice sums
-    float2 *red = reinterpret_cast<float2 *>(smem + 512);       // [2][NWARPS] warp totals
+    float2 *red = reinterpret_cast<float2 *>(smem + 512);       // [2][NWARPS <= 32] warp totals
     unsigned char *ring = smem + CLUSTER_HEADER_BYTES;
 
     const int tid = threadIdx.x;
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(NT, 1) cluster_kernel(const __grid_constant__ 
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
-        for (int i = 0; i < 4; ++i) mbar_init(&clbar[i], CL);
+        for (int i = 0; i < 4; ++i) mbar_init(&clbar[i], 1);  // armed once per row
         mbar_init(xbar, CL);
         fence_mbar_init();
     }
@@ -159,11 +159,25 @@ __global__ void __launch_bounds__(NT, 1) cluster_kernel(const __grid_constant__ 
     // RD = 4 slots never overwrite sums still to be read, and no slot
     // barrier runs two phases ahead of a waiter.
     bool ok = true;
+    // Stage and phase of row k, and stage of row k - 1, advanced one step per
+    // row: no 64-bit division by the runtime ring depth in the row loop (a
+    // few of those per row cost as many instructions as the row's arithmetic).
+    int a_stage = 0, b_stage = 0;
+    uint32_t a_phase = 0;
+    auto next_a = [&]() {
+        if (++a_stage == S) {
+            a_stage = 0;
+            a_phase ^= 1u;
+        }
+    };
+    static_assert(RD == 4, "slot k & 3, slot phase (k >> 2) & 1");
     if constexpr (PIPE) {
     for (int64_t k = 0; k <= nk; ++k) {
         if (k < nk) {
-            const int sk = (int)(k % S);
-            ok = ok && mbar_wait_bounded(&full[sk], (uint32_t)((k / S) & 1), a.wait_budget);
+            if (tid == 0) mbar_arrive_expect_tx(&clbar[k & 3], CL * 8);  // row k's CL pairs
+            const int sk = a_stage;
+            ok = ok && mbar_wait_bounded(&full[sk], a_phase, a.wait_budget);
+            next_a();
             const uint4 *r0 = reinterpret_cast<const uint4 *>(stage_ptr(sk, 0));
             const uint4 *r1 = reinterpret_cast<const uint4 *>(stage_ptr(sk, NTENS >= 2 ? 1 : 0));
             float2 s2 = make_float2(0.f, 0.f), d2 = make_float2(0.f, 0.f);
@@ -194,26 +208,27 @@ __global__ void __launch_bounds__(NT, 1) cluster_kernel(const __grid_constant__ 
         // iteration k - 1; a failed wait anywhere is seen by all.
         if (__syncthreads_or(!ok)) break;
         if (tid == 0 && k >= 2 && issued < nk) issue_next();  // into row k-2's stage
-        if (k < nk) {
+        if (k < nk && warp == 0) {
+            // warp 0 (the sender) sums the warp totals in one fixed order:
+            // lane l holds warp l's, zeros past NWARPS
             const float2 *rb = red + (k & 1) * NWARPS;
-            const int wl = lane & (WP - 1);
-            float2 tot = wl < NWARPS ? rb[wl] : make_float2(0.f, 0.f);
-            tot.x = group_sum<WP>(tot.x);
-            if constexpr (VJP) tot.y = group_sum<WP>(tot.y);
-            // lane q of warp 0 writes CTA q's slot and arrives on its barrier,
+            float2 tot = lane < NWARPS ? rb[lane] : make_float2(0.f, 0.f);
+            tot.x = group_sum<32>(tot.x);
+            if constexpr (VJP) tot.y = group_sum<32>(tot.y);
+            // lane q writes CTA q's slot, completing 8 bytes on its barrier,
             // so the CL sends go out side by side
-            const int p = (int)(k % RD);
-            if (tid < CL) {
-                dsmem_store_f2(dsmem_addr(&cred[p * CL + rank], (uint32_t)tid), tot);
-                mbar_arrive_remote(dsmem_addr(&clbar[p], (uint32_t)tid));
-            }
+            const int p = (int)(k & 3);
+            if (lane < CL)
+                dsmem_store_async_f2(dsmem_addr(&cred[p * CL + rank], (uint32_t)lane), tot,
+                                     dsmem_addr(&clbar[p], (uint32_t)lane));
         }
         if (k >= 1) {
             const int64_t kk = k - 1;
             const int64_t row = cid + kk * ncl;
-            const int sk = (int)(kk % S);
-            const int p = (int)(kk % RD);
-            ok = ok && mbar_wait_cluster_bounded(&clbar[p], (uint32_t)((kk / RD) & 1),
+            const int sk = b_stage;
+            if (++b_stage == S) b_stage = 0;
+            const int p = (int)(kk & 3);
+            ok = ok && mbar_wait_cluster_bounded(&clbar[p], (uint32_t)((kk >> 2) & 1),
                                                  a.wait_budget);
             if (ok) {
                 float ss = 0.f, dot = 0.f;
@@ -274,13 +289,15 @@ __global__ void __launch_bounds__(NT, 1) cluster_kernel(const __grid_constant__ 
     // registers across the exchange, or re-read from its stage when four
     // vectors of x and g would not fit them (the VJP).
     for (int64_t k = 0; k < nk; ++k) {
-        const int sk = (int)(k % S);
+        const int sk = a_stage;
         const int64_t row = cid + k * ncl;
-        ok = ok && mbar_wait_bounded(&full[sk], (uint32_t)((k / S) & 1), a.wait_budget);
         const uint4 *r0 = reinterpret_cast<const uint4 *>(stage_ptr(sk, 0));
         const uint4 *r1 = reinterpret_cast<const uint4 *>(stage_ptr(sk, NTENS >= 2 ? 1 : 0));
         const uint4 *r2 = reinterpret_cast<const uint4 *>(stage_ptr(sk, NTENS - 1));
         float2 xa[V][VP], xb[V][VP];
+        if (tid == 0) mbar_arrive_expect_tx(&clbar[k & 3], CL * 8);  // row k's CL pairs
+        ok = ok && mbar_wait_bounded(&full[sk], a_phase, a.wait_budget);
+        next_a();
         float2 s2 = make_float2(0.f, 0.f), d2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
@@ -305,17 +322,17 @@ __global__ void __launch_bounds__(NT, 1) cluster_kernel(const __grid_constant__ 
         if (lane == 0) red[(k & 1) * NWARPS + warp] = make_float2(sa, sb);
         if (__syncthreads_or(!ok)) break;
         if (tid == 0 && k >= 1 && issued < nk) issue_next();  // into row k-1's stage
-        const float2 *rb = red + (k & 1) * NWARPS;
-        const int wl = lane & (WP - 1);
-        float2 tot = wl < NWARPS ? rb[wl] : make_float2(0.f, 0.f);
-        tot.x = group_sum<WP>(tot.x);
-        if constexpr (VJP) tot.y = group_sum<WP>(tot.y);
-        const int p = (int)(k % RD);
-        if (tid < CL) {
-            dsmem_store_f2(dsmem_addr(&cred[p * CL + rank], (uint32_t)tid), tot);
-            mbar_arrive_remote(dsmem_addr(&clbar[p], (uint32_t)tid));
+        const int p = (int)(k & 3);
+        if (warp == 0) {  // the sender, as in the pipelined loop
+            const float2 *rb = red + (k & 1) * NWARPS;
+            float2 tot = lane < NWARPS ? rb[lane] : make_float2(0.f, 0.f);
+            tot.x = group_sum<32>(tot.x);
+            if constexpr (VJP) tot.y = group_sum<32>(tot.y);
+            if (lane < CL)
+                dsmem_store_async_f2(dsmem_addr(&cred[p * CL + rank], (uint32_t)lane), tot,
+                                     dsmem_addr(&clbar[p], (uint32_t)lane));
         }
-        ok = ok && mbar_wait_cluster_bounded(&clbar[p], (uint32_t)((k / RD) & 1), a.wait_budget);
+        ok = ok && mbar_wait_cluster_bounded(&clbar[p], (uint32_t)((k >> 2) & 1), a.wait_budget);
         if (ok) {
             float ss = 0.f, dot = 0.f;
 #pragma unroll

@@ -9,8 +9,8 @@ cudaError_t launch_cluster_bf16(int mode, const Plan &p, const KernelArgs &a, cu
 
 namespace rmsn {
 
-// Queried with the bf16 VJP instance of 512 threads (two vectors) and 200 KB of shared
-// memory, so that one CTA fills an SM as every cluster plan does.
+// Queried with the bf16 VJP instance of two vectors a thread, at 512 threads and 200 KB of
+// shared memory, so that one CTA fills an SM as every cluster plan does.
 int cluster_capacity(int cl) {
     constexpr int MAX_DEVICES = 64;
     static std::atomic<int> cache[MAX_DEVICES][9];  // 0: not queried; else capacity + 1
@@ -23,9 +23,9 @@ int cluster_capacity(int cl) {
     static std::atomic<uint64_t> m2{0}, m4{0}, m8{0};
     std::atomic<uint64_t> *mask = nullptr;
     switch (cl) {
-        case 2: kern = (const void *)cluster_kernel<__nv_bfloat16, MODE_VJP, 512, 2, 2, true>; mask = &m2; break;
-        case 4: kern = (const void *)cluster_kernel<__nv_bfloat16, MODE_VJP, 512, 2, 4, true>; mask = &m4; break;
-        case 8: kern = (const void *)cluster_kernel<__nv_bfloat16, MODE_VJP, 512, 2, 8, true>; mask = &m8; break;
+        case 2: kern = (const void *)cluster_kernel<__nv_bfloat16, MODE_VJP, CLUSTER_NT_V2, 2, 2, true>; mask = &m2; break;
+        case 4: kern = (const void *)cluster_kernel<__nv_bfloat16, MODE_VJP, CLUSTER_NT_V2, 2, 4, true>; mask = &m4; break;
+        case 8: kern = (const void *)cluster_kernel<__nv_bfloat16, MODE_VJP, CLUSTER_NT_V2, 2, 8, true>; mask = &m8; break;
         default: cache[dev][cl].store(1); return 0;
     }
     int n = 0;

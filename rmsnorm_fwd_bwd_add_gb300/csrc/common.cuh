@@ -218,6 +218,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
+// Non-blocking test of the phase with the given parity (try_wait may suspend
+// the thread for a while; test_wait returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// One arrival on an mbarrier of this CTA (release: this thread's earlier
+// shared-memory accesses are ordered before it).
+__device__ __forceinline__ void mbar_arrive_local(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // Waits for the phase of `bar` with the given parity to complete; gives up
 // after `budget` SM clock cycles and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long budget) {
@@ -304,6 +324,19 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
 __device__ __forceinline__ void dsmem_store_f2(uint32_t addr, float2 v) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
                  : "memory");
+}
+
+// Asynchronous store of a float2 into another CTA's shared memory (addr, a
+// shared::cluster address) that completes 8 bytes of the transaction count
+// of that CTA's mbarrier (bar, a shared::cluster address) when it lands.
+// Unlike an arrival with release semantics, it does not wait for this
+// thread's earlier global writes to become visible first.
+__device__ __forceinline__ void dsmem_store_async_f2(uint32_t addr, float2 v, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+            addr),
+        "f"(v.x), "f"(v.y), "r"(bar)
+        : "memory");
 }
 
 // One arrival on an mbarrier in another CTA of the cluster, ordered after

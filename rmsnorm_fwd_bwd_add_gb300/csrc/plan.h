@@ -49,7 +49,20 @@ struct KernelArgs {
     // Cluster tier: columns of each CTA's slice of a row (a whole number of
     // 16-byte vectors).
     int cl_cols;
+    // Staged forwards that claim their tiles at run time: claim_k group
+    // counters (CLAIM_STRIDE apart) and then the count of finished CTAs, all
+    // zero at launch and put back to zero by the launch's last CTA; null for
+    // the static round robin.  claim_k divides the grid.
+    unsigned long long *tile_ctr;
+    int claim_k;
 };
+
+// Layout of one set of claim counters (in 8-byte words): group counter j at
+// j * CLAIM_STRIDE (a 32-byte sector each), the finished-CTA count after the
+// CLAIM_MAX_K group counters.
+constexpr int CLAIM_MAX_K = 8;
+constexpr int CLAIM_STRIDE = 4;
+constexpr int CLAIM_WORDS = CLAIM_STRIDE * (CLAIM_MAX_K + 1);
 
 struct Plan {
     int tier;
@@ -171,6 +184,10 @@ constexpr int staged_ctas_per_sm(int mode, int nt, int g, int v) {
 constexpr int GENERIC_NT = 256;
 constexpr int STAGED_HEADER_BYTES = 640;  // 16 mbarriers (128 B) + reduction scratch (512 B)
 constexpr int MAX_STAGES = 8;
+// Threads of a cluster CTA at two vectors a thread (the VJP's 92 registers
+// fit 640 threads) and at four (512).
+constexpr int CLUSTER_NT_V2 = 640;
+constexpr int CLUSTER_NT_V4 = 512;
 
 // Launchers (one translation unit per tier / dtype).  dtype: 0 fp16, 1 bf16,
 // 2 fp32.

@@ -64,7 +64,7 @@ inline size_t smem_per_cta(int cps) {
 
 
 // Overrides of the staged tier's choices, read once from RMSNORM_TUNE
-// ("cfg=N,cps=N,stages=N,tmap=0", any subset) for tuning sweeps and for
+// ("cfg=N,cps=N,stages=N,tmap=0,claim=0,claimk=N", any subset) for tuning sweeps and for
 // testing the per-row copy path that strided sub-warp tiles take where no
 // tensor map can be made.  Unset, the plan is a pure function of the problem
 // and the device.
@@ -73,6 +73,8 @@ struct Tuning {
     int cps = 0;      // CTAs per SM (capped by what the registers allow)
     int stages = 0;   // maximum ring depth
     bool tmap = true; // tensor maps for strided sub-warp tiles
+    bool claim = true; // staged forwards: tiles claimed at run time
+    int claim_k = 1;  // claim groups (a power of two up to CLAIM_MAX_K)
 };
 
 inline Tuning parse_tuning() {
@@ -87,6 +89,10 @@ inline Tuning parse_tuning() {
         else if (std::sscanf(tok, "cps=%d", &v) == 1 && v >= 1 && v <= 6) t.cps = v;
         else if (std::sscanf(tok, "stages=%d", &v) == 1 && v >= 2 && v <= MAX_STAGES) t.stages = v;
         else if (std::sscanf(tok, "tmap=%d", &v) == 1) t.tmap = v != 0;
+        else if (std::sscanf(tok, "claim=%d", &v) == 1) t.claim = v != 0;
+        else if (std::sscanf(tok, "claimk=%d", &v) == 1 && v >= 1 && v <= CLAIM_MAX_K &&
+                 (v & (v - 1)) == 0)
+            t.claim_k = v;
     }
     return t;
 }
@@ -203,46 +209,43 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
 
 // Cluster plan for aligned rows longer than the staged and direct tiers take
 // (VJP: more than 2048 vectors, forward: more than 4096): clusters of 2, 4 or
-// 8 CTAs of 512 threads, one per SM, each CTA's slice a whole number of
-// vectors, at most 1024 (two a thread) or 2048 (four), with a ring of at
+// 8 CTAs, one per SM, each CTA's slice a whole number of vectors (at most
+// 2048) and each CTA sized to its slice, threads rounded up to a warp: two
+// vectors a thread up to CLUSTER_NT_V2 threads, else four.  A CTA of 512
+// threads for every slice left half its warps a vector short of the rest at
+// each row's barrier (2000 x 40000 bf16 VJP, slices of 1250 vectors: 3652 ->
+// 3721 GB/s with 640 threads of two).  The ring takes at
 // least three slices (four or more: the row loop overlaps a row's exchange
 // with the next row, which measured faster wherever they fit: 2000 x 40000
 // bf16 VJP 2815 -> 3276 GB/s, D = 24576 3431 -> 4051; three: one row at a
-// time, which lets four-vector slices fit: D = 32768 3210 -> 4063, 65536
-// 2198 -> 2741).  Of the fitting sizes, the one with the most SMs busy (clusters the
-// device holds at once, cap[cl], times CTAs per cluster), counting a CTA
-// whose threads get fewer than two vectors a row as that fraction of an SM:
-// the per-row work of reducing and exchanging is not amortised over less
-// (2000 x 40000 bf16 VJP, 8 CTAs of 625 vectors: 1.2 a thread, 30 % of the
-// copy bandwidth).
+// time, which lets the longest slices fit: D = 32768 3210 -> 4063, 65536
+// 2198 -> 2741).  Of the fitting sizes, the one with the most SMs busy
+// (clusters the device holds at once, cap[cl], times CTAs per cluster).
 inline bool plan_cluster(int mode, int64_t rows, int D, int esize, const int *cap, int sm_count,
                          Plan *p) {
     const int64_t nv = (int64_t)D * esize / 16;
     const int ntens = input_tensors(mode);
-    constexpr int NT = 512;
     int best_cl = 0;
-    double best = 0.0;
+    int64_t best = 0;
     for (int cl : {2, 4, 8}) {
-        const int64_t slice = (nv + cl - 1) / cl;  // vectors of one CTA's slice
-        if (slice > 4 * NT) continue;
+        const int64_t slice = ceil_div(nv, cl);  // vectors of one CTA's slice
+        if (slice > 4 * CLUSTER_NT_V4) continue;
         if ((int64_t)SMEM_ONE_PER_SM / ((int64_t)ntens * slice * 16) < 3) continue;
         const int64_t clusters = cap ? cap[cl] : sm_count / cl;
         if (clusters <= 0) continue;
-        const double per_thread = (double)slice / NT;
-        const double score = (double)(std::min<int64_t>(clusters, rows) * cl) *
-                             std::min(1.0, per_thread / 2.0);
-        if (score > best) {
-            best = score;
+        const int64_t busy = std::min<int64_t>(clusters, rows) * cl;
+        if (busy > best) {
+            best = busy;
             best_cl = cl;
         }
     }
     if (!best_cl) return false;
-    const int64_t per_cta_vec = (nv + best_cl - 1) / best_cl;
+    const int64_t per_cta_vec = ceil_div(nv, best_cl);
     *p = Plan{};
     p->tier = TIER_CLUSTER;
-    p->nt = NT;
-    p->g = NT;
-    p->v = per_cta_vec <= 2 * NT ? 2 : 4;
+    p->v = per_cta_vec <= 2 * CLUSTER_NT_V2 ? 2 : 4;
+    p->nt = (int)(ceil_div(ceil_div(per_cta_vec, p->v), 32) * 32);
+    p->g = p->nt;
     p->cl = best_cl;
     p->cl_cols = (int)(per_cta_vec * 16 / esize);
     p->tile_rows = 1;

@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
 
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);   // [MAX_STAGES]
+    int64_t *stage_tile = reinterpret_cast<int64_t *>(smem + 64);  // [MAX_STAGES] claimed tiles
     float2 *red = reinterpret_cast<float2 *>(smem + 128);  // [2][NWARPS]
     unsigned char *ring = smem + STAGED_HEADER_BYTES;
 
@@ -114,6 +115,26 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     const uint32_t SB = a.stage_bytes;
     const int64_t grid = gridDim.x;
     const int64_t nk = (a.num_tiles - (int64_t)blockIdx.x + grid - 1) / grid;  // >= 1
+    // Claimed tiles: a forward may take most of its tiles from counters at
+    // run time (a.tile_ctr) instead of the static round robin, so that every
+    // CTA stays busy until the last tile is taken -- a CTA slowed down by the
+    // memory system simply takes fewer.  The CTAs form K = a.claim_k groups
+    // (CTA b in group b % K, K dividing the grid); group j owns tiles j, j +
+    // K, j + 2K, ... and a counter of its own, so K counters share the
+    // claims.  Each CTA's first S tiles are fixed (its ring fills with no
+    // claim to wait for); after that it claims one tile at a time, one
+    // refill ahead.  Rows of a forward are independent, so the results do
+    // not depend on which CTA takes a row.  Not the VJP (a CTA's gw partial
+    // row sums a fixed set of rows, which keeps gw's bits fixed), nor shifted
+    // rows (a CTA's columns follow its rows' offset), nor tiles copied row by
+    // row.
+    constexpr bool DYN_OK = !VJP && !SH && !SPREAD_COPIES;
+    const bool dyn = DYN_OK && a.tile_ctr != nullptr;
+    const int CK = dyn ? a.claim_k : 1;                       // groups (counters)
+    const int64_t c_home = (int64_t)blockIdx.x % CK;          // this CTA's group
+    const int64_t c_rank = (int64_t)blockIdx.x / CK;          // its rank in the group
+    const int64_t c_size = grid / CK;                         // CTAs of a group
+    unsigned long long *c_ctr = dyn ? a.tile_ctr + CLAIM_STRIDE * c_home : nullptr;
     const float eps = a.eps;
     // 1/D once per CTA: the per-row means are products, not divisions (exact
     // for D a power of two; within an ulp of the quotient otherwise).
@@ -136,8 +157,22 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     // issues its copies.  With SPREAD_COPIES thread 0 posts the bytes before
     // the CTA barrier that ends the previous tile in that stage, and after the
     // barrier every thread issues a share of the tile's copies.
-    int64_t issued = 0;  // tiles of this CTA issued so far
+    int64_t issued = 0;  // tiles of this CTA issued so far (claimed: stages armed)
     int issue_stage = 0;
+    bool exhausted = false;  // claimed tiles: the group's tiles have run out
+    int64_t pending = 0;     // claimed tiles: the next claim, made a refill ahead
+    auto more = [&]() -> bool { return dyn ? !exhausted : issued < nk; };
+    // Thread 0, claimed tiles: the next tile of this CTA, or -1.  Group
+    // index i (tile c_home + i * K): the CTA's first S are c_rank + s *
+    // c_size, the rest S * c_size + the counter's next value.
+    auto next_tile = [&]() -> int64_t {
+        const bool fixed = issued < S;
+        const int64_t gi = fixed ? c_rank + issued * c_size : (int64_t)S * c_size + pending;
+        const int64_t t = c_home + gi * CK;
+        if (t >= a.num_tiles) return -1;
+        if (!fixed) pending = (int64_t)atomicAdd(c_ctr, 1ull);  // the next claim, ahead of need
+        return t;
+    };
     const uint64_t policy = l2_evict_first_policy();
     // First row and row count of this CTA's tile number idx; false for the
     // tile the test hook drops.
@@ -212,7 +247,24 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     auto issue_next = [&]() {  // thread 0, the whole tile
         int64_t row0;
         int nr;
-        if (tile_of(issued, row0, nr)) {
+        bool have;
+        if (dyn) {
+            const int64_t t = next_tile();
+            if (t < 0) {  // none left: the stage's phase completes empty
+                stage_tile[issue_stage] = -1;
+                exhausted = true;
+                mbar_arrive_local(&full[issue_stage]);
+                advance();
+                return;
+            }
+            stage_tile[issue_stage] = t;  // published by the arrival below
+            row0 = t * TR;
+            nr = (int)min((int64_t)TR, rows - row0);
+            have = t != a.drop_tile;
+        } else {
+            have = tile_of(issued, row0, nr);
+        }
+        if (have) {
             uint64_t *bar = &full[issue_stage];
             if constexpr (!SPREAD_COPIES) {
                 // dense tiles, or CTA per row (one row: one copy per tensor);
@@ -240,14 +292,30 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     // may still be landing in shared memory before the CTA retires (at most
     // the last S issued tiles: an earlier stage was consumed before it was
     // issued again).
+    // Claimed tiles: the last CTA to finish puts the counter back to zero for
+    // the next launch handed it, which reads it only once this grid has
+    // completed (every CTA counts itself once, after its last claim).
+    auto finish_claims = [&]() {
+        if (dyn && tid == 0) {
+            unsigned long long *done = a.tile_ctr + CLAIM_STRIDE * CLAIM_MAX_K;
+            __threadfence();
+            if (atomicAdd(done, 1ull) == (unsigned long long)grid - 1ull) {
+                __threadfence();
+                for (int j = 0; j < CK; ++j) atomicExch(a.tile_ctr + CLAIM_STRIDE * j, 0ull);
+                atomicExch(done, 0ull);
+            }
+        }
+    };
     auto fail = [&]() {
         if (tid == 0) {
             atomicOr(a.status, DEVSTATUS_WAIT_TIMEOUT);
             for (int64_t kk = max((int64_t)0, issued - S); kk < issued; ++kk) {
-                if ((int64_t)blockIdx.x + kk * grid == a.drop_tile) continue;
+                const int64_t t = dyn ? stage_tile[kk % S] : (int64_t)blockIdx.x + kk * grid;
+                if (t == a.drop_tile) continue;
                 mbar_wait_bounded(&full[kk % S], (uint32_t)((kk / S) & 1), DEFAULT_WAIT_BUDGET);
             }
         }
+        finish_claims();
     };
 
     if (tid == 0) {
@@ -258,8 +326,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     // Launched as a programmatic dependent: nothing in global memory may be
     // touched before the previous kernel on the stream has completed.
     griddep_wait();
+    if (dyn && tid == 0) pending = (int64_t)atomicAdd(c_ctr, 1ull);  // used after the fixed tiles
     {
-        const int64_t n0 = min((int64_t)S, nk);
+        const int64_t n0 = dyn ? (int64_t)S : min((int64_t)S, nk);
         if constexpr (SPREAD_COPIES) {
             if (tmap_mode) {
                 if (tid == 0)
@@ -274,7 +343,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                 }
             }
         } else if (tid == 0) {
-            while (issued < n0) issue_next();
+            while (issued < n0 && more()) issue_next();
         }
     }
 
@@ -463,11 +532,16 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     int s = 0;        // stage of tile k
     uint32_t ph = 0;  // parity of that stage's phase
     if constexpr (CTA_ROW) {
-        for (int64_t k = 0; k < nk; ++k) {
-            const int64_t row = (int64_t)blockIdx.x + k * grid;  // tile_rows == 1
+        for (int64_t k = 0; dyn || k < nk; ++k) {
+            int64_t row = (int64_t)blockIdx.x + k * grid;  // tile_rows == 1
             // The VJP may be handed the forward's scale; fetch it early.
             const float r_saved = (GEN && VJP && a.rstd) ? __ldg(a.rstd + row) : 0.f;
             const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_budget);
+            bool end = false;  // claimed tiles: the stage says none is left
+            if (dyn) {
+                row = ok ? stage_tile[s] : 0;
+                end = ok && row < 0;
+            }
             float2 xa[V][VP], xb[V][VP];
             float sa, sb;
             load_row(reinterpret_cast<const uint4 *>(stage_ptr(s, 0)),
@@ -483,7 +557,8 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                 fail();
                 return;
             }
-            if (tid == 0 && k >= 1 && issued < nk) issue_next();
+            if (end) break;  // every thread read the same stage word
+            if (tid == 0 && k >= 1 && more()) issue_next();
             // Each group of WP lanes (the warp count rounded up to a power of
             // two) sums all warp totals: the same sums a 32-lane tree with
             // zeros past NWARPS gives, in log2(WP) shuffle levels.
@@ -507,15 +582,22 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
             }
         }
     } else {
-        for (int64_t k = 0; k < nk; ++k) {
-            const int64_t row0 = ((int64_t)blockIdx.x + k * grid) * TR;
-            const int nr = (int)min((int64_t)TR, rows - row0);
+        for (int64_t k = 0; dyn || k < nk; ++k) {
+            int64_t row0 = ((int64_t)blockIdx.x + k * grid) * TR;
+            int nr = (int)min((int64_t)TR, rows - row0);
             // The VJP may be handed the forward's scale: fetch this thread's
             // first row's early, and each next row's one row ahead.
             float r_next = 0.f;
             if constexpr (GEN && VJP)
                 if (a.rstd && gid < nr) r_next = __ldg(a.rstd + row0 + gid);
             const bool ok = mbar_wait_bounded(&full[s], ph, a.wait_budget);
+            bool end = false;  // claimed tiles: the stage says none is left
+            if (dyn) {
+                const int64_t t = ok ? stage_tile[s] : -1;
+                end = ok && t < 0;
+                row0 = t < 0 ? 0 : t * TR;
+                nr = t < 0 ? 0 : (int)min((int64_t)TR, rows - row0);
+            }
             const uint4 *t0 = reinterpret_cast<const uint4 *>(stage_ptr(s, 0));
             const uint4 *t1 = reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS >= 2 ? 1 : 0));
             const uint4 *t2 = reinterpret_cast<const uint4 *>(stage_ptr(s, NTENS - 1));
@@ -555,6 +637,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                 fail();
                 return;
             }
+            if (end) break;  // every thread read the same stage word
             if constexpr (SPREAD_COPIES) {
                 if (tmap_mode) {
                     if (tid == 0 && issued < nk) issue_tmap();
@@ -562,7 +645,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
                     issue_copies(issued, issue_stage, tid, NT);
                     advance();
                 }
-            } else if (tid == 0 && issued < nk) {
+            } else if (tid == 0 && more()) {
                 issue_next();
             }
             if (++s == S) {
@@ -572,6 +655,7 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
         }
     }
 
+    finish_claims();
     // The next kernel on the stream may start launching (it waits for this
     // one to complete before touching memory).
     griddep_launch_dependents();

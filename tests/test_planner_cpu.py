@@ -196,11 +196,13 @@ def test_shifted_plans(plans):
 
 def test_cluster_plans(plans):
     """Rows of more than 2048 (VJP) or 4096 (forward) vectors: clusters of 2, 4
-    or 8 CTAs of 512 threads whose slices (whole 16-byte vectors, two or four
-    a thread) cover the row with no CTA left empty, one CTA per SM, rings of
-    at least three stages (four or more, for the pipelined loop, wherever
+    or 8 CTAs whose slices (whole 16-byte vectors) cover the row with no CTA
+    left empty, each CTA sized to its slice (two vectors a thread up to 640
+    threads, else four; threads rounded up to a warp), one CTA per SM, rings
+    of at least three stages (four or more, for the pipelined loop, wherever
     they fit) in one SM's shared memory, and a grid of whole clusters
-    (without a device query: SMs // cl clusters at most)."""
+    (without a device query: SMs // cl clusters at most) of the size that
+    keeps the most SMs busy."""
     _, rows = plans
     n = 0
     for (mode, es, D, R, tier, cfg, nt, g, v, max_nv, stages, tr, ntiles, grid, smem, sb,
@@ -212,10 +214,11 @@ def test_cluster_plans(plans):
         nv = D * es // 16
         ntens = 1 if mode == 1 else 3 if mode == 3 else 2
         assert align == 1 and R > 8 and nv > (2048 if mode >= 2 else 4096), where
-        assert cl in (2, 4, 8) and nt == 512 and v in (2, 4), where
+        assert cl in (2, 4, 8) and v in (2, 4) and nt % 32 == 0, where
         assert cl_cols * es % 16 == 0, where
         slice_v = cl_cols * es // 16
-        assert slice_v <= v * nt and (v == 2 or slice_v > 2 * nt), where
+        assert (v == 2) == (slice_v <= 1280) and nt <= (640 if v == 2 else 512), where
+        assert slice_v <= v * nt < slice_v + 32 * v, where  # the CTA fits its slice
         assert cl * slice_v >= nv and (cl - 1) * slice_v < nv, where
         assert sb == cl_cols * es, where
         assert 3 <= stages <= 8 and smem == 1024 + stages * ntens * sb, where
@@ -224,4 +227,7 @@ def test_cluster_plans(plans):
         assert smem + RESERVED_PER_CTA <= SMEM_PER_SM and smem <= SMEM_PER_CTA, where
         assert ntiles == R and grid % cl == 0 and grid // cl == min(R, SM // cl), where
         assert ntens * sb <= TX_LIMIT, where
+        fitting = [c for c in (2, 4, 8) if -(-nv // c) <= 2048
+                   and (225 * 1024) // (ntens * -(-nv // c) * 16) >= 3]
+        assert cl == max(fitting, key=lambda c: (min(R, SM // c) * c, -c)), where
     assert n > 30
