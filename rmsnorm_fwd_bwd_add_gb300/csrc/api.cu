@@ -245,14 +245,16 @@ int align_of(std::initializer_list<const Mat *> ms, const void *w, const void *r
 }
 
 // Whether a forward plan takes its tiles from counters: the CTA-per-row
-// staged forwards (aligned rows, not shifted ones) whose rows take long
-// enough.  A claim is an L2 atomic whose round trip, with HBM saturated,
+// staged forwards of CLAIM_MIN_NT threads or more on dense aligned rows whose
+// rows take long enough.  A claim is an L2 atomic whose round trip, with HBM saturated,
 // outlasts a short row: claims lost time wherever a CTA's row moved less than
 // ~96 KB per SM (GB300, bf16 with residual, rows 16384: D = 4096 (two CTAs an
 // SM) -3 %, 8192 +-0; 8192 x 4096 fp16 without residual -20 %) and won it
 // above (D = 16384 with residual, 128 KB: 6310 -> 6677 GB/s).
-bool claims_tiles(const Plan &p, int mode, int64_t D, int es, int sm_count) {
-    if (p.tier != TIER_STAGED || p.shift || p.g != p.nt || is_vjp(mode)) return false;
+bool claims_tiles(const Plan &p, int mode, int64_t D, int es, int align, int sm_count) {
+    if (p.tier != TIER_STAGED || p.shift || p.g != p.nt || is_vjp(mode) || align != ALIGN_VEC ||
+        p.nt < CLAIM_MIN_NT)
+        return false;
     const size_t row_traffic = (size_t)D * es * (mode == MODE_FWD_RES ? 4 : 2);
     const size_t per_sm = row_traffic * (size_t)std::max(1, p.grid / std::max(1, sm_count));
     return per_sm >= CLAIM_MIN_ROW_TRAFFIC;
@@ -496,7 +498,7 @@ int rmsnorm_fwd_ex(const void *x, int64_t ld_x, const void *residual, int64_t ld
     a.ld_out1 = new_residual ? mn.ld : 0;
     a.partials = nullptr;
     a.rstd = rstd;
-    if (claims_tiles(p, mode, D, es, dev.sm_count)) {
+    if (claims_tiles(p, mode, D, es, align, dev.sm_count)) {
         a.tile_ctr = tile_counter(dev, static_cast<cudaStream_t>(stream));
         // as many groups as divide the grid, up to the tuned or default number
         int k = planner::tuning().claim_k;
@@ -644,8 +646,9 @@ const char *rmsnorm_describe_dispatch(int op, int64_t rows, int64_t D, int dtype
     std::snprintf(buf, sizeof(buf), "%s%s:cfg%d:nt%d:g%d:v%d:s%d:tr%d:grid%d:smem%zu:cl%d%s",
                   tier_name(p.tier), p.shift ? "-shift" : "", p.cfg, p.nt, p.g, p.v, p.stages,
                   p.tile_rows, p.grid, p.smem, p.cl,
-                  claims_tiles(p, mode, D, es, dev.sm_count) && planner::tuning().claim ? ":claim"
-                                                                                        : "");
+                  claims_tiles(p, mode, D, es, align, dev.sm_count) && planner::tuning().claim
+                      ? ":claim"
+                      : "");
     return buf;
 }
 

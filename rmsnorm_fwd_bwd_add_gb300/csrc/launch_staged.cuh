@@ -9,11 +9,11 @@
 
 namespace rmsn {
 
-template <typename T, int MODE, int NT, int G, int V, bool GEN, bool SH>
+template <typename T, int MODE, int NT, int G, int V, bool GEN, bool SH, bool CLAIM = false>
 cudaError_t launch_staged_inst(const Plan &p, const KernelArgs &a, cudaStream_t stream) {
     constexpr int MINB = staged_max_ctas_per_sm(MODE, NT, G, V);
     static std::atomic<uint64_t> smem_mask{0};
-    auto kern = staged_kernel<T, MODE, NT, G, V, MINB, GEN, SH>;
+    auto kern = staged_kernel<T, MODE, NT, G, V, MINB, GEN, SH, CLAIM>;
     cudaError_t e = allow_max_dynamic_smem((const void *)kern, smem_mask);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.grid), dim3(NT), p.smem, stream, a);
@@ -41,6 +41,11 @@ cudaError_t launch_staged_general(const Plan &p, const KernelArgs &a, cudaStream
     if constexpr (input_tensors(MODE) >= 2) gen = gen || a.ld_in1 != D;
     if constexpr (input_tensors(MODE) == 3) gen = gen || a.ld_in2 != D;
     if constexpr (MODE == MODE_FWD_RES) gen = gen || a.ld_out1 != D;
+    // The dense CTA-per-row forwards of at least CLAIM_MIN_NT threads have a
+    // claimed-tiles instance, launched when the call hands them counters.
+    if constexpr (!is_vjp(MODE) && G == NT && NT >= CLAIM_MIN_NT)
+        if (!gen && a.tile_ctr)
+            return launch_staged_inst<T, MODE, NT, G, V, false, false, true>(p, a, stream);
     if (!gen) return launch_staged_inst<T, MODE, NT, G, V, false, false>(p, a, stream);
     if constexpr (G == NT) {
         return launch_staged_inst<T, MODE, NT, G, V, true, false>(p, a, stream);

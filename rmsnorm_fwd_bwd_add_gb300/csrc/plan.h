@@ -63,6 +63,9 @@ struct KernelArgs {
 constexpr int CLAIM_MAX_K = 8;
 constexpr int CLAIM_STRIDE = 4;
 constexpr int CLAIM_WORDS = CLAIM_STRIDE * (CLAIM_MAX_K + 1);
+// Staged configurations that can claim tiles: CTA per row, this many
+// threads or more (the rows long enough for a claim to pay).
+constexpr int CLAIM_MIN_NT = 768;
 
 struct Plan {
     int tier;

@@ -64,7 +64,7 @@ inline size_t smem_per_cta(int cps) {
 
 
 // Overrides of the staged tier's choices, read once from RMSNORM_TUNE
-// ("cfg=N,cps=N,stages=N,tmap=0,claim=0,claimk=N", any subset) for tuning sweeps and for
+// ("cfg=N,cps=N,stages=N,tmap=0,claim=0,claimk=N,cl=N", any subset) for tuning sweeps and for
 // testing the per-row copy path that strided sub-warp tiles take where no
 // tensor map can be made.  Unset, the plan is a pure function of the problem
 // and the device.
@@ -75,6 +75,7 @@ struct Tuning {
     bool tmap = true; // tensor maps for strided sub-warp tiles
     bool claim = true; // staged forwards: tiles claimed at run time
     int claim_k = 1;  // claim groups (a power of two up to CLAIM_MAX_K)
+    int cl = 0;       // cluster tier: CTAs per cluster (2, 4 or 8)
 };
 
 inline Tuning parse_tuning() {
@@ -90,6 +91,7 @@ inline Tuning parse_tuning() {
         else if (std::sscanf(tok, "stages=%d", &v) == 1 && v >= 2 && v <= MAX_STAGES) t.stages = v;
         else if (std::sscanf(tok, "tmap=%d", &v) == 1) t.tmap = v != 0;
         else if (std::sscanf(tok, "claim=%d", &v) == 1) t.claim = v != 0;
+        else if (std::sscanf(tok, "cl=%d", &v) == 1 && (v == 2 || v == 4 || v == 8)) t.cl = v;
         else if (std::sscanf(tok, "claimk=%d", &v) == 1 && v >= 1 && v <= CLAIM_MAX_K &&
                  (v & (v - 1)) == 0)
             t.claim_k = v;
@@ -228,6 +230,7 @@ inline bool plan_cluster(int mode, int64_t rows, int D, int esize, const int *ca
     int best_cl = 0;
     int64_t best = 0;
     for (int cl : {2, 4, 8}) {
+        if (tuning().cl && cl != tuning().cl) continue;
         const int64_t slice = ceil_div(nv, cl);  // vectors of one CTA's slice
         if (slice > 4 * CLUSTER_NT_V4) continue;
         if ((int64_t)SMEM_ONE_PER_SM / ((int64_t)ntens * slice * 16) < 3) continue;

@@ -45,7 +45,7 @@
 
 namespace rmsn {
 
-template <typename T, int MODE, int NT, int G, int V, int MINB, bool GEN, bool SH>
+template <typename T, int MODE, int NT, int G, int V, int MINB, bool GEN, bool SH, bool CLAIM>
 __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant__ KernelArgs a) {
     constexpr int NWARPS = NT / 32;
     constexpr int WP = NWARPS <= 4 ? 4 : NWARPS <= 8 ? 8 : NWARPS <= 16 ? 16 : 32;
@@ -127,8 +127,9 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     // not depend on which CTA takes a row.  Not the VJP (a CTA's gw partial
     // row sums a fixed set of rows, which keeps gw's bits fixed), nor shifted
     // rows (a CTA's columns follow its rows' offset), nor tiles copied row by
-    // row.
-    constexpr bool DYN_OK = !VJP && !SH && !SPREAD_COPIES;
+    // row; and only in the CLAIM instances, so that the others run the static
+    // loop with none of this compiled in (it cost the D = 8192 forward 2.5 %).
+    constexpr bool DYN_OK = CLAIM && !VJP && !SH && !SPREAD_COPIES;
     const bool dyn = DYN_OK && a.tile_ctr != nullptr;
     const int CK = dyn ? a.claim_k : 1;                       // groups (counters)
     const int64_t c_home = (int64_t)blockIdx.x % CK;          // this CTA's group
