@@ -144,7 +144,10 @@ int rmsnorm_fwd(const void *x, const void *residual, const void *w, float eps,
  * allocation failure returns RMSNORM_ERR_NO_MEMORY.  No [rows, D] temporary
  * is ever allocated.  A call that runs as a single CTA (one row) writes its one
  * partial row straight into gw when gw is 16-byte aligned: no scratch, one
- * kernel, the same bits.
+ * kernel, the same bits.  A decode-sized call of 2-8 rows (16-byte aligned
+ * rows of up to 2048 vectors) runs as one thread-block cluster of its rows
+ * that adds the rows' contributions in row order itself and, with gw 16-byte
+ * aligned, writes gw directly: no scratch, one kernel.
  */
 int rmsnorm_vjp(const void *x, const void *w, const void *g, float eps,
                 float weight_bias, void *gx, float *gw, int64_t rows, int64_t D,

@@ -280,7 +280,11 @@ unsigned long long *tile_counter(const DevInfo &d, cudaStream_t s) {
 }
 
 // gw partial rows of a VJP plan: one per CTA, or one per cluster.
-int partial_rows(const Plan &p) { return p.tier == TIER_CLUSTER ? p.grid / p.cl : p.grid; }
+int partial_rows(const Plan &p) {
+    return p.tier == TIER_CLUSTER                ? p.grid / p.cl
+           : (p.tier == TIER_DIRECT && p.cl > 1) ? 1  // the cluster sums its rows itself
+                                                   : p.grid;
+}
 
 size_t partials_bytes(const Plan &p, int64_t D) {
     const size_t b = (size_t)partial_rows(p) * (size_t)D * sizeof(float);

@@ -339,6 +339,17 @@ __device__ __forceinline__ void dsmem_store_async_f2(uint32_t addr, float2 v, ui
         : "memory");
 }
 
+// 16-byte load from a shared::cluster address (this or another CTA of the
+// cluster).
+__device__ __forceinline__ float4 dsmem_load_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // One arrival on an mbarrier in another CTA of the cluster, ordered after
 // this thread's earlier (shared::cluster) writes.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {

@@ -7,7 +7,13 @@
 // ring.  Each thread owns V 16-byte vectors of the row (eight fp16/bf16 or
 // four fp32 elements each, fixed across rows); the sum of squares is a warp shuffle tree plus the warp totals added
 // in warp order through shared memory.  The VJP keeps its gw contributions in
-// registers and writes one partial row per CTA.
+// registers and writes one partial row per CTA -- or, launched as one
+// thread-block cluster of a decode step's rows (CGW), sums the CTAs'
+// contributions itself: each CTA leaves its row's contribution in its shared
+// memory, and after the cluster barrier each CTA adds, for its share of the
+// columns, every CTA's contribution in rank order (distributed shared memory)
+// and writes gw; a second cluster barrier keeps every contribution in place
+// until all are read.  One kernel per decode VJP, with no scratch.
 //
 // Sources: "Fused residual-add RMSNorm and fused RoPE + KV-append decode
 // kernels", Background (FusedAddRMSNorm; the decode loop runs it once per
@@ -20,7 +26,7 @@
 
 namespace rmsn {
 
-template <typename T, int MODE, int NT, int V>
+template <typename T, int MODE, int NT, int V, bool CGW = false>
 __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
     constexpr int NWARPS = NT / 32;
     constexpr int NTENS = input_tensors(MODE);
@@ -158,7 +164,33 @@ __global__ void __launch_bounds__(NT) direct_kernel(const KernelArgs a) {
     }
 
     griddep_launch_dependents();
-    if constexpr (VJP) {
+    if constexpr (VJP && CGW) {
+        // One row per CTA, gridDim.x CTAs in one cluster: gw = the sum of the
+        // CTAs' contributions, in rank order, written to a.partials (gw).
+        extern __shared__ __align__(16) float part[];  // [D]
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int vi = tid + j * NT;
+            if (vi < NV) {
+#pragma unroll
+                for (int u = 0; u < E / 4; ++u)
+                    reinterpret_cast<float4 *>(part + (size_t)vi * E)[u] = make_float4(
+                        acc[j][4 * u], acc[j][4 * u + 1], acc[j][4 * u + 2], acc[j][4 * u + 3]);
+            }
+        }
+        cluster_sync_all();  // every CTA's contribution is in place and visible
+        const int ncta = (int)gridDim.x;
+        const int rank = (int)cluster_rank();
+        for (int q4 = rank * NT + tid; q4 < D / 4; q4 += ncta * NT) {
+            float4 s = dsmem_load_f4(dsmem_addr(part + 4 * q4, 0u));
+            for (int c = 1; c < ncta; ++c) {
+                const float4 t = dsmem_load_f4(dsmem_addr(part + 4 * q4, (uint32_t)c));
+                s = make_float4(s.x + t.x, s.y + t.y, s.z + t.z, s.w + t.w);
+            }
+            reinterpret_cast<float4 *>(a.partials)[q4] = s;
+        }
+        cluster_sync_all();  // no CTA leaves while another may still read its part[]
+    } else if constexpr (VJP) {
         float *prow = a.partials + (size_t)blockIdx.x * D;
 #pragma unroll
         for (int j = 0; j < V; ++j) {

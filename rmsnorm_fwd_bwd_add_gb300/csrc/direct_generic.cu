@@ -35,6 +35,15 @@ namespace {
 
 template <typename T, int MODE, int NT, int V>
 cudaError_t direct_one(const Plan &p, const KernelArgs &a, cudaStream_t s) {
+    if constexpr (is_vjp(MODE)) {
+        if (p.cl > 1) {  // a decode step's rows as one cluster that sums gw itself
+            static std::atomic<uint64_t> smem_mask{0};
+            auto kern = direct_kernel<T, MODE, NT, V, true>;
+            cudaError_t e = allow_max_dynamic_smem((const void *)kern, smem_mask);
+            if (e != cudaSuccess) return e;
+            return launch_pdl_cluster(kern, dim3(p.grid), dim3(NT), p.smem, s, p.cl, a);
+        }
+    }
     return launch_pdl(direct_kernel<T, MODE, NT, V>, dim3(p.grid), dim3(NT), 0, s, a);
 }
 

@@ -307,6 +307,12 @@ inline Plan make_plan(int mode, int64_t rows, int D, int esize, int align, int s
                 p.num_tiles = rows;
                 const int64_t resident = std::max(1, 2048 / c.nt);
                 p.grid = (int)std::min<int64_t>(rows, (int64_t)sm_count * resident);
+                // A decode VJP of 2-8 rows runs as one cluster of its rows,
+                // which sums gw itself: no partial rows, no second kernel.
+                if (is_vjp(mode) && rows >= 2 && rows <= DECODE_ROWS) {
+                    p.cl = (int)rows;
+                    p.smem = (size_t)D * sizeof(float);
+                }
                 return p;
             }
         }

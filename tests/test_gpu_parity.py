@@ -148,6 +148,31 @@ def test_edge_shapes(rows, D, dtype):
     check_vjp(case, rounded_h(want_h, dtype), conditioned=True)
 
 
+@pytest.mark.parametrize("rows,D,dtype", [(2, 2048, torch.bfloat16), (3, 4096, torch.float16),
+                                          (5, 8192, torch.bfloat16), (7, 16384, torch.bfloat16),
+                                          (8, 1024, torch.float32)],
+                         ids=lambda v: str(v).replace("torch.", ""))
+def test_decode_vjp_as_one_cluster(rows, D, dtype):
+    """A decode VJP of 2-8 rows runs as one cluster of its rows that sums gw
+    itself (plan ":cl<rows>", one kernel): gx and gw against the oracle, gw
+    bit for bit across calls, and the same result with gw off a 16-byte
+    boundary (one scratch row, then the fixed-order stage 2 of that row)."""
+    case = W.random_case(rows, D, dtype, seed=rows * 1000 + D, residual=False, weight_bias=1.0)
+    plan = rn.rmsnorm_describe_dispatch("vjp", rows, D, dtype)
+    assert plan.startswith("direct") and plan.endswith(":cl%d" % rows), plan
+    x = _dev(case.x)
+    gx, gw = check_vjp(case, case.x)
+    gw2 = rn.rmsnorm_vjp(x, _dev(case.w), _dev(case.g), case.eps, case.weight_bias)[1]
+    assert torch.equal(gw.view(torch.int32), gw2.view(torch.int32))
+    buf = torch.empty(D + 8, dtype=torch.float32, device=DEV)
+    gw_off = buf[1:1 + D]  # 4 bytes past a 16-byte boundary
+    assert gw_off.data_ptr() % 16 != 0
+    gx3 = torch.empty_like(x)
+    rn.rmsnorm_vjp(x, _dev(case.w), _dev(case.g), case.eps, case.weight_bias, gx=gx3, gw=gw_off)
+    assert torch.equal(gx3, gx)
+    assert torch.equal(gw_off.view(torch.int32), gw.view(torch.int32))
+
+
 def test_empty_rows():
     x = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
     w = torch.ones(64, dtype=torch.bfloat16, device=DEV)

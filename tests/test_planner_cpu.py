@@ -76,6 +76,11 @@ def test_tiers_and_configurations(plans):
             assert tier == 3, (mode, es, D, R)  # a cluster of CTAs per row
         elif R <= 8 and nv <= (2048 if vjp else 4096):
             assert tier == 1, (mode, es, D, R)
+            # a decode VJP of 2-8 rows: one cluster of its rows sums gw itself
+            if vjp and R >= 2:
+                assert cl == R and smem == D * 4 and grid == R, (mode, es, D, R)
+            else:
+                assert cl == 0, (mode, es, D, R)
         else:
             assert tier == 2, (mode, es, D, R)
 
