@@ -6,15 +6,19 @@
 // rows c, c + clusters, ..., a static assignment).  CTA `rank` of the cluster
 // owns the contiguous column slice [rank * C, rank * C + C) of every row and
 // streams that slice through its own ring with the 1-D TMA bulk copy, exactly
-// as the staged kernels stream whole rows.  Per row, each CTA reduces its
-// slice (warp shuffle tree, then the warp totals), writes the slice's
-// (sum h^2, dot) into its slot of every cluster CTA's shared memory
-// (distributed shared memory) and arrives on their mbarriers; each CTA then
-// adds the CL slots in rank order, so every CTA of the cluster forms the same
-// row sums, bit for bit, whatever order the slots arrived in.  A CTA's
-// columns never change, so its w' and its gw contributions stay in
-// registers; the cluster writes one gw partial row (one per cluster), summed
-// in a fixed order by the same stage-2 kernel as the other tiers.
+// as the staged kernels stream whole rows; the CTA is sized to its slice.
+// Per row, each CTA reduces its slice (warp shuffle tree, then warp 0 sums
+// the warp totals in one fixed order) and warp 0 writes the slice's
+// (sum h^2, dot) into its slot of every cluster CTA's shared memory with an
+// asynchronous store (st.async) that completes 8 bytes on that CTA's slot
+// mbarrier, which each CTA arms once per row for all CL slots.  (A release
+// arrival instead would make the sender wait, every row, for its own earlier
+// global stores to be acknowledged.)  Each CTA then adds the CL slots in rank
+// order, so every CTA of the cluster forms the same row sums, bit for bit,
+// whatever order the slots arrived in.  A CTA's columns never change, so its
+// w' and its gw contributions stay in registers; the cluster writes one gw
+// partial row (one per cluster), summed in a fixed order by the same stage-2
+// kernel as the other tiers.
 //
 // Every wait is bounded.  On a timeout the CTA flags it, waits (bounded) for
 // its own copies in flight, and before it exits arrives on every cluster
