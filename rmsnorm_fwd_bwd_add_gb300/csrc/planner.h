@@ -11,10 +11,9 @@
 //   * rows <= DECODE_ROWS (decode: one token per sequence)  -> direct tier;
 //   * D <= 16384 -> staged tier (TMA bulk ring): sub-warp/warp per row for
 //     D <= 1024, CTA per row above;
-//   * longer aligned rows -> direct tier (forward up to 4096 vectors: one CTA
-//     per row, the row in registers), then the cluster tier (2-8 CTAs per
-//     row, each streaming a slice of up to 2048 vectors, four stages of which
-//     fit one SM), then generic;
+//   * longer aligned rows -> the cluster tier (2-8 CTAs per row, one per SM,
+//     each streaming a slice of up to 2048 vectors through a ring of three to
+//     eight stages), then generic;
 //   * rows <= DECODE_ROWS of up to 4096 (forward) / 2048 (VJP) vectors ->
 //     direct tier.
 #pragma once
@@ -210,7 +209,7 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
 }
 
 // Cluster plan for aligned rows longer than the staged and direct tiers take
-// (VJP: more than 2048 vectors, forward: more than 4096): clusters of 2, 4 or
+// (more than 2048 vectors): clusters of 2, 4 or
 // 8 CTAs, one per SM, each CTA's slice a whole number of vectors (at most
 // 2048) and each CTA sized to its slice, threads rounded up to a warp: two
 // vectors a thread up to CLUSTER_NT_V2 threads, else four.  A CTA of 512
@@ -290,7 +289,12 @@ inline Plan make_plan(int mode, int64_t rows, int D, int esize, int align, int s
                 best = ci;
         if (best >= 0 && plan_staged(mode, rows, D, esize, sm_count, best, shift, &p)) return p;
     }
-    if (align == ALIGN_VEC && rows > DECODE_ROWS && nv > (is_vjp(mode) ? 2048 : 4096) &&
+    // Rows of more than 2048 vectors: the cluster tier, forward and VJP.  The
+    // forwards of 2049-4096 vectors ran 17-40 % slower on the direct tier
+    // (a row in one CTA's registers; GB300, same buffers back to back, bf16
+    // 4096 x 24576 with residual 5218 -> 6114 GB/s, without 4156 -> 5624, fp16
+    // 8192 x 20480 without 3930 -> 5517, fp32 4096 x 12288 5125 -> 6163).
+    if (align == ALIGN_VEC && rows > DECODE_ROWS && nv > 2048 &&
         plan_cluster(mode, rows, D, esize, cluster_cap, sm_count, &p))
         return p;
     if (aligned) {

@@ -70,8 +70,6 @@ def test_tiers_and_configurations(plans):
             fits = [c for c, (_, _, _, mx) in cfgs.items() if c != WIDE and nv <= mx]
             assert cfg == min(fits, key=lambda c: cfgs[c][3]), (D, es, cfg)
             assert (nt, g, v, max_nv) == cfgs[cfg]
-        elif R > 8 and not vjp and nv <= 4096:
-            assert tier == 1, (mode, es, D, R)  # the row in one CTA's registers
         elif R > 8 and _cluster_fits(mode, nv):
             assert tier == 3, (mode, es, D, R)  # a cluster of CTAs per row
         elif R <= 8 and nv <= (2048 if vjp else 4096):
@@ -200,7 +198,7 @@ def test_shifted_plans(plans):
 
 
 def test_cluster_plans(plans):
-    """Rows of more than 2048 (VJP) or 4096 (forward) vectors: clusters of 2, 4
+    """Rows of more than 2048 vectors (forward and VJP): clusters of 2, 4
     or 8 CTAs whose slices (whole 16-byte vectors) cover the row with no CTA
     left empty, each CTA sized to its slice (two vectors a thread up to 640
     threads, else four; threads rounded up to a warp), one CTA per SM, rings
@@ -218,7 +216,7 @@ def test_cluster_plans(plans):
         where = (mode, es, D, R)
         nv = D * es // 16
         ntens = 1 if mode == 1 else 3 if mode == 3 else 2
-        assert align == 1 and R > 8 and nv > (2048 if mode >= 2 else 4096), where
+        assert align == 1 and R > 8 and nv > 2048, where
         assert cl in (2, 4, 8) and v in (2, 4) and nt % 32 == 0, where
         assert cl_cols * es % 16 == 0, where
         slice_v = cl_cols * es // 16
