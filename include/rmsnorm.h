@@ -289,12 +289,12 @@ int rmsnorm_rope_kv_append(const void *q, const void *k, const void *v,
  *   - Limit: a problem whose scratch (one fp32 row of D per partial row of
  *     the plan these pointers get) exceeds RMSNORM_VJP_NOALLOC_MAX_BYTES
  *     returns RMSNORM_ERR_UNSUPPORTED and enqueues nothing.  On a 152-SM
- *     GB300, at any row count: dense fp16/bf16 rows up to D = 65536 and fp32
- *     rows up to D = 32768 whose tensors start on 16-byte boundaries (at most
- *     912 partial rows of D <= 1536, 152 rows of D <= 16384, and one row per
- *     cluster, at most 76, beyond), and dense rows whose tensors all start at
- *     one shared offset from a boundary up to D = 16383 (fp16/bf16) or 8191
- *     (fp32).  Anything else (tensors at different offsets, strided rows off
+ *     GB300, at any row count: dense fp16/bf16 rows up to D = 131072 and fp32
+ *     rows up to D = 65536 whose tensors start on 16-byte boundaries (one
+ *     partial row per CTA of the CTA-per-row and sub-warp tiers, one per
+ *     cluster of the cluster tier: at most 10 MB), and dense rows whose
+ *     tensors all start at one shared offset from a boundary up to D = 16383
+ *     (fp16/bf16) or 8191 (fp32).  Anything else (tensors at different offsets, strided rows off
  *     boundaries, longer rows) runs on the element-at-a-time tier with
  *     max(min(rows, 8), min(2 x SMs, rows * 3 * size / 40)) partial rows,
  *     which fit while that count x D x 4 bytes <= 16 MiB (e.g. D <= 13,797

@@ -93,6 +93,26 @@ def test_noalloc_gw_bits_survive_other_calls(lib):
     assert torch.equal(bits[0], bits[1]) and torch.equal(bits[0], bits[2])
 
 
+@pytest.mark.parametrize("D,dtype", [(131072, torch.bfloat16), (65536, torch.float32)])
+def test_noalloc_longest_aligned_rows(lib, D, dtype):
+    """The longest aligned rows the array admits (16384 vectors: clusters of
+    eight CTAs, one partial row per cluster) run and match the oracle; rows one
+    vector longer run on the element-at-a-time tier, whose partial rows do not
+    fit, and are refused."""
+    from rmsnorm_fwd_bwd_add_gb300 import workloads as W
+    case = W.random_case(24, D, dtype, seed=D, residual=False, weight_bias=0.0)
+    x, w, g = case.x.to(DEV), case.w.to(DEV), case.g.to(DEV)
+    st, gx, gw = _call_noalloc(lib, x, w, g, case.eps, 0.0)
+    assert st == 0, lib.rmsnorm_status_string(st)
+    want_gx, want_gw = oracle.vjp(f64(case.x), f64(case.w), f64(case.g), case.eps, 0.0)
+    assert_close("noalloc gx D=%d" % D, gx, want_gx)
+    assert_close("noalloc gw D=%d" % D, gw, want_gw, torch.float32)
+    D2 = D + 16 // x.element_size()
+    x2 = torch.zeros(2000, D2, dtype=dtype, device=DEV)
+    st, _, _ = _call_noalloc(lib, x2, torch.ones(D2, dtype=dtype, device=DEV), x2, 1e-6, 0.0)
+    assert st == 2
+
+
 def test_noalloc_refuses_problems_beyond_its_array(lib):
     from rmsnorm_fwd_bwd_add_gb300 import _native
     # Long rows whose tensors sit at different offsets from 16-byte
