@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import rmsnorm_fwd_bwd_add_gb300 as rn
 from rmsnorm_fwd_bwd_add_gb300 import workloads as W
 from parity import (assert_close, assert_close_conditioned, f64, gx_term_magnitude, oracle_fwd,
@@ -69,6 +70,16 @@ def rounded_h(want_h, dtype):
     return torch.from_numpy(want_h).to(dtype)
 
 
+def check_fwd_unfused(case, out, xr):
+    """The fused forward normalises the unrounded fp32 sum h; the unfused graph
+    (add, round, then normalise) normalises round(h).  The two differ by at most
+    one rounding of h, so the fused output also meets the tolerance against
+    the oracle run on round(h) without a residual (the secondary check of the
+    fused op's reading)."""
+    want, _ = oracle.fwd(f64(xr), f64(case.w), case.eps, case.weight_bias)
+    assert_close(case.name + " out against the unfused graph", out, want)
+
+
 # ---- the five configurations -------------------------------------------------
 
 def test_config1_small_multiwarp_band():
@@ -84,10 +95,11 @@ def test_config1_small_multiwarp_band():
 def test_config2_decode(rows, D, gemma):
     case = W.config2(rows, D, gemma)
     assert rn.rmsnorm_describe_dispatch("fwd", rows, D, case.dtype, True).startswith("direct")
-    _, nr, want_h = check_fwd(case)
+    out, nr, want_h = check_fwd(case)
     xr = rounded_h(want_h, case.dtype)
     mismatch = (nr.cpu() != xr).sum().item()
     assert mismatch <= max(1, nr.numel() // 10000)
+    check_fwd_unfused(case, out, xr)
     check_vjp(case, xr)
 
 
@@ -101,12 +113,14 @@ def test_config3_vjp_8192x4096_fp16():
 @pytest.mark.parametrize("D", W.PREFILL_D)
 def test_config4_prefill(D):
     case = W.config4(D)
-    _, nr, want_h = check_fwd(case)
+    out, nr, want_h = check_fwd(case)
     xr = rounded_h(want_h, case.dtype)
     del want_h
     mismatch = (nr.cpu() != xr).sum().item()
     assert mismatch <= nr.numel() // 10000
     del nr
+    check_fwd_unfused(case, out, xr)
+    del out
     check_vjp(case, xr)
 
 
