@@ -221,27 +221,48 @@ inline bool plan_staged(int mode, int64_t rows, int D, int esize, int sm_count, 
 // bf16 VJP 2815 -> 3276 GB/s, D = 24576 3431 -> 4051; three: one row at a
 // time, which lets the longest slices fit: D = 32768 3210 -> 4063, 65536
 // 2198 -> 2741).  Of the fitting sizes, the one with the most SMs busy
-// (clusters the device holds at once, cap[cl], times CTAs per cluster).
+// (clusters the device holds at once, cap[cl], times CTAs per cluster); but a
+// forward whose busiest size leaves the ring three slices deep takes a size
+// with four or more if that keeps at least 94 % as many SMs busy and gives
+// each cluster at least 32 rows (GB/s, with a residual, clusters of two on
+// 152 SMs with three stages against four on 144 with five: bf16 4096 x 32768
+// 5994 -> 6475, fp32 2048 x 16384 6001 -> 6212; with fewer rows a cluster
+// the longer row chain loses: bf16 1024 x 30720 5675 -> 5609, 300 x 32768
+// 5214 -> 4250).  The VJP keeps the busiest size (bf16 4096 x 32768: 5972
+// against 4286).
 inline bool plan_cluster(int mode, int64_t rows, int D, int esize, const int *cap, int sm_count,
                          Plan *p) {
     const int64_t nv = (int64_t)D * esize / 16;
     const int ntens = input_tensors(mode);
     int best_cl = 0;
     int64_t best = 0;
+    int64_t busy_of[9] = {}, depth_of[9] = {}, clusters_of[9] = {};
     for (int cl : {2, 4, 8}) {
         if (tuning().cl && cl != tuning().cl) continue;
         const int64_t slice = ceil_div(nv, cl);  // vectors of one CTA's slice
         if (slice > 4 * CLUSTER_NT_V4) continue;
-        if ((int64_t)SMEM_ONE_PER_SM / ((int64_t)ntens * slice * 16) < 3) continue;
+        const int64_t depth = (int64_t)SMEM_ONE_PER_SM / ((int64_t)ntens * slice * 16);
+        if (depth < 3) continue;
         const int64_t clusters = cap ? cap[cl] : sm_count / cl;
         if (clusters <= 0) continue;
         const int64_t busy = std::min<int64_t>(clusters, rows) * cl;
+        busy_of[cl] = busy;
+        depth_of[cl] = depth;
+        clusters_of[cl] = clusters;
         if (busy > best) {
             best = busy;
             best_cl = cl;
         }
     }
     if (!best_cl) return false;
+    if (!is_vjp(mode) && depth_of[best_cl] < 4) {
+        int alt = 0;
+        for (int cl : {2, 4, 8})
+            if (depth_of[cl] >= 4 && busy_of[cl] * 100 >= best * 94 &&
+                rows >= 32 * clusters_of[cl] && (!alt || busy_of[cl] > busy_of[alt]))
+                alt = cl;
+        if (alt) best_cl = alt;
+    }
     const int64_t per_cta_vec = ceil_div(nv, best_cl);
     *p = Plan{};
     p->tier = TIER_CLUSTER;

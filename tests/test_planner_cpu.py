@@ -205,7 +205,9 @@ def test_cluster_plans(plans):
     of at least three stages (four or more, for the pipelined loop, wherever
     they fit) in one SM's shared memory, and a grid of whole clusters
     (without a device query: SMs // cl clusters at most) of the size that
-    keeps the most SMs busy."""
+    keeps the most SMs busy, except that a forward whose busiest size leaves
+    the ring three slices deep takes a size with four or more that keeps at
+    least 94 % as many SMs busy and gives each cluster at least 32 rows."""
     _, rows = plans
     n = 0
     for (mode, es, D, R, tier, cfg, nt, g, v, max_nv, stages, tr, ntiles, grid, smem, sb,
@@ -230,7 +232,18 @@ def test_cluster_plans(plans):
         assert smem + RESERVED_PER_CTA <= SMEM_PER_SM and smem <= SMEM_PER_CTA, where
         assert ntiles == R and grid % cl == 0 and grid // cl == min(R, SM // cl), where
         assert ntens * sb <= TX_LIMIT, where
-        fitting = [c for c in (2, 4, 8) if -(-nv // c) <= 2048
-                   and (225 * 1024) // (ntens * -(-nv // c) * 16) >= 3]
-        assert cl == max(fitting, key=lambda c: (min(R, SM // c) * c, -c)), where
+        def depth(c):
+            return (225 * 1024) // (ntens * -(-nv // c) * 16)
+
+        def busy(c):
+            return min(R, SM // c) * c
+
+        fitting = [c for c in (2, 4, 8) if -(-nv // c) <= 2048 and depth(c) >= 3]
+        want = max(fitting, key=lambda c: (busy(c), -c))
+        if mode in (0, 1) and depth(want) < 4:
+            deeper = [c for c in fitting if depth(c) >= 4 and busy(c) * 100 >= busy(want) * 94
+                      and R >= 32 * (SM // c)]
+            if deeper:
+                want = max(deeper, key=lambda c: (busy(c), -c))
+        assert cl == want, where
     assert n > 30
