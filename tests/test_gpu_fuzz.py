@@ -1,0 +1,112 @@
+"""Seeded random problems across the whole dispatch space, each checked against
+the fp64 oracle on every element: row lengths from 1 to 131072 (log-uniform,
+half of them rounded to whole 16-byte vectors), 1 to 20000 rows (a quarter of
+them decode-sized), fp16, bf16 and fp32, with and without a residual,
+weight_bias 0 or 1, and the row tensors at a shared offset from a 16-byte
+boundary or at different offsets.  The forward (out, new_residual), the VJP
+(gx, gw; gw bit for bit on a second call) and the two-output VJP run on every
+problem.  The fixed edge lists elsewhere pin the tier boundaries; these
+draws land between them."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rmsnorm_fwd_bwd_add_gb300 as rn
+from rmsnorm_fwd_bwd_add_gb300 import workloads as W
+from parity import assert_close, assert_close_conditioned, f64, gx_term_magnitude
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+MAX_ELEMS = 1 << 22  # rows x D per problem: the oracle finishes each in well under a second
+
+
+def _draw(i):
+    rng = np.random.RandomState(9000 + i)
+    dtype = [torch.bfloat16, torch.float16, torch.float32][rng.randint(3)]
+    es = torch.empty(0, dtype=dtype).element_size()
+    dmax = 131072 if es == 2 else 65536
+    D = int(np.exp(rng.uniform(0.0, np.log(dmax))))
+    if rng.rand() < 0.5:  # whole 16-byte vectors
+        per = 16 // es
+        D = max(per, D - D % per)
+    D = max(1, min(D, dmax))
+    if rng.rand() < 0.25:
+        rows = int(rng.randint(1, 9))
+    else:
+        rows = int(np.exp(rng.uniform(np.log(9), np.log(20000))))
+    rows = max(1, min(rows, MAX_ELEMS // D))
+    u = rng.rand()
+    offsets = (0, 0) if u < 0.6 else (1, 1) if u < 0.75 else (3, 3) if u < 0.9 else (1, 2)
+    return dict(rows=rows, D=D, dtype=dtype, residual=bool(rng.rand() < 0.75),
+                wb=float(rng.randint(2)), eps=float([1e-5, 1e-6][rng.randint(2)]),
+                off=offsets, seed=int(rng.randint(1 << 30)))
+
+
+DRAWS = [_draw(i) for i in range(48)]
+
+
+def _ids(d):
+    return "r%d_d%d_%s_off%d%d%s" % (d["rows"], d["D"], str(d["dtype"])[6:], d["off"][0],
+                                    d["off"][1], "_res" if d["residual"] else "")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    from rmsnorm_fwd_bwd_add_gb300 import build
+    build.build()
+    rn.rmsnorm_debug_inject(-1, 0)
+    yield
+    assert rn.rmsnorm_device_status(clear=True) == 0, "a kernel reported a wait timeout"
+
+
+def _at(t, off):
+    """t's values in device memory `off` elements past a 16-byte boundary."""
+    buf = torch.empty(t.numel() + 16, dtype=t.dtype, device=DEV)
+    v = buf[off:off + t.numel()].view(t.shape)
+    v.copy_(t.to(DEV))
+    return v
+
+
+def _empty_at(shape, dtype, off):
+    n = int(np.prod(shape))
+    buf = torch.full((n + 16,), float("nan"), dtype=dtype, device=DEV)
+    return buf[off:off + n].view(shape)
+
+
+@pytest.mark.parametrize("d", DRAWS, ids=[_ids(d) for d in DRAWS])
+def test_random_problem(d):
+    rows, D, dt, (o1, o2) = d["rows"], d["D"], d["dtype"], d["off"]
+    case = W.random_case(rows, D, dt, seed=d["seed"], residual=True, weight_bias=d["wb"],
+                         eps=d["eps"])
+    case.name = _ids(d)
+    x, g = _at(case.x, o1), _at(case.g, o1)
+    res = _at(case.residual, o2) if d["residual"] else None
+    w = _at(case.w, 0)
+    out = _empty_at((rows, D), dt, o1)
+    nr = _empty_at((rows, D), dt, o2) if d["residual"] else None
+    rn.rmsnorm_fwd(x, w, case.eps, case.weight_bias, res, out=out, new_residual=nr)
+    want_out, want_h = oracle.fwd(f64(case.x), f64(case.w), case.eps, case.weight_bias,
+                                  f64(case.residual) if d["residual"] else None)
+    assert_close(case.name + " out", out, want_out)
+    if d["residual"]:
+        assert_close(case.name + " new_residual", nr, want_h)
+    # the VJP's input: the exact h rounded on the CPU, or x itself
+    xr = torch.from_numpy(want_h).to(dt) if d["residual"] else case.x
+    del out, nr, want_out, want_h
+    xd = _at(xr, o1)
+    gx = _empty_at((rows, D), dt, o1)
+    _, gw = rn.rmsnorm_vjp(xd, w, g, case.eps, case.weight_bias, gx=gx)
+    want_gx, want_gw = oracle.vjp(f64(xr), f64(case.w), f64(case.g), case.eps, case.weight_bias)
+    terms = gx_term_magnitude(xr, case.w, case.g, case.eps, case.weight_bias)
+    assert_close_conditioned(case.name + " gx", gx, want_gx, terms)
+    assert_close(case.name + " gw", gw, want_gw, torch.float32)
+    gw2 = rn.rmsnorm_vjp(xd, w, g, case.eps, case.weight_bias, gx=gx)[1]
+    assert torch.equal(gw.view(torch.int32), gw2.view(torch.int32))
+    gres = _at(case.residual, o2)
+    gh = _empty_at((rows, D), dt, o1)
+    _, gwf = rn.rmsnorm_fused_vjp(xd, w, g, case.eps, case.weight_bias, gres, g_h=gh)
+    want_gh, want_gwf = oracle.fused_vjp(f64(xr), f64(case.w), f64(case.g), case.eps,
+                                         case.weight_bias, f64(case.residual))
+    assert_close_conditioned(case.name + " g_h", gh, want_gh, terms)
+    assert_close(case.name + " fused gw", gwf, want_gwf, torch.float32)
