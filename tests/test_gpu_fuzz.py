@@ -43,7 +43,7 @@ def _draw(i):
                 off=offsets, seed=int(rng.randint(1 << 30)))
 
 
-DRAWS = [_draw(i) for i in range(48)]
+DRAWS = [_draw(i) for i in range(128)]
 
 
 def _ids(d):
