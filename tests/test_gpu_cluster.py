@@ -76,6 +76,19 @@ def test_long_rows(rows, D, dtype):
     _check(case)
 
 
+@pytest.mark.parametrize("rows,D,dtype", [(1200, 32768, torch.bfloat16), (1300, 16384, torch.float32)],
+                         ids=lambda v: str(v).replace("torch.", ""))
+def test_forward_takes_the_deeper_ring(rows, D, dtype):
+    """Rows of 4096 vectors with a residual: clusters of two would leave a
+    three-slice ring, so with at least 32 rows a cluster the forward runs in
+    clusters of four (five stages) while the VJP keeps clusters of two."""
+    case = W.random_case(rows, D, dtype, seed=rows + D, weight_bias=0.0, eps=1e-6)
+    case.name = "deeper_r%d_d%d" % (rows, D)
+    assert _plan("fwd", case, True).endswith(":cl4"), _plan("fwd", case, True)
+    assert _plan("vjp", case).endswith(":cl2"), _plan("vjp", case)
+    _check(case)
+
+
 def test_cluster_gw_under_graph_replay():
     case = W.random_case(600, 24576, torch.bfloat16, seed=5, residual=False)
     x, w, g = (t.to(DEV) for t in (case.x, case.w, case.g))
