@@ -59,10 +59,14 @@ __global__ void __launch_bounds__(NT, MINB) staged_kernel(const __grid_constant_
     // Some VJP instances re-read a row from the stage for their outputs
     // instead of holding it in registers across the reduction (a CTA-per-row
     // stage is released only at the next row's barrier): those staged_reload
-    // names, and the CTA-per-row VJPs of shifted rows, whose edge handling
-    // costs registers (D = 4097 bf16, 320 threads: 8 bytes spilled when held,
-    // 86 registers re-read; 4024 -> 4252 GB/s, 16384 rows).
-    constexpr bool RELOAD = staged_reload(MODE, NT, G, V) || (SH && is_vjp(MODE) && G == NT);
+    // names, and the CTA-per-row VJPs of shifted rows whose register cap is
+    // below 128 a thread, where the edge handling's registers would spill (D =
+    // 4097 bf16, 320 threads: 8 bytes spilled when held, 86 registers re-read;
+    // 4024 -> 4252 GB/s, 16384 rows).  With a cap of 128 they hold their rows
+    // (110-112 registers; bf16, 16384 rows, rotating buffers: D = 4097 5358 ->
+    // 5582 GB/s, D = 2052 4339 -> 4988, D = 8196 5779 -> 6165).
+    constexpr bool RELOAD = staged_reload(MODE, NT, G, V) ||
+                            (SH && is_vjp(MODE) && G == NT && NT * MINB > 512);
     constexpr int NTENS = input_tensors(MODE);
     constexpr bool VJP = is_vjp(MODE);
     constexpr bool ADD = (MODE == MODE_VJP_ADD);
