@@ -5,8 +5,11 @@ them decode-sized), fp16, bf16 and fp32, with and without a residual,
 weight_bias 0 or 1, and the row tensors at a shared offset from a 16-byte
 boundary or at different offsets.  The forward (out, new_residual), the VJP
 (gx, gw; gw bit for bit on a second call) and the two-output VJP run on every
-problem.  The fixed edge lists elsewhere pin the tier boundaries; these
-draws land between them."""
+problem.  A second set draws rows a stride apart (each tensor a slice of a
+wider buffer, at its own padding) through the general entry points, with
+the per-row scale written by the forward and supplied to the VJP on some
+draws.  The fixed edge lists elsewhere pin the tier boundaries; these draws
+land between them."""
 import numpy as np
 import pytest
 import torch
@@ -110,3 +113,89 @@ def test_random_problem(d):
                                          case.weight_bias, f64(case.residual))
     assert_close_conditioned(case.name + " g_h", gh, want_gh, terms)
     assert_close(case.name + " fused gw", gwf, want_gwf, torch.float32)
+
+
+def _draw_strided(i):
+    rng = np.random.RandomState(7000 + i)
+    dtype = [torch.bfloat16, torch.float16, torch.float32][rng.randint(3)]
+    es = torch.empty(0, dtype=dtype).element_size()
+    per = 16 // es
+    D = int(np.exp(rng.uniform(0.0, np.log(20000 if es == 2 else 10000))))
+    if rng.rand() < 0.5:
+        D = max(per, D - D % per)
+    if rng.rand() < 0.2:
+        rows = int(rng.randint(1, 9))
+    else:
+        rows = int(np.exp(rng.uniform(np.log(9), np.log(8000))))
+
+    def pad():  # elements past D in each row of a tensor's buffer
+        return int(per * rng.randint(0, 9)) if rng.rand() < 0.6 else int(rng.randint(1, 2 * per))
+    pads = dict(x=pad(), res=pad(), out=pad(), nr=pad(), g=pad(), gres=pad(), gx=pad())
+    rows = max(1, min(rows, MAX_ELEMS // (D + max(pads.values()))))
+    return dict(rows=rows, D=D, dtype=dtype, pads=pads, rstd=bool(rng.rand() < 0.5),
+                gres=bool(rng.rand() < 0.5), wb=float(rng.randint(2)),
+                eps=float([1e-5, 1e-6][rng.randint(2)]), seed=int(rng.randint(1 << 30)))
+
+
+STRIDED = [_draw_strided(i) for i in range(48)]
+
+
+def _sids(d):
+    return "r%d_d%d_%s_ld+%d%s%s" % (d["rows"], d["D"], str(d["dtype"])[6:], d["pads"]["x"],
+                                     "_rstd" if d["rstd"] else "", "_gres" if d["gres"] else "")
+
+
+def _strided(t, padding, fill=None):
+    """t's rows as a [rows, D] view into a [rows, D + padding] buffer."""
+    rows, D = t.shape
+    buf = torch.full((rows, D + padding), 7.0 if fill is None else fill, dtype=t.dtype, device=DEV)
+    v = buf[:, :D]
+    v.copy_(t.to(DEV))
+    return v, buf
+
+
+@pytest.mark.parametrize("d", STRIDED, ids=[_sids(d) for d in STRIDED])
+def test_random_strided_problem(d):
+    rows, D, dt, pads = d["rows"], d["D"], d["dtype"], d["pads"]
+    case = W.random_case(rows, D, dt, seed=d["seed"], residual=True, weight_bias=d["wb"],
+                         eps=d["eps"])
+    case.name = _sids(d)
+    w = case.w.to(DEV)
+    x, _ = _strided(case.x, pads["x"])
+    res, _ = _strided(case.residual, pads["res"])
+    out, out_buf = _strided(torch.zeros(rows, D, dtype=dt), pads["out"])
+    nr, nr_buf = _strided(torch.zeros(rows, D, dtype=dt), pads["nr"])
+    _, _, r = rn.rmsnorm_fwd_ex(x, w, case.eps, case.weight_bias, res, out=out, new_residual=nr,
+                                rstd=True if d["rstd"] else None)
+    want_out, want_h = oracle.fwd(f64(case.x), f64(case.w), case.eps, case.weight_bias,
+                                  f64(case.residual))
+    assert_close(case.name + " out", out, want_out)
+    assert_close(case.name + " new_residual", nr, want_h)
+    for buf in (out_buf, nr_buf):  # the padding is untouched
+        assert torch.all(buf[:, D:] == 7.0)
+    if d["rstd"]:
+        want_r = oracle.rstd(f64(case.x), case.eps, f64(case.residual))
+        assert_close(case.name + " rstd", r, want_r, torch.float32)
+    # the VJP on the exact h rounded on the CPU, rows a stride apart
+    xr = torch.from_numpy(want_h).to(dt)
+    del out, nr, want_out
+    xv, _ = _strided(xr, pads["x"])
+    g, _ = _strided(case.g, pads["g"])
+    gres, _ = _strided(case.residual, pads["gres"]) if d["gres"] else (None, None)
+    gx, gx_buf = _strided(torch.zeros(rows, D, dtype=dt), pads["gx"])
+    rstd32 = oracle.rstd(f64(xr), case.eps).astype(np.float32) if d["rstd"] else None
+    _, gw = rn.rmsnorm_vjp_ex(xv, w, g, case.eps, case.weight_bias, gres, gx=gx,
+                              rstd=torch.from_numpy(rstd32).to(DEV) if d["rstd"] else None)
+    if d["rstd"]:
+        want_gx, want_gw = oracle.vjp_rstd(f64(xr), f64(case.w), f64(case.g),
+                                           rstd32.astype(np.float64), case.weight_bias)
+    else:
+        want_gx, want_gw = oracle.vjp(f64(xr), f64(case.w), f64(case.g), case.eps,
+                                      case.weight_bias)
+    terms = gx_term_magnitude(xr, case.w, case.g, case.eps, case.weight_bias)
+    if d["gres"]:
+        want_gx = want_gx + f64(case.residual)
+        terms = terms + np.abs(f64(case.residual))
+    assert_close_conditioned(case.name + " gx", gx, want_gx, terms)
+    assert_close(case.name + " gw", gw, want_gw, torch.float32)
+    assert torch.all(gx_buf[:, D:] == 7.0)
