@@ -8,8 +8,9 @@ boundary or at different offsets.  The forward (out, new_residual), the VJP
 problem.  A second set draws rows a stride apart (each tensor a slice of a
 wider buffer, at its own padding) through the general entry points, with
 the per-row scale written by the forward and supplied to the VJP on some
-draws.  The fixed edge lists elsewhere pin the tier boundaries; these draws
-land between them."""
+draws.  A third set draws the gated activation's shapes and offsets.  The
+fixed edge lists elsewhere pin the tier boundaries; these draws land between
+them."""
 import numpy as np
 import pytest
 import torch
@@ -199,3 +200,30 @@ def test_random_strided_problem(d):
     assert_close_conditioned(case.name + " gx", gx, want_gx, terms)
     assert_close(case.name + " gw", gw, want_gw, torch.float32)
     assert torch.all(gx_buf[:, D:] == 7.0)
+
+
+def _draw_gated(i):
+    rng = np.random.RandomState(5000 + i)
+    dtype = [torch.bfloat16, torch.float16][rng.randint(2)]
+    d = int(np.exp(rng.uniform(0.0, np.log(16384))))
+    if rng.rand() < 0.5:
+        d = max(8, d - d % 8)
+    rows = int(np.exp(rng.uniform(0.0, np.log(5000))))
+    rows = max(1, min(rows, MAX_ELEMS // (2 * d)))
+    return dict(rows=rows, d=d, dtype=dtype, off=int([0, 0, 1, 3][rng.randint(4)]),
+                seed=int(rng.randint(1 << 30)))
+
+
+GATED = [_draw_gated(i) for i in range(24)]
+
+
+@pytest.mark.parametrize("d", GATED, ids=["r%d_d%d_%s_off%d" % (g["rows"], g["d"],
+                                                                  str(g["dtype"])[6:], g["off"])
+                                          for g in GATED])
+def test_random_gated_problem(d):
+    gen = torch.Generator().manual_seed(d["seed"])
+    x = (torch.randn(d["rows"], 2 * d["d"], generator=gen) * 3.0).to(d["dtype"])
+    xd = _at(x, d["off"])
+    out = rn.rmsnorm_gated_silu(xd)
+    assert out.shape == (d["rows"], d["d"])
+    assert_close("gated r%d d%d" % (d["rows"], d["d"]), out, oracle.gated_silu(f64(x)))
